@@ -1,0 +1,508 @@
+#!/usr/bin/env python
+"""Benchmark of the OSCAR INT2 KV-cache serving path (write path + fused paged
+decode attention) on synthetic Qwen3-shaped attention layers.
+
+A step is one decode step of one layer for the whole batch: quant_append of
+one new token per request (rotate, clip, quantise and pack the token leaving
+the recent window, ring write) followed by decode_attn (query rotation,
+split-K INT2 + BF16 attention, merge and un-rotation). Inputs are resident in
+device memory before timing starts.
+
+Default workload: Qwen3-8B layer shape (32 query / 8 KV heads, d = 128), batch
+1 at 32768 tokens. Its cache (25.6 MB) fits in L2, so the timed loop cycles
+through enough independent layer caches to exceed 4x the L2 size, as a model
+with that many layers would. The Qwen3-32B-shaped batch-28 x 100000-token
+layer (2.15 GB) is measured as well and reported under "extra".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl oscar|reference]
+
+Under torchrun each rank runs its own replica (weak scaling, no collective on
+the data path); timings are the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import WORKLOADS, draw_kv, draw_page_pool, draw_queries, draw_ragged_lengths  # noqa: E402
+
+METRIC = "paged INT2 decode-attn µs/step & HBM GB/s (% of peak), bs1@32k and bs28@100k"
+D = 128
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for name in ("decode_attn.cu", "oscar_internal.cuh"):
+        with open(os.path.join(ROOT, "bit_rotated_kv_oscar_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per decode launch from a committed ncu summary, if it was taken
+    on the current decode kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        if t.get("source_hash") != source_hash():
+            return None
+        return t.get("bytes_per_launch", {}).get(workload)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# one workload: layers, caches, inputs
+# ---------------------------------------------------------------------------
+
+class Workload:
+    def __init__(self, name, device, n_steps_total, rank=0, min_layers=None):
+        from bit_rotated_kv_oscar_gb300 import abi
+        from bit_rotated_kv_oscar_gb300.cache import PagedCache
+        from bit_rotated_kv_oscar_gb300.calibrate import calibrate
+
+        spec = WORKLOADS[name]
+        self.spec, self.name, self.device = spec, name, device
+        hq, hkv, S, W, B = spec.num_q_heads, spec.num_kv_heads, spec.sink, spec.recent, spec.batch
+        self.B = B
+        seed = spec.seed + 1000 * rank
+        self.lengths = draw_ragged_lengths(seed, B, spec.context_min, spec.context)
+        max_len = int(self.lengths.max()) + n_steps_total + 16
+        max_pages = (max_len + 15) // 16
+        # offline calibration on 2048 synthetic calibration tokens
+        q_cal = draw_queries(seed, 900, spec.calib_tokens, hq, hkv, D).numpy()
+        k_cal, v_cal = (t.numpy() for t in draw_kv(seed, 900, spec.calib_tokens, hkv, D, spec.token_spikes))
+        cal = calibrate(q_cal, k_cal, v_cal)
+        self.cfg = abi.make_config(hq, hkv, S, W, B, max_pages)
+        num_pages = B * max_pages
+        # cache bytes of one layer at the starting lengths
+        int2_tok = np.maximum(self.lengths - W, S) - S
+        per_layer = int(hkv * 96 * int2_tok.sum())
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        n_layers = 1 if per_layer > 4 * l2 else int(math.ceil(4 * l2 / max(per_layer, 1)))
+        if min_layers:
+            n_layers = max(n_layers, min_layers)
+        self.layers = []
+        for li in range(n_layers):
+            ctx = abi.Context(self.cfg)
+            ctx.load_rotations(cal["R_K"], cal["R_V"], cal["clip_K"], cal["clip_V"])
+            cache = PagedCache(ctx, num_pages, device=device,
+                               page_order=draw_page_pool(seed + li, num_pages, spec.shuffled_pages))
+            for b in range(B):
+                cache.reserve(b, max_len, upload=False)
+            cache.upload()
+            self.layers.append((ctx, cache))
+        self._populate()
+        # per-step inputs (a small ring of distinct draws, resident on the device)
+        self.n_inputs = 8
+        self.q = [draw_queries(seed, 100 + i, B, hq, hkv, D, device=device).to(torch.bfloat16)
+                  for i in range(self.n_inputs)]
+        kv = [draw_kv(seed, 100 + i, B, hkv, D, spec.token_spikes, device=device) for i in range(self.n_inputs)]
+        self.k = [a.to(torch.bfloat16).view(B, 1, hkv, D).contiguous() for a, _ in kv]
+        self.v = [b_.to(torch.bfloat16).view(B, 1, hkv, D).contiguous() for _, b_ in kv]
+        self.o = torch.empty(B, hq, D, device=device)
+        self.per_layer_bytes = per_layer
+
+    def _populate(self):
+        """Fill every request of every layer: the longest request of layer 0 goes
+        through quant_append (the product's write path) in chunks; its pages,
+        window rows and state are then copied to the other requests and layers
+        (distinct addresses, same contents)."""
+        spec, B = self.spec, self.B
+        ctx0, c0 = self.layers[0]
+        hkv = spec.num_kv_heads
+        b0 = int(np.argmax(self.lengths))
+        L0 = int(self.lengths[b0])
+        chunk = 16384
+        pos = 0
+        while pos < L0:
+            n = min(chunk, L0 - pos)
+            k, v = draw_kv(spec.seed, 10_000 + pos // chunk, n, hkv, D, spec.token_spikes, device=self.device)
+            ctx0.quant_append(c0.page_table[b0:], c0.state[b0:], k.to(torch.bfloat16).contiguous(),
+                              v.to(torch.bfloat16).contiguous(), 1, n)
+            pos += n
+        torch.cuda.synchronize()
+        pool0 = c0.pool.view(-1, hkv, 1536)
+        win0 = c0.window.view(B, hkv, 2, spec.sink + spec.recent, D)
+        st0 = c0.state[b0].clone()
+        S, W = spec.sink, spec.recent
+        src_pages = torch.as_tensor(c0.page_table_host[b0].astype(np.int64), device=self.device)
+        for li, (ctx, cache) in enumerate(self.layers):
+            pool = cache.pool.view(-1, hkv, 1536)
+            win = cache.window.view(B, hkv, 2, S + W, D)
+            for b in range(B):
+                if li == 0 and b == b0:
+                    continue
+                L = int(self.lengths[b])
+                npg = (L + 15) // 16
+                dst = torch.as_tensor(cache.page_table_host[b, :npg].astype(np.int64), device=self.device)
+                pool[dst] = pool0[src_pages[:npg]]
+                win[b].copy_(win0[b0])
+                E = max(S, L - W)
+                cache.state[b] = torch.tensor([L, E], dtype=torch.int32, device=self.device)
+        torch.cuda.synchronize()
+
+    def decode_bytes(self, extra_tokens):
+        """Algorithmic HBM bytes of one decode_attn call with every request extra_tokens longer."""
+        s = self.spec
+        L = self.lengths + extra_tokens
+        E = np.maximum(L - s.recent, s.sink)
+        n_int2 = E - s.sink
+        n_bf16 = np.minimum(L, s.sink) + (L - E)
+        pages = (E + 15) // 16
+        b = s.num_kv_heads * (96 * n_int2 + 512 * n_bf16) + 4 * pages
+        return float(b.sum() + self.B * s.num_q_heads * D * (2 + 4))
+
+    def append_bytes(self):
+        """Algorithmic HBM bytes of one single-token quant_append for the batch:
+        read the new K/V (512 B per head), read the evicted ring token (512 B),
+        write its INT2 codes + metadata (96 B) and the new ring row (512 B)."""
+        s = self.spec
+        return float(self.B * s.num_kv_heads * (512 + 512 + 96 + 512))
+
+    def step(self, i, stream, ev=None):
+        ctx, cache = self.layers[i % len(self.layers)]
+        j = i % self.n_inputs
+        if ev is not None:
+            ev[0].record(stream)
+        ctx.quant_append(cache.page_table, cache.state, self.k[j], self.v[j], self.B, 1, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ctx.decode_attn(self.q[j], cache.page_table, cache.state, self.o, self.B, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+
+def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True):
+    n_total = 2 * args.warmup + 3 * args.steps + 4096 + 64
+    wl = Workload(name, device, n_total, rank)
+    stream = torch.cuda.current_stream(device)
+    # warm-up: at least W steps and about half a second under load
+    i = 0
+    t0 = time.time()
+    sampler = ClockSampler(clocks_index)
+    sampler.start()
+    while i < args.warmup or time.time() - t0 < 0.5:
+        wl.step(i, stream)
+        i += 1
+        if i % 256 == 0:
+            torch.cuda.synchronize()
+        if i > n_total - 2 * args.steps - 2 * args.warmup - 32:
+            break
+    torch.cuda.synchronize()
+    warm_done = i
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        wl.step(i + k, stream, evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    app_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    dec_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    i += args.steps
+    if dist:
+        t = torch.tensor([total_ms, app_ms, dec_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, app_ms, dec_ms = (float(x) for x in t.tolist())
+    us_step = total_ms * 1000.0 / args.steps
+    mid = warm_done + args.steps // 2
+    dbytes = wl.decode_bytes(mid // len(wl.layers))
+    res = {
+        "workload": name, "us_per_step": us_step, "decode_us": dec_ms * 1000.0,
+        "append_us": app_ms * 1000.0, "decode_bytes": dbytes, "append_bytes": wl.append_bytes(),
+        "layers_cycled": len(wl.layers), "per_layer_bytes": wl.per_layer_bytes, "clocks": clocks,
+        "batch": wl.B, "lengths": [int(x) for x in wl.lengths[:4]],
+    }
+    if with_e2e:
+        res["e2e"] = run_e2e(wl, args, device, i, dist)
+    return res
+
+
+def run_e2e(wl, args, device, i0, dist):
+    """Same steps through the public API with host buffers: per step the new
+    q / k / v go host->device from pinned memory and o comes back."""
+    stream = torch.cuda.current_stream(device)
+    j = 0
+    hq = [t.cpu().pin_memory() for t in wl.q]
+    hk = [t.cpu().pin_memory() for t in wl.k]
+    hv = [t.cpu().pin_memory() for t in wl.v]
+    qd, kd, vd = (torch.empty_like(wl.q[0]), torch.empty_like(wl.k[0]), torch.empty_like(wl.v[0]))
+    ho = torch.empty(wl.o.shape, dtype=wl.o.dtype).pin_memory()
+    h2d = qd.numel() * 2 + kd.numel() * 2 + vd.numel() * 2
+    d2h = ho.numel() * 4
+
+    def one(k):
+        ctx, cache = wl.layers[k % len(wl.layers)]
+        j = k % wl.n_inputs
+        qd.copy_(hq[j], non_blocking=True)
+        kd.copy_(hk[j], non_blocking=True)
+        vd.copy_(hv[j], non_blocking=True)
+        ctx.quant_append(cache.page_table, cache.state, kd, vd, wl.B, 1, stream)
+        ctx.decode_attn(qd, cache.page_table, cache.state, wl.o, wl.B, stream)
+        ho.copy_(wl.o, non_blocking=True)
+
+    for k in range(max(3, args.warmup)):
+        one(i0 + k)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    base = i0 + max(3, args.warmup)
+    start.record(stream)
+    for k in range(args.steps):
+        one(base + k)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": ms * 1000.0 / args.steps, "unit": "us/step", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# ---------------------------------------------------------------------------
+
+def oracle_step_sample(name, kv_heads_in_sample=1, seed_offset=0):
+    """Time one oracle decode step (append of one token + float64 attention over
+    the whole cache) for request 0 restricted to `kv_heads_in_sample` KV heads.
+    Returns (seconds, scale) where scale converts to one full batch step."""
+    import oracle
+    from oracle import OracleCache, decode_attention, next_state
+
+    spec = WORKLOADS[name]
+    seed = spec.seed + seed_offset
+    hkv = kv_heads_in_sample
+    g = spec.gqa
+    L = int(draw_ragged_lengths(seed, spec.batch, spec.context_min, spec.context)[0])
+    q_cal = draw_queries(seed, 900, 512, g * hkv, hkv, D).numpy()
+    k_cal, v_cal = (t.numpy() for t in draw_kv(seed, 900, 512, hkv, D))
+    cal = oracle.calibrate(q_cal, k_cal, v_cal)
+    k, v = (t.numpy() for t in draw_kv(seed, 1, L + 1, hkv, D))
+    q = draw_queries(seed, 2, 1, g * hkv, hkv, D).numpy()[0]
+    L0, E0 = next_state(0, spec.sink, L, spec.recent, spec.sink)
+    cache = OracleCache(cal["R_K32"], cal["R_V32"], cal["clip_K32"], cal["clip_V32"], spec.sink)
+    cache.build(k, v, L0, E0)
+    t0 = time.perf_counter()
+    # the appended token evicts one ring entry: rotate + quantise it (K and V), then attend
+    p = max(E0, spec.sink)
+    for x, r, c in ((k, cal["R_K32"], cal["clip_K32"]), (v, cal["R_V32"], cal["clip_V32"])):
+        xr = np.einsum("nhi,hij->nhj", x[p:p + 1].astype(np.float64), r.astype(np.float64))
+        oracle.quantize_groups(xr.astype(np.float32), c.reshape(1, -1, 1))
+    decode_attention(q, cache)
+    dt = time.perf_counter() - t0
+    scale = spec.batch * spec.num_kv_heads / hkv
+    return dt, scale
+
+
+def run_reference(args, name, rank):
+    """The oracle as the reference arm: each step one bounded sample."""
+    cores = os.cpu_count()
+    times = []
+    for k in range(args.warmup + args.steps):
+        dt, scale = oracle_step_sample(name, 1, seed_offset=k)
+        if k >= args.warmup:
+            times.append(dt * scale)
+    us = float(np.mean(times)) * 1e6
+    sample = "per step: 1 of %d KV heads of request 0 (oracle decode step: append + float64 attention " \
+             "over the whole cache), scaled to the full batch" % WORKLOADS[name].num_kv_heads
+    return {
+        "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference", "config": {"workload": name},
+        "cpu_baseline": {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_bs1_32k")
+    ap.add_argument("--extra", default="qwen3_32b_bs28_100k", help="second workload ('' to skip)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, args.workload, rank)))
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from bit_rotated_kv_oscar_gb300 import build as _b
+    if rank == 0 or not os.path.exists(_b.LIB):
+        _b.build()
+    if dist:
+        dist.barrier()
+    peak, peak_kind = peaks()
+    main_res = run_oscar(args.workload, args, device, rank, world, dist, local)
+    extras = []
+    if args.extra:
+        for name in args.extra.split(","):
+            r = run_oscar(name, args, device, rank, world, dist, local, with_e2e=False)
+            extras.append(r)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        dt, scale = oracle_step_sample(args.workload, 2)
+        cpu = {"value": dt * scale * 1e6, "unit": "us/step", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": "one decode step (append + float64 attention over the whole cache) of KV heads "
+                         "0-1 of request 0, scaled to all %d KV heads x %d requests" %
+                         (WORKLOADS[args.workload].num_kv_heads, WORKLOADS[args.workload].batch)}
+
+    def roof(r):
+        achieved = r["decode_bytes"] / (r["decode_us"] * 1e-6) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(r["workload"]),
+                "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                "kernel": "decode_attn call (rotate_q + decode + merge launches)",
+                "algorithmic_bytes_per_launch": r["decode_bytes"]}
+
+    if rank == 0:
+        spec = WORKLOADS[args.workload]
+        out = {
+            "metric": METRIC, "value": round(main_res["us_per_step"], 3), "unit": "us/step",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(main_res["us_per_step"] / 1000.0, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": spec.batch, "context": spec.context,
+                       "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "head_dim": D,
+                       "page": spec.page_size, "group": spec.group_size, "sink": spec.sink,
+                       "recent": spec.recent, "parallelism": "replicas x%d" % world,
+                       "l2": "inputs larger than L2: %d independent layer caches cycled" % main_res["layers_cycled"]},
+            "decode_us": round(main_res["decode_us"], 3), "append_us": round(main_res["append_us"], 3),
+            "decode_gbs": round(main_res["decode_bytes"] / (main_res["decode_us"] * 1e-6) / 1e9, 1),
+            "roofline": roof(main_res),
+            "cpu_baseline": cpu,
+            "e2e": main_res["e2e"],
+            "gpu_launches": 4 * args.steps,
+            "clocks": main_res["clocks"],
+            "extra": [],
+        }
+        for r in extras:
+            out["extra"].append({
+                "workload": r["workload"], "us_per_step": round(r["us_per_step"], 3),
+                "decode_us": round(r["decode_us"], 3), "append_us": round(r["append_us"], 3),
+                "decode_gbs": round(r["decode_bytes"] / (r["decode_us"] * 1e-6) / 1e9, 1),
+                "roofline": roof(r), "clocks": r["clocks"], "layers_cycled": r["layers_cycled"],
+            })
+        print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,93 @@
+"""Offline calibration of one layer's fixed rotations and clip values.
+
+Host setup, run once per layer before serving (not part of the per-token
+path). Written with torch float64 on the CPU.
+
+Steps ("OSCAR: Offline Spectral Covariance-Aware Rotation ..." (gist.science,
+it), Riepilogo Tecnico 2.2 A; "Juntos, AI Open-Sources OSCAR ..." (7minutos.es),
+section "Lo que OSCAR hace diferente"):
+  C_Q = (1/N) sum q_n^T q_n and C_S = (1/N) V^T S^T S V per KV head (averaged
+  over the head's query heads, S the causal scores at scale 1/sqrt(d));
+  eigenbases U_Q, U_S with eigenvalues in descending order (each eigenvector's
+  largest entry positive); R = U H P with H the orthonormal Sylvester
+  Hadamard matrix and P the bit-reversal permutation; one clip per layer at a
+  percentile of |x R| over the calibration activations.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+
+def _hadamard(d: int) -> torch.Tensor:
+    h = torch.tensor([[1.0]], dtype=torch.float64)
+    base = torch.tensor([[1.0, 1.0], [1.0, -1.0]], dtype=torch.float64)
+    while h.shape[0] < d:
+        h = torch.kron(base, h)
+    return h / d ** 0.5
+
+
+def _bit_reversal(d: int) -> torch.Tensor:
+    bits = d.bit_length() - 1
+    idx = torch.arange(d)
+    rev = torch.zeros(d, dtype=torch.long)
+    for k in range(bits):
+        rev |= ((idx >> k) & 1) << (bits - 1 - k)
+    p = torch.zeros(d, d, dtype=torch.float64)
+    p[idx, rev] = 1.0
+    return p
+
+
+def _eigvecs_desc(c: torch.Tensor) -> torch.Tensor:
+    w, u = torch.linalg.eigh(c)
+    order = torch.argsort(w, descending=True, stable=True)
+    u = u[:, order]
+    piv = u.abs().argmax(dim=0)
+    sgn = torch.sign(u[piv, torch.arange(u.shape[1])])
+    sgn[sgn == 0] = 1
+    return u * sgn
+
+
+def _percentile(x: torch.Tensor, pct: float) -> float:
+    # linear interpolation between order statistics
+    v = torch.sort(x.reshape(-1)).values
+    pos = (v.numel() - 1) * pct / 100.0
+    lo = int(np.floor(pos))
+    hi = min(lo + 1, v.numel() - 1)
+    return float(v[lo] + (v[hi] - v[lo]) * (pos - lo))
+
+
+def calibrate(q_cal, k_cal, v_cal, percentile: float = 99.9, scale: float | None = None) -> dict:
+    """q_cal [N, Hq, d], k_cal / v_cal [N, Hkv, d] -> float32 R_K, R_V [Hkv, d, d], clip_K, clip_V [Hkv]."""
+    q = torch.as_tensor(q_cal).to(torch.float64)
+    k = torch.as_tensor(k_cal).to(torch.float64)
+    v = torch.as_tensor(v_cal).to(torch.float64)
+    n, hq, d = q.shape
+    hkv = k.shape[1]
+    g = hq // hkv
+    if scale is None:
+        scale = d ** -0.5
+    hp = _hadamard(d) @ _bit_reversal(d)
+    causal = torch.ones(n, n, dtype=torch.bool).triu(1)
+    r_k = torch.empty(hkv, d, d, dtype=torch.float64)
+    r_v = torch.empty(hkv, d, d, dtype=torch.float64)
+    for h in range(hkv):
+        cq = torch.zeros(d, d, dtype=torch.float64)
+        cs = torch.zeros(d, d, dtype=torch.float64)
+        for j in range(h * g, (h + 1) * g):
+            qj = q[:, j]
+            cq += qj.T @ qj / n
+            logits = (qj @ k[:, h].T * scale).masked_fill(causal, float("-inf"))
+            sv = torch.softmax(logits, dim=1) @ v[:, h]
+            cs += sv.T @ sv / n
+        r_k[h] = _eigvecs_desc(cq / g) @ hp
+        r_v[h] = _eigvecs_desc(cs / g) @ hp
+    clip_k = _percentile(torch.einsum("nhi,hij->nhj", k, r_k).abs(), percentile)
+    clip_v = _percentile(torch.einsum("nhi,hij->nhj", v, r_v).abs(), percentile)
+    return {
+        "R_K": r_k.to(torch.float32).numpy(),
+        "R_V": r_v.to(torch.float32).numpy(),
+        "clip_K": np.full(hkv, clip_k, dtype=np.float32),
+        "clip_V": np.full(hkv, clip_v, dtype=np.float32),
+    }

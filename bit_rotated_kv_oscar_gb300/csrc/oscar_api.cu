@@ -1,0 +1,361 @@
+// C ABI of liboscar: context, validation, workspace and kernel launches.
+// The statement of every entry point is in include/oscar.h.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <string>
+#include <vector>
+
+#include "oscar_internal.cuh"
+
+using namespace oscar;
+
+struct oscar_ctx {
+  oscar_config cfg{};
+  int device = 0;
+  int num_sms = 0;
+  // bound cache
+  uint8_t* pool = nullptr;
+  int64_t num_pages = 0;
+  __nv_bfloat16* window = nullptr;
+  // owned device memory
+  float* R_K = nullptr;
+  float* R_V = nullptr;
+  float* R_VT = nullptr;
+  float* clip_K = nullptr;
+  float* clip_V = nullptr;
+  float* pv_scale = nullptr;
+  uint32_t* qrec = nullptr;
+  float* part = nullptr;
+  uint32_t* flags = nullptr;    // [0] error flags, [1] append ticket counter
+  int max_splits = 0;
+  bool loaded = false;
+  std::string last_error;
+};
+
+namespace {
+
+const char* kNullCtxMsg = "null context";
+
+int fail(oscar_ctx* ctx, int status, const std::string& msg) {
+  if (ctx) ctx->last_error = msg;
+  return status;
+}
+
+int cuda_fail(oscar_ctx* ctx, cudaError_t e, const char* what) {
+  std::string m = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return fail(ctx, OSCAR_ERR_CUDA, m);
+}
+
+int check_config_msg(const oscar_config* c, std::string* msg) {
+  if (!c) {
+    *msg = "null config";
+    return OSCAR_ERR_INVALID_ARG;
+  }
+  if (c->num_q_heads < 1 || c->num_kv_heads < 1 || c->num_q_heads % c->num_kv_heads) {
+    *msg = "num_q_heads must be a positive multiple of num_kv_heads";
+    return OSCAR_ERR_INVALID_ARG;
+  }
+  if (c->sink < 0 || c->recent < 1 || c->max_batch < 1 || c->max_pages_per_seq < 1 ||
+      c->num_splits < 0 || !(c->softmax_scale >= 0.f) || isinf(c->softmax_scale)) {
+    *msg = "sink >= 0, recent >= 1, max_batch >= 1, max_pages_per_seq >= 1, num_splits >= 0, "
+           "finite softmax_scale >= 0 required";
+    return OSCAR_ERR_INVALID_ARG;
+  }
+  if (c->head_dim != kHeadDim || c->page_size != kPage || c->group_size != kGroup) {
+    *msg = "only head_dim 128, page_size 16, group_size 32 are built";
+    return OSCAR_ERR_UNSUPPORTED;
+  }
+  const int g = c->num_q_heads / c->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) {
+    *msg = "query group size must be 1, 2, 4 or 8";
+    return OSCAR_ERR_UNSUPPORTED;
+  }
+  if (c->sink + c->recent > 1024) {
+    *msg = "sink + recent must not exceed 1024";
+    return OSCAR_ERR_UNSUPPORTED;
+  }
+  if ((int64_t)c->max_pages_per_seq * kPage > INT32_MAX) {
+    *msg = "max_pages_per_seq too large for int32 positions";
+    return OSCAR_ERR_INVALID_ARG;
+  }
+  return OSCAR_OK;
+}
+
+int auto_splits(const oscar_ctx* ctx, int batch) {
+  if (ctx->cfg.num_splits > 0) return ctx->cfg.num_splits;
+  const int64_t units = (int64_t)batch * ctx->cfg.num_kv_heads;
+  const int64_t pages = ctx->cfg.max_pages_per_seq;
+  // at least one wave of two CTAs per SM; at most 256 pages (32 per warp) per CTA
+  int64_t by_wave = (2 * (int64_t)ctx->num_sms + units - 1) / units;
+  int64_t by_pages = (pages + 255) / 256;
+  int64_t s = by_wave > by_pages ? by_wave : by_pages;
+  const int64_t cap = (pages + 7) / 8;  // keep >= 8 pages per split
+  if (s > cap) s = cap;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+template <class T>
+cudaError_t dalloc(T** p, size_t bytes) {
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes);
+}
+
+}  // namespace
+
+extern "C" {
+
+int oscar_version(void) { return OSCAR_ABI_VERSION; }
+
+const char* oscar_status_string(int status) {
+  switch (status) {
+    case OSCAR_OK: return "ok";
+    case OSCAR_ERR_INVALID_ARG: return "invalid argument";
+    case OSCAR_ERR_NOT_LOADED: return "rotations not loaded";
+    case OSCAR_ERR_OUT_OF_RANGE: return "out of range";
+    case OSCAR_ERR_CUDA: return "CUDA error";
+    case OSCAR_ERR_UNSUPPORTED: return "unsupported shape";
+    case OSCAR_ERR_NOT_BOUND: return "cache not bound";
+    default: return "unknown status";
+  }
+}
+
+int oscar_check_config(const oscar_config* cfg) {
+  std::string msg;
+  return check_config_msg(cfg, &msg);
+}
+
+int oscar_cache_bytes(const oscar_config* cfg, int64_t num_pages, size_t* pool_bytes,
+                      size_t* window_bytes) {
+  std::string msg;
+  int st = check_config_msg(cfg, &msg);
+  if (st) return st;
+  if (num_pages < 0 || !pool_bytes || !window_bytes) return OSCAR_ERR_INVALID_ARG;
+  *pool_bytes = (size_t)num_pages * cfg->num_kv_heads * kBlockBytes;
+  *window_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * 2 * (cfg->sink + cfg->recent) *
+                  kHeadDim * sizeof(__nv_bfloat16);
+  return OSCAR_OK;
+}
+
+void oscar_destroy(oscar_ctx* ctx) {
+  if (!ctx) return;
+  cudaFree(ctx->R_K);
+  cudaFree(ctx->R_V);
+  cudaFree(ctx->R_VT);
+  cudaFree(ctx->clip_K);
+  cudaFree(ctx->clip_V);
+  cudaFree(ctx->pv_scale);
+  cudaFree(ctx->qrec);
+  cudaFree(ctx->part);
+  cudaFree(ctx->flags);
+  delete ctx;
+}
+
+int oscar_create(const oscar_config* cfg, oscar_ctx** out) {
+  if (!out) return OSCAR_ERR_INVALID_ARG;
+  *out = nullptr;
+  std::string msg;
+  int st = check_config_msg(cfg, &msg);
+  if (st) return st;
+  oscar_ctx* ctx = new (std::nothrow) oscar_ctx();
+  if (!ctx) return OSCAR_ERR_CUDA;
+  ctx->cfg = *cfg;
+  if (ctx->cfg.softmax_scale == 0.f) ctx->cfg.softmax_scale = 1.f / sqrtf((float)kHeadDim);
+  cudaError_t e = cudaGetDevice(&ctx->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  const int hkv = cfg->num_kv_heads, g = cfg->num_q_heads / cfg->num_kv_heads;
+  const size_t rbytes = (size_t)hkv * kHeadDim * kHeadDim * sizeof(float);
+  if (e == cudaSuccess) e = dalloc(&ctx->R_K, rbytes);
+  if (e == cudaSuccess) e = dalloc(&ctx->R_V, rbytes);
+  if (e == cudaSuccess) e = dalloc(&ctx->R_VT, rbytes);
+  if (e == cudaSuccess) e = dalloc(&ctx->clip_K, hkv * sizeof(float));
+  if (e == cudaSuccess) e = dalloc(&ctx->clip_V, hkv * sizeof(float));
+  if (e == cudaSuccess) e = dalloc(&ctx->pv_scale, hkv * sizeof(float));
+  if (e == cudaSuccess) {
+    ctx->max_splits = auto_splits(ctx, cfg->max_batch);
+    for (int b = 1; b < cfg->max_batch; ++b) {
+      int s = auto_splits(ctx, b);
+      if (s > ctx->max_splits) ctx->max_splits = s;
+    }
+    e = dalloc(&ctx->qrec, (size_t)cfg->max_batch * hkv * kQrecWords * sizeof(uint32_t));
+  }
+  if (e == cudaSuccess)
+    e = dalloc(&ctx->part, (size_t)cfg->max_batch * hkv * (ctx->max_splits + 1) * g * kPartFloats *
+                               sizeof(float));
+  if (e == cudaSuccess) e = dalloc(&ctx->flags, 2 * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(ctx->flags, 0, 2 * sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    oscar_destroy(ctx);
+    return OSCAR_ERR_CUDA;
+  }
+  *out = ctx;
+  return OSCAR_OK;
+}
+
+int oscar_bind_cache(oscar_ctx* ctx, void* int2_pool, int64_t num_pages, void* window) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  if (!int2_pool || !window || num_pages < 1)
+    return fail(ctx, OSCAR_ERR_INVALID_ARG, "bind_cache: null buffer or num_pages < 1");
+  if (((uintptr_t)int2_pool & 15) || ((uintptr_t)window & 15))
+    return fail(ctx, OSCAR_ERR_INVALID_ARG, "bind_cache: pool and window must be 16-byte aligned");
+  if (num_pages > INT32_MAX) return fail(ctx, OSCAR_ERR_INVALID_ARG, "bind_cache: page ids are int32");
+  ctx->pool = static_cast<uint8_t*>(int2_pool);
+  ctx->num_pages = num_pages;
+  ctx->window = static_cast<__nv_bfloat16*>(window);
+  return OSCAR_OK;
+}
+
+int oscar_load_rotations(oscar_ctx* ctx, const float* R_K, const float* R_V, const float* clip_K,
+                         const float* clip_V) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  if (!R_K || !R_V || !clip_K || !clip_V)
+    return fail(ctx, OSCAR_ERR_INVALID_ARG, "load_rotations: null pointer");
+  const int hkv = ctx->cfg.num_kv_heads;
+  const size_t n = (size_t)hkv * kHeadDim * kHeadDim;
+  std::vector<float> rvt(n), ps(hkv);
+  for (int h = 0; h < hkv; ++h) {
+    if (!(clip_K[h] > 0.f) || !(clip_V[h] > 0.f) || isinf(clip_K[h]) || isinf(clip_V[h]))
+      return fail(ctx, OSCAR_ERR_INVALID_ARG, "load_rotations: clip values must be finite and > 0");
+    for (int i = 0; i < kHeadDim; ++i)
+      for (int j = 0; j < kHeadDim; ++j) {
+        const float a = R_K[((size_t)h * kHeadDim + i) * kHeadDim + j];
+        const float bv = R_V[((size_t)h * kHeadDim + i) * kHeadDim + j];
+        if (!isfinite(a) || !isfinite(bv))
+          return fail(ctx, OSCAR_ERR_INVALID_ARG, "load_rotations: non-finite rotation entry");
+        rvt[((size_t)h * kHeadDim + j) * kHeadDim + i] = bv;
+      }
+    // largest power of two with pscale * (2 clip_V / 3) * 1.01 <= 65504, at most 2^15
+    const double smax = 2.0 * clip_V[h] / 3.0 * 1.01;
+    int ex = (int)floor(log2(65504.0 / smax));
+    if (ex > 15) ex = 15;
+    if (ex < -30) ex = -30;
+    ps[h] = ldexpf(1.f, ex);
+  }
+  cudaError_t e = cudaMemcpy(ctx->R_K, R_K, n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->R_V, R_V, n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->R_VT, rvt.data(), n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->clip_K, clip_K, hkv * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->clip_V, clip_V, hkv * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->pv_scale, ps.data(), hkv * sizeof(float), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "load_rotations");
+  ctx->loaded = true;
+  return OSCAR_OK;
+}
+
+static int append_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
+                       const void* k, const void* v, int32_t batch, int32_t n_new, float* trace,
+                       int32_t trace_positions, void* stream) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  if (!ctx->loaded) return fail(ctx, OSCAR_ERR_NOT_LOADED, "quant_append: rotations not loaded");
+  if (!ctx->pool) return fail(ctx, OSCAR_ERR_NOT_BOUND, "quant_append: no cache bound");
+  if (!page_table || !state || !k || !v)
+    return fail(ctx, OSCAR_ERR_INVALID_ARG, "quant_append: null pointer");
+  if (batch < 1 || n_new < 0) return fail(ctx, OSCAR_ERR_INVALID_ARG, "quant_append: batch >= 1, n_new >= 0");
+  if (batch > ctx->cfg.max_batch)
+    return fail(ctx, OSCAR_ERR_OUT_OF_RANGE, "quant_append: batch exceeds max_batch");
+  if ((int64_t)n_new > (int64_t)ctx->cfg.max_pages_per_seq * kPage)
+    return fail(ctx, OSCAR_ERR_OUT_OF_RANGE, "quant_append: n_new exceeds the page-table capacity");
+  if (trace && trace_positions < 1)
+    return fail(ctx, OSCAR_ERR_INVALID_ARG, "quant_append: trace_positions must be >= 1");
+  if (n_new == 0) return OSCAR_OK;
+  AppendParams p{};
+  p.page_table = page_table;
+  p.pt_stride = ctx->cfg.max_pages_per_seq;
+  p.state = state;
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.pool = ctx->pool;
+  p.num_pages = ctx->num_pages;
+  p.window = ctx->window;
+  p.R_K = ctx->R_K;
+  p.R_V = ctx->R_V;
+  p.clip_K = ctx->clip_K;
+  p.clip_V = ctx->clip_V;
+  p.num_kv_heads = ctx->cfg.num_kv_heads;
+  p.sink = ctx->cfg.sink;
+  p.recent = ctx->cfg.recent;
+  p.n_new = n_new;
+  p.batch = batch;
+  p.fold_rv = ctx->cfg.fold_rv;
+  p.trace = trace;
+  p.trace_positions = trace ? trace_positions : 0;
+  p.err_flags = ctx->flags;
+  p.counter = ctx->flags + 1;
+  cudaError_t e = launch_quant_append(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "quant_append launch");
+  return OSCAR_OK;
+}
+
+int oscar_quant_append(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
+                       const void* k, const void* v, int32_t batch, int32_t n_new, void* stream) {
+  return append_impl(ctx, page_table, state, k, v, batch, n_new, nullptr, 0, stream);
+}
+
+int oscar_quant_append_traced(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
+                              const void* k, const void* v, int32_t batch, int32_t n_new,
+                              float* trace, int32_t trace_positions, void* stream) {
+  if (!trace) return fail(ctx, OSCAR_ERR_INVALID_ARG, "quant_append_traced: null trace");
+  return append_impl(ctx, page_table, state, k, v, batch, n_new, trace, trace_positions, stream);
+}
+
+int oscar_decode_splits(const oscar_ctx* ctx, int32_t batch, int32_t* splits) {
+  if (!ctx || !splits || batch < 1) return OSCAR_ERR_INVALID_ARG;
+  *splits = auto_splits(ctx, batch);
+  return OSCAR_OK;
+}
+
+int oscar_decode_attn(oscar_ctx* ctx, const void* q, const int32_t* page_table,
+                      const oscar_seq_state* state, float* o, int32_t batch, void* stream) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  if (!ctx->loaded) return fail(ctx, OSCAR_ERR_NOT_LOADED, "decode_attn: rotations not loaded");
+  if (!ctx->pool) return fail(ctx, OSCAR_ERR_NOT_BOUND, "decode_attn: no cache bound");
+  if (!q || !page_table || !state || !o) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_attn: null pointer");
+  if (batch < 1) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_attn: batch >= 1");
+  if (batch > ctx->cfg.max_batch) return fail(ctx, OSCAR_ERR_OUT_OF_RANGE, "decode_attn: batch exceeds max_batch");
+  DecodeParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.page_table = page_table;
+  p.pt_stride = ctx->cfg.max_pages_per_seq;
+  p.state = state;
+  p.pool = ctx->pool;
+  p.num_pages = ctx->num_pages;
+  p.window = ctx->window;
+  p.R_K = ctx->R_K;
+  p.R_VT = ctx->R_VT;
+  p.qrec = ctx->qrec;
+  p.part = ctx->part;
+  p.o = o;
+  p.pv_scale = ctx->pv_scale;
+  p.num_q_heads = ctx->cfg.num_q_heads;
+  p.num_kv_heads = ctx->cfg.num_kv_heads;
+  p.gqa = ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads;
+  p.sink = ctx->cfg.sink;
+  p.recent = ctx->cfg.recent;
+  p.splits = auto_splits(ctx, batch);
+  p.fold_rv = ctx->cfg.fold_rv;
+  p.scale_log2 = ctx->cfg.softmax_scale * 1.4426950408889634f;
+  p.err_flags = ctx->flags;
+  cudaError_t e = launch_decode(p, batch, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "decode_attn launch");
+  return OSCAR_OK;
+}
+
+int oscar_error_flags(oscar_ctx* ctx, uint32_t* flags, int32_t clear) {
+  if (!ctx || !flags) return OSCAR_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  uint32_t f = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&f, ctx->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(ctx->flags, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "error_flags");
+  *flags = f;
+  return OSCAR_OK;
+}
+
+const char* oscar_last_error(const oscar_ctx* ctx) {
+  if (!ctx) return kNullCtxMsg;
+  return ctx->last_error.c_str();
+}
+
+}  // extern "C"

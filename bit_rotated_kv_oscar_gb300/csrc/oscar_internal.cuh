@@ -1,0 +1,69 @@
+// Internal declarations shared by the CUDA translation units of liboscar.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/oscar.h"
+
+namespace oscar {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 16;
+constexpr int kGroup = 32;
+constexpr int kGroups = kHeadDim / kGroup;   // 4 quantisation groups per token
+constexpr int kBlockBytes = OSCAR_PAGE_BLOCK_BYTES;
+constexpr int kMaxGqa = 8;
+// per-(request, KV head) record written by the query-rotation kernel:
+// 1024 words of fp16x2 mma A fragments, 32 floats of group sums, 1 float scale
+constexpr int kQrecWords = 1088;
+constexpr int kPartFloats = kHeadDim + 2;    // o[128], m, l
+
+struct AppendParams {
+  const int32_t* page_table;
+  int32_t pt_stride;
+  oscar_seq_state* state;
+  const __nv_bfloat16* k;   // [B][n_new][Hkv][128]
+  const __nv_bfloat16* v;
+  uint8_t* pool;
+  int64_t num_pages;
+  __nv_bfloat16* window;    // [B][Hkv][2][S+W][128]
+  const float* R_K;         // [Hkv][128][128]
+  const float* R_V;
+  const float* clip_K;      // [Hkv]
+  const float* clip_V;
+  int32_t num_kv_heads, sink, recent, n_new, batch;
+  int32_t fold_rv;          // 1: V arrives already rotated (R_V folded into the projection)
+  float* trace;             // optional [B][trace_positions][Hkv][2][128]
+  int32_t trace_positions;
+  uint32_t* err_flags;
+  uint32_t* counter;        // zero between launches
+};
+
+struct DecodeParams {
+  const __nv_bfloat16* q;   // [B][Hq][128]
+  const int32_t* page_table;
+  int32_t pt_stride;
+  const oscar_seq_state* state;
+  const uint8_t* pool;
+  int64_t num_pages;
+  const __nv_bfloat16* window;
+  const float* R_K;         // [Hkv][128][128]
+  const float* R_VT;        // [Hkv][128][128], R_VT[h][i][j] = R_V[h][j][i]
+  uint32_t* qrec;           // [B][Hkv][kQrecWords]
+  float* part;              // [B][Hkv][splits + 1][gqa][kPartFloats]
+  float* o;                 // [B][Hq][128]
+  const float* pv_scale;    // [Hkv] power of two applied to p * s_v before fp16 rounding
+  int32_t num_q_heads, num_kv_heads, gqa, sink, recent, splits, fold_rv;
+  float scale_log2;         // softmax_scale * log2(e)
+  uint32_t* err_flags;
+};
+
+// launchers (return cudaGetLastError())
+cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s);
+int decode_smem_bytes();
+
+}  // namespace oscar

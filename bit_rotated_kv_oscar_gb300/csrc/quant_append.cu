@@ -1,0 +1,228 @@
+// Write path of the OSCAR INT2 cache: rotate, clip, group-quantise, pack.
+//
+// One CTA of 512 threads handles one new token of one request and one KV head
+// (K and V together). Depending on the token's position it either copies the
+// token into the BF16 sink, quantises it straight into its INT2 page, or
+// places it in the BF16 recent ring after quantising the ring entry it
+// evicts. Sources: "Juntos, AI Open-Sources OSCAR ..." (7minutos.es), section
+// "El sistema de servicio" (write path: rotate, clip to the calibrated
+// threshold, asymmetric per-token INT2 groups; sink and recent tokens in BF16);
+// "OSCAR: Offline Spectral Covariance-Aware Rotation ..." (gist.science, it),
+// Riepilogo Tecnico 2.2 B (mixed-precision paged layout).
+#include "oscar_internal.cuh"
+
+namespace oscar {
+
+constexpr int kThreads = 512;
+
+__device__ __forceinline__ float warp_min(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ bool state_ok(int L, int E, int S, int W) {
+  return L >= 0 && E >= S && E <= (L > S ? L : S) && L - E <= W;
+}
+
+// page block of (request b, position pos, KV head h) or nullptr (flag raised)
+__device__ __forceinline__ uint8_t* block_of(const AppendParams& p, int b, int64_t pos, int h) {
+  int64_t pidx = pos / kPage;
+  if (pidx >= p.pt_stride) {
+    atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
+    return nullptr;
+  }
+  int32_t id = p.page_table[(int64_t)b * p.pt_stride + pidx];
+  if (id < 0 || id >= p.num_pages) {
+    atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
+    return nullptr;
+  }
+  return p.pool + ((int64_t)id * p.num_kv_heads + h) * kBlockBytes;
+}
+
+__global__ void __launch_bounds__(kThreads)
+oscar_quant_append_kernel(AppendParams p) {
+  const int tid = threadIdx.x;
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int S = p.sink, W = p.recent;
+  const int Hkv = p.num_kv_heads;
+
+  __shared__ int s_L, s_E, s_last;
+  __shared__ float xs[2][kHeadDim];            // token being quantised, K and V
+  __shared__ float red[2][2][kHeadDim];        // partial dot products
+  __shared__ uint8_t codes[2][kHeadDim];
+  __shared__ __half meta[2][kGroups][2];
+
+  if (tid == 0) {
+    oscar_seq_state st = p.state[b];
+    s_L = st.seq_len;
+    s_E = st.int2_end;
+    __threadfence();
+    unsigned total = gridDim.x * gridDim.y * gridDim.z;
+    s_last = (atomicAdd(p.counter, 1u) == total - 1u);
+  }
+  __syncthreads();
+  const int L = s_L, E = s_E;
+  const bool ok = state_ok(L, E, S, W);
+  if (!ok && tid == 0 && j == 0 && h == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_STATE);
+
+  if (ok) {
+    const int64_t q = (int64_t)L + j;
+    int64_t E2 = (int64_t)L + p.n_new - W;
+    if (E2 < E) E2 = E;
+    if (E2 < S) E2 = S;
+    const size_t slots = (size_t)(S + W);
+    __nv_bfloat16* win_k = p.window + (((size_t)b * Hkv + h) * 2 + 0) * slots * kHeadDim;
+    __nv_bfloat16* win_v = p.window + (((size_t)b * Hkv + h) * 2 + 1) * slots * kHeadDim;
+    const size_t in_off = (((size_t)b * p.n_new + j) * Hkv + h) * kHeadDim;
+
+    // what this CTA quantises: -1 none, else the position; and where it comes from
+    int64_t qpos = -1;
+    const __nv_bfloat16* src_k = nullptr;
+    const __nv_bfloat16* src_v = nullptr;
+    int64_t ring_slot_new = -1;
+    if (q < S) {
+      // sink token: BF16 copy
+      if (tid < kHeadDim) {
+        win_k[(size_t)q * kHeadDim + tid] = p.k[in_off + tid];
+        win_v[(size_t)q * kHeadDim + tid] = p.v[in_off + tid];
+      }
+    } else if (q < E2) {
+      qpos = q;
+      src_k = p.k + in_off;
+      src_v = p.v + in_off;
+    } else {
+      // ring occupant; the entry at its slot may have to be quantised first
+      const int64_t pe = q - (int64_t)W * ((q - L) / W + 1);
+      if (pe >= E && pe < E2 && pe >= S) {
+        qpos = pe;
+        const size_t sl = (size_t)(S + pe % W) * kHeadDim;
+        src_k = win_k + sl;
+        src_v = win_v + sl;
+      }
+      ring_slot_new = S + q % W;
+    }
+
+    if (qpos >= 0 && tid < 2 * kHeadDim) {
+      const int kind = tid >> 7, c = tid & 127;
+      const __nv_bfloat16* src = kind ? src_v : src_k;
+      xs[kind][c] = __bfloat162float(src[c]);
+    }
+    __syncthreads();  // ring entry read before it is overwritten below
+
+    if (ring_slot_new >= 0 && tid < 2 * kHeadDim) {
+      const int kind = tid >> 7, c = tid & 127;
+      __nv_bfloat16* dst = (kind ? win_v : win_k) + (size_t)ring_slot_new * kHeadDim;
+      dst[c] = (kind ? p.v : p.k)[in_off + c];
+    }
+
+    if (qpos >= 0) {
+      // rotation x @ R: thread (kind, half, c) sums 64 terms, two halves added in order
+      {
+        const int kind = tid >> 8, half = (tid >> 7) & 1, c = tid & 127;
+        const float* R = (kind ? p.R_V : p.R_K) + (size_t)h * kHeadDim * kHeadDim;
+        const int i0 = half * 64;
+        float acc = 0.f;
+        if (kind == 1 && p.fold_rv) {
+          acc = half ? 0.f : xs[1][c];  // identity: V is already in the R_V basis
+        } else {
+#pragma unroll 16
+          for (int i = 0; i < 64; ++i) acc = fmaf(xs[kind][i0 + i], __ldg(&R[(i0 + i) * kHeadDim + c]), acc);
+        }
+        red[kind][half][c] = acc;
+      }
+      __syncthreads();
+      if ((tid & 255) < kHeadDim) {
+        const int kind = tid >> 8, c = tid & 127;
+        const float x_rot = red[kind][0][c] + red[kind][1][c];
+        if (p.trace && qpos < p.trace_positions) {
+          p.trace[((((size_t)b * p.trace_positions + qpos) * Hkv + h) * 2 + kind) * kHeadDim + c] = x_rot;
+        }
+        const float clip = (kind ? p.clip_V : p.clip_K)[h];
+        const float x = fminf(fmaxf(x_rot, -clip), clip);
+        // one warp = one group of 32 channels
+        const float mn = warp_min(x), mx = warp_max(x);
+        const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+        const __half z16 = __float2half_rn(mn);
+        const float sf = __half2float(s16), zf = __half2float(z16);
+        int code = 0;
+        if (sf != 0.f) {
+          float u = rintf(__fdiv_rn(__fsub_rn(x, zf), sf));
+          u = fminf(fmaxf(u, 0.f), 3.f);
+          code = (int)u;
+        }
+        codes[kind][c] = (uint8_t)code;
+        if ((c & 31) == 0) {
+          meta[kind][c >> 5][0] = s16;
+          meta[kind][c >> 5][1] = z16;
+        }
+      }
+      __syncthreads();
+      uint8_t* blk = tid < 72 ? block_of(p, b, qpos, h) : nullptr;
+      if (blk) {
+        const int t = (int)(qpos % kPage);
+        if (tid < 8) {
+          // K: 8 words of this token
+          const int bb = tid >> 1, x = tid & 1;
+          uint32_t w = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int ch = 16 * i + 2 * bb + 8 * x;
+            w |= (uint32_t)codes[0][ch] << (2 * i);
+            w |= (uint32_t)codes[0][ch + 1] << (16 + 2 * i);
+          }
+          const int a = t & 7, th = t >> 3;
+          *reinterpret_cast<uint32_t*>(blk + 16 * (4 * a + bb) + 4 * (2 * th + x)) = w;
+        } else if (tid >= 32 && tid < 48) {
+          // V: 16 half-words of this token
+          const int u = tid - 32, a = u >> 1, x = u & 1;
+          uint32_t hw = 0;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) hw |= (uint32_t)codes[1][16 * i + a + 8 * x] << (2 * i);
+          const int tt = t >> 3, bb = (t & 7) >> 1, hi = t & 1;
+          *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a + bb) + 4 * (2 * tt + x) + 2 * hi) =
+              (uint16_t)hw;
+        } else if (tid >= 64 && tid < 72) {
+          // scale / zero of each group, K and V
+          const int u = tid - 64, kind = u >> 2, gq = u & 3;
+          const int jj = 4 * kind + gq, bb = (t & 7) >> 1;
+          uint8_t* m = blk + 1024 + 16 * (4 * jj + bb) + 4 * (2 * (t >> 3)) + 2 * (t & 1);
+          *reinterpret_cast<__half*>(m) = meta[kind][gq][0];
+          *reinterpret_cast<__half*>(m + 4) = meta[kind][gq][1];
+        }
+      }
+    }
+  }
+
+  // the CTA that took the last ticket publishes the new state of every request
+  if (s_last && tid == 0) {
+    __threadfence();
+    for (int bb = 0; bb < p.batch; ++bb) {
+      oscar_seq_state st = p.state[bb];
+      if (!state_ok(st.seq_len, st.int2_end, S, W)) continue;
+      int64_t nl = (int64_t)st.seq_len + p.n_new;
+      int64_t ne = nl - W;
+      if (ne < st.int2_end) ne = st.int2_end;
+      if (ne < S) ne = S;
+      st.seq_len = (int32_t)nl;
+      st.int2_end = (int32_t)ne;
+      p.state[bb] = st;
+    }
+    *p.counter = 0u;
+    __threadfence();
+  }
+}
+
+
+cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s) {
+  dim3 grid((unsigned)p.n_new, (unsigned)p.num_kv_heads, (unsigned)p.batch);
+  oscar_quant_append_kernel<<<grid, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace oscar

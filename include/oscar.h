@@ -1,0 +1,208 @@
+/*
+ * oscar.h - C ABI of the OSCAR INT2 KV-cache serving library (GB300, sm_103a).
+ *
+ * The library implements the online serving path of OSCAR (Offline Spectral
+ * Covariance-Aware Rotation): the write path that rotates each new key or value
+ * vector by a fixed per-head rotation, clips it and stores it as packed 2-bit
+ * groups in a paged cache, and the fused decode attention that reads BF16 sink
+ * and recent tokens together with the INT2 history in one pass.
+ *
+ * Sources, cited by page title and section:
+ *   [IT] "OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV Cache
+ *        Quantization", gist.science explainer (Italian), "Riepilogo Tecnico".
+ *   [ES] "Juntos, AI Open-Sources OSCAR: un sistema de cuantificación de caché KV
+ *        de 2 bits consciente de la atención para servicios de LLM de contexto
+ *        prolongado", 7minutos.es.
+ *
+ * Conventions shared by every call
+ *   - Activations are row vectors; a rotation acts on the right: x_rot = x @ R,
+ *     R row-major [d][d], x_rot[j] = sum_i x[i] * R[i][j].
+ *   - Every function returns 0 (OSCAR_OK) or a negative oscar_status. No call
+ *     aborts, throws or traps; the message of the last failure on a context is
+ *     returned by oscar_last_error().
+ *   - Device buffers (pool, window, page table, state, q, k, v, o) are owned by
+ *     the caller. The library owns its device copies of the rotations and clip
+ *     values and a split-K workspace allocated by oscar_create().
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Kernel work is asynchronous on that stream; errors found by the host are
+ *     reported at once, errors found by the device are latched in a flag word
+ *     read by oscar_error_flags().
+ *   - Supported shapes: head_dim 128, page_size 16, group_size 32, and a query
+ *     group (num_q_heads / num_kv_heads) of 1, 2, 4 or 8. Anything else is
+ *     OSCAR_ERR_UNSUPPORTED.
+ *
+ * Storage formats (owned by the library, allocated by the caller)
+ *
+ *   INT2 pool: num_pages * num_kv_heads blocks of 1536 bytes; the block of page
+ *   id p and KV head h starts at byte (p * num_kv_heads + h) * 1536. A page
+ *   holds 16 consecutive positions, slot t = position % 16. Codes and
+ *   metadata of one token are spread over the block so that each lane of a
+ *   warp reads the exact operand fragment it feeds to the tensor cores:
+ *     K code of slot t, channel c (2 bits, bytes [0, 512)):
+ *       i = c/16, r = c%16, x = r/8, b = (r%8)/2, hi = r%2, a = t%8, th = t/8;
+ *       32-bit little-endian word at byte 16*(4a+b) + 4*(2*th+x), bit 16*hi+2*i.
+ *     V code of slot t, channel c (bytes [512, 1024)):
+ *       i = c/16, r = c%16, x = r/8, a = r%8, tt = t/8, b = (t%8)/2, hi = t%2;
+ *       word at byte 512 + 16*(4a+b) + 4*(2*tt+x), bit 16*hi+2*i.
+ *     fp16 scale (field 0) / zero (field 1) of group gq (channels 32gq..32gq+31)
+ *       of slot t, kind 0 = K, 1 = V (bytes [1024, 1536)):
+ *       j = 4*kind + gq, b = (t%8)/2; half at byte
+ *       1024 + 16*(4j+b) + 4*(2*(t/8)+field) + 2*(t%2).
+ *   Slots of positions outside [sink, int2_end) are never read.
+ *
+ *   Window: bf16 [max_batch][num_kv_heads][2 (K, V)][sink + recent][128].
+ *   Slot s < sink holds position s; slot sink + (pos % recent) holds a recent
+ *   position pos.
+ *
+ *   Page table: int32 [batch][max_pages_per_seq]; entry n maps positions
+ *   [16n, 16n+16) of the request to a page id. Several requests may map the
+ *   same page id (shared prefix); such pages must not be appended to.
+ *
+ *   Sequence state: oscar_seq_state [batch] in device memory. seq_len = cached
+ *   tokens L; int2_end = E, the first position still held in BF16 after the
+ *   sink. A new request is {0, sink}. Invariants: sink <= E, E <= max(L, sink),
+ *   L - E <= recent. Positions [0, min(sink, L)) are in the sink, [sink, E) are
+ *   INT2, [E, L) are in the recent ring.
+ */
+#ifndef OSCAR_H
+#define OSCAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OSCAR_ABI_VERSION 1
+#define OSCAR_PAGE_BLOCK_BYTES 1536
+
+typedef enum oscar_status {
+  OSCAR_OK = 0,
+  OSCAR_ERR_INVALID_ARG = -1,  /* null pointer, bad shape or size */
+  OSCAR_ERR_NOT_LOADED = -2,   /* rotations not loaded */
+  OSCAR_ERR_OUT_OF_RANGE = -3, /* batch or length beyond what the context was created for */
+  OSCAR_ERR_CUDA = -4,         /* a CUDA runtime call failed; see oscar_last_error */
+  OSCAR_ERR_UNSUPPORTED = -5,  /* shape the kernels are not built for */
+  OSCAR_ERR_NOT_BOUND = -6     /* no cache bound to the context */
+} oscar_status;
+
+/* Device-side error flags (bit set = condition seen since the last clear). */
+#define OSCAR_FLAG_BAD_PAGE_ID 1u   /* a page-table entry outside [0, num_pages); access skipped */
+#define OSCAR_FLAG_BAD_STATE 2u     /* a sequence state breaking the invariants; request skipped */
+
+typedef struct oscar_config {
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;          /* 128 */
+  int32_t page_size;         /* 16 */
+  int32_t group_size;        /* 32: channels per quantisation group */
+  int32_t sink;              /* S >= 0: leading tokens kept in BF16 */
+  int32_t recent;            /* W >= 1: trailing tokens kept in BF16 */
+  int32_t max_batch;         /* requests per call, >= 1 */
+  int32_t max_pages_per_seq; /* page-table row stride, >= 1 */
+  float softmax_scale;       /* 0 selects 1/sqrt(head_dim) */
+  int32_t fold_rv;           /* 1: R_V is folded into the model's value and output projections
+                                ([ES] "El sistema de servicio"): values arrive already in the
+                                R_V basis, so the write path does not rotate V and decode
+                                returns its output in the R_V basis (no R_V^T applied) */
+  int32_t num_splits;        /* INT2 splits per (request, KV head) in decode; 0 = automatic */
+} oscar_config;
+
+typedef struct oscar_seq_state {
+  int32_t seq_len;  /* L */
+  int32_t int2_end; /* E */
+} oscar_seq_state;
+
+typedef struct oscar_ctx oscar_ctx;
+
+/* ABI version (OSCAR_ABI_VERSION). */
+int oscar_version(void);
+
+/* Static text for a status code. */
+const char* oscar_status_string(int status);
+
+/* Host-only check of a configuration: OSCAR_OK, OSCAR_ERR_INVALID_ARG or
+ * OSCAR_ERR_UNSUPPORTED. Touches no GPU. */
+int oscar_check_config(const oscar_config* cfg);
+
+/* Bytes the caller must allocate for an INT2 pool of num_pages pages and for
+ * the BF16 window of cfg->max_batch requests. Host only. [IT] 2.2 B (paged
+ * mixed-precision layout); [ES] "El sistema de servicio" (sink / recent / history). */
+int oscar_cache_bytes(const oscar_config* cfg, int64_t num_pages, size_t* pool_bytes,
+                      size_t* window_bytes);
+
+/* Create a context on the current CUDA device: validates cfg, allocates the
+ * rotation copies and the split-K workspace. *out is NULL on failure. */
+int oscar_create(const oscar_config* cfg, oscar_ctx** out);
+
+/* Free a context and everything it allocated (NULL is ignored). */
+void oscar_destroy(oscar_ctx* ctx);
+
+/* Bind caller-owned device memory: the INT2 pool (oscar_cache_bytes bytes,
+ * 16-byte aligned) and the BF16 window. May be called again to rebind. */
+int oscar_bind_cache(oscar_ctx* ctx, void* int2_pool, int64_t num_pages, void* window);
+
+/* Load the fixed per-layer rotations and clip values computed offline.
+ * [IT] 2.2 A (R_K = U_Q H_Had P_br, R_V = U_S H_Had P_br, clip thresholds from
+ * the rotated calibration activations); [ES] "Lo que OSCAR hace diferente".
+ * R_K, R_V: HOST float32 [num_kv_heads][128][128] row-major; clip_K, clip_V:
+ * HOST float32 [num_kv_heads], > 0. Copied synchronously; the caller keeps
+ * ownership of its arrays. */
+int oscar_load_rotations(oscar_ctx* ctx, const float* R_K, const float* R_V,
+                         const float* clip_K, const float* clip_V);
+
+/* Write path: append n_new tokens to each of `batch` requests.
+ * [ES] "El sistema de servicio": each token is rotated, clipped to the
+ * calibrated threshold and quantised to asymmetric per-token INT2 groups;
+ * sink and recent tokens stay in BF16.
+ * k, v: DEVICE bf16 [batch][n_new][num_kv_heads][128] (positions L..L+n_new-1).
+ * page_table: DEVICE int32 [batch][max_pages_per_seq]; it must map every
+ * position below the new int2_end. state: DEVICE [batch], read and updated.
+ * With E' = max(E, sink, L + n_new - recent): positions below sink go to the
+ * sink, positions in [E, E') are rotated (x @ R), clipped to [-c, c],
+ * quantised per group of 32 channels with s = fp16((max-min)/3), z = fp16(min),
+ * code = clamp(rint((x - z)/s), 0, 3) (0 when s == 0), and packed; taken from
+ * the ring when already cached, else from k/v. The remaining new positions go
+ * to the ring. Afterwards state = {L + n_new, E'}. */
+int oscar_quant_append(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
+                       const void* k, const void* v, int32_t batch, int32_t n_new,
+                       void* stream);
+
+/* oscar_quant_append that also records, for every token it quantises, the
+ * rotated float32 value before clipping: trace DEVICE float32
+ * [batch][trace_positions][num_kv_heads][2 (K, V)][128], indexed by absolute
+ * position; positions >= trace_positions are not recorded. Same arithmetic. */
+int oscar_quant_append_traced(oscar_ctx* ctx, const int32_t* page_table,
+                              oscar_seq_state* state, const void* k, const void* v,
+                              int32_t batch, int32_t n_new, float* trace,
+                              int32_t trace_positions, void* stream);
+
+/* Read path: one decode query per request over its whole cache.
+ * [IT] 2.2 B "Integrazione del Kernel"; [ES] "El sistema de servicio" (unpack,
+ * dequantise, undo the rotation and attend in one pass). Because R is
+ * orthogonal the library rotates the query by R_K instead of de-rotating
+ * every key, accumulates INT2 values in the R_V basis and applies R_V^T to
+ * the merged output once (skipped when fold_rv = 1).
+ * q: DEVICE bf16 [batch][num_q_heads][128]; o: DEVICE float32
+ * [batch][num_q_heads][128]; query head j reads KV head j / (Hq/Hkv).
+ * o = softmax(q K^T * softmax_scale) V over all L cached positions; a request
+ * with L = 0 gets o = 0. */
+int oscar_decode_attn(oscar_ctx* ctx, const void* q, const int32_t* page_table,
+                      const oscar_seq_state* state, float* o, int32_t batch, void* stream);
+
+/* Number of INT2 splits per (request, KV head) decode uses for `batch`. */
+int oscar_decode_splits(const oscar_ctx* ctx, int32_t batch, int32_t* splits);
+
+/* Read (and optionally clear) the device error flags. Synchronises the
+ * device. flags receives an OR of OSCAR_FLAG_* bits. */
+int oscar_error_flags(oscar_ctx* ctx, uint32_t* flags, int32_t clear);
+
+/* Message of the last failure on ctx ("" if none; a static text for NULL). */
+const char* oscar_last_error(const oscar_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H */
