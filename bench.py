@@ -23,6 +23,7 @@ the data path); timings are the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -140,12 +141,14 @@ def profiled_traffic(workload):
 # ---------------------------------------------------------------------------
 
 class Workload:
-    def __init__(self, name, device, n_steps_total, rank=0, min_layers=None):
+    def __init__(self, name, device, n_steps_total, rank=0, min_layers=None, batch_override=0):
         from bit_rotated_kv_oscar_gb300 import abi
         from bit_rotated_kv_oscar_gb300.cache import PagedCache
         from bit_rotated_kv_oscar_gb300.calibrate import calibrate
 
         spec = WORKLOADS[name]
+        if batch_override:
+            spec = dataclasses.replace(spec, batch=batch_override)
         self.spec, self.name, self.device = spec, name, device
         hq, hkv, S, W, B = spec.num_q_heads, spec.num_kv_heads, spec.sink, spec.recent, spec.batch
         self.B = B
@@ -223,7 +226,7 @@ class Workload:
                 pool[dst] = pool0[src_pages[:npg]]
                 win[b].copy_(win0[b0])
                 E = max(S, L - W)
-                cache.state[b] = torch.tensor([L, E], dtype=torch.int32, device=self.device)
+                cache.state[b] = torch.tensor([L, E, b, 0], dtype=torch.int32, device=self.device)
         torch.cuda.synchronize()
 
     def decode_bytes(self, extra_tokens):
@@ -259,7 +262,7 @@ class Workload:
 
 def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True):
     n_total = 2 * args.warmup + 3 * args.steps + 4096 + 64
-    wl = Workload(name, device, n_total, rank)
+    wl = Workload(name, device, n_total, rank, batch_override=getattr(args, 'batch', 0))
     stream = torch.cuda.current_stream(device)
     # warm-up: at least W steps and about half a second under load
     i = 0
@@ -424,6 +427,8 @@ def main():
     ap.add_argument("--workload", default="qwen3_8b_bs1_32k")
     ap.add_argument("--extra", default="qwen3_32b_bs28_100k", help="second workload ('' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch (smaller cases for profiling captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -52,7 +52,8 @@ class OscarConfig(ctypes.Structure):
 
 
 class SeqState(ctypes.Structure):
-    _fields_ = [("seq_len", ctypes.c_int32), ("int2_end", ctypes.c_int32)]
+    _fields_ = [("seq_len", ctypes.c_int32), ("int2_end", ctypes.c_int32),
+                ("window_row", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p

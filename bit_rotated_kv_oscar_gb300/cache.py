@@ -32,8 +32,10 @@ class PagedCache:
         self.window = torch.zeros(window_bytes // 2, dtype=torch.bfloat16, device=device)
         self.page_table_host = np.full((cfg.max_batch, cfg.max_pages_per_seq), -1, dtype=np.int32)
         self.page_table = torch.from_numpy(self.page_table_host.copy()).to(device)
-        st = np.zeros((cfg.max_batch, 2), dtype=np.int32)
+        # oscar_seq_state rows: seq_len, int2_end, window_row, reserved
+        st = np.zeros((cfg.max_batch, 4), dtype=np.int32)
         st[:, 1] = cfg.sink
+        st[:, 2] = np.arange(cfg.max_batch)
         self.state = torch.from_numpy(st).to(device)
         order = np.arange(self.num_pages, dtype=np.int32) if page_order is None else \
             np.asarray(page_order, dtype=np.int32)
@@ -80,7 +82,7 @@ class PagedCache:
                     self.free.append(pid)
                 row[n] = -1
         self.upload(b)
-        self.state[b] = torch.tensor([0, self.cfg.sink], dtype=torch.int32)
+        self.state[b] = torch.tensor([0, self.cfg.sink, b, 0], dtype=torch.int32)
 
     def fork(self, src: int, dst: int, prefix_tokens: int):
         """Request dst shares the first prefix_tokens of src (page aligned, all INT2 or sink).
@@ -104,7 +106,7 @@ class PagedCache:
                              self.cfg.sink + self.cfg.recent, 128)
         if self.cfg.sink:
             w[dst, :, :, :self.cfg.sink].copy_(w[src, :, :, :self.cfg.sink])
-        self.state[dst] = torch.tensor([prefix_tokens, prefix_tokens], dtype=torch.int32)
+        self.state[dst] = torch.tensor([prefix_tokens, prefix_tokens, dst, 0], dtype=torch.int32)
 
     # ------------------------------------------------------------- accounting
     def footprint_bytes(self, batch: int):

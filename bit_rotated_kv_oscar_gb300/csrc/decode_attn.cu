@@ -39,10 +39,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 4;
 constexpr int kStageBytes = kWarps * kStages * kBlockBytes;   // 48 KB
 constexpr int kMaxWindow = 1024;                                // sink + recent limit
-
-__device__ __forceinline__ bool state_ok(int L, int E, int S, int W) {
-  return L >= 0 && E >= S && E <= (L > S ? L : S) && L - E <= W;
-}
+constexpr int kWinChunk = kWindowChunk;                         // window tokens per CTA
 
 // factor of a code read from slot i (see the file comment)
 __host__ __device__ constexpr float slot_factor(int i) {
@@ -103,67 +100,100 @@ __device__ __forceinline__ float warp_maxf(float x) {
 // --------------------------------------------------------------------------
 // 1. query rotation and operand fragments
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) oscar_rotate_q_kernel(DecodeParams p) {
-  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
+constexpr int kRotThreads = 256;
+constexpr int kRotSmem = kHeadDim * kHeadDim * 4;  // one 128 x 128 float matrix
+
+// copy a 128 x 128 float matrix into shared memory with every copy in flight at
+// once (cp.async does not go through registers); the caller waits and syncs
+__device__ __forceinline__ void stage_matrix(float* dst, const float* src, int tid, int nthreads) {
+  for (int i = tid; i < kHeadDim * kHeadDim / 4; i += nthreads) cp_async16(dst + 4 * i, src + 4 * i);
+  cp_commit();
+}
+
+__global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  float* Rs = reinterpret_cast<float*>(dsm);                  // R_K[h], [128][128]
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int c = tid & (kHeadDim - 1), half = tid >> 7;
   const int g = p.gqa;
   __shared__ float qs[kMaxGqa][kHeadDim];
+  __shared__ float red[kMaxGqa][kHeadDim];
   __shared__ __half hs[2][kMaxGqa][kHeadDim];
+  __shared__ __half gsum[2][kMaxGqa][kGroups];
   __shared__ float wmax[4];
-  for (int m = 0; m < g; ++m)
-    qs[m][c] = __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + c]);
+  stage_matrix(Rs, p.R_K + (size_t)h * kHeadDim * kHeadDim, tid, kRotThreads);
+  for (int i = tid; i < g * kHeadDim; i += kRotThreads)
+    qs[i >> 7][i & 127] = __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g) * kHeadDim + i]);
+  cp_wait<0>();
   __syncthreads();
+  // thread (half, c): rows [64 half, 64 half + 64) of q R_K for every head
   float acc[kMaxGqa];
 #pragma unroll
   for (int m = 0; m < kMaxGqa; ++m) acc[m] = 0.f;
-  const float* R = p.R_K + (size_t)h * kHeadDim * kHeadDim;
+  const int i0 = half * 64;
 #pragma unroll 8
-  for (int i = 0; i < kHeadDim; ++i) {
-    const float r = __ldg(&R[i * kHeadDim + c]);
+  for (int i = 0; i < 64; ++i) {
+    const float r = Rs[(i0 + i) * kHeadDim + c];
 #pragma unroll
     for (int m = 0; m < kMaxGqa; ++m)
-      if (m < g) acc[m] = fmaf(qs[m][i], r, acc[m]);
+      if (m < g) acc[m] = fmaf(qs[m][i0 + i], r, acc[m]);
   }
-  float amax = 0.f;
+  if (half == 1) {
 #pragma unroll
-  for (int m = 0; m < kMaxGqa; ++m) {
-    acc[m] = m < g ? acc[m] * p.scale_log2 : 0.f;
-    amax = fmaxf(amax, fabsf(acc[m]));
+    for (int m = 0; m < kMaxGqa; ++m) red[m][c] = acc[m];
   }
-  amax = warp_maxf(amax);
-  if ((c & 31) == 0) wmax[c >> 5] = amax;
   __syncthreads();
-  amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-  // operand scale 2^k keeps the largest entry in [2^13, 2^14): far from fp16
-  // overflow, and the small entries of the lo part stay representable
-  int e = 0;
-  if (amax > 0.f) frexpf(amax, &e);
-  const int k = amax > 0.f ? min(14 - e, 100) : 0;
-  const float s2k = ldexpf(1.f, k);
-  const float inv_f = 1.f / slot_factor(c >> 4);
+  if (half == 0) {
+    float amax = 0.f;
 #pragma unroll
-  for (int m = 0; m < kMaxGqa; ++m) {
-    const float a = acc[m] * s2k * inv_f;
-    const __half hi = __float2half_rn(a);
-    hs[0][m][c] = hi;
-    hs[1][m][c] = __float2half_rn(a - __half2float(hi));
+    for (int m = 0; m < kMaxGqa; ++m) {
+      acc[m] = m < g ? (acc[m] + red[m][c]) * p.scale_log2 : 0.f;
+      amax = fmaxf(amax, fabsf(acc[m]));
+    }
+    amax = warp_maxf(amax);
+    if ((c & 31) == 0) wmax[c >> 5] = amax;
   }
-  uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
-  // group sums of q~ (per head) scaled like the mma results: 2^(k-24) sum q~
-  const float gscale = ldexpf(1.f, k - 24);
+  __syncthreads();
+  if (half == 0) {
+    const float amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+    // operand scale 2^k keeps the largest entry in [2^13, 2^14): far from fp16
+    // overflow, and the small entries of the lo part stay representable
+    int e = 0;
+    if (amax > 0.f) frexpf(amax, &e);
+    const int k = amax > 0.f ? min(14 - e, 100) : 0;
+    const float s2k = ldexpf(1.f, k);
+    const float inv_f = 1.f / slot_factor(c >> 4);
 #pragma unroll
-  for (int m = 0; m < kMaxGqa; ++m) {
-    const float s = warp_sum(acc[m]);
-    if ((c & 31) == 0) rec[1024 + (c >> 5) * 8 + m] = __float_as_uint(s * gscale);
-  }
-  if (c == 0) {
-    rec[1056] = __float_as_uint(ldexpf(1.f, 24 - k));
-    for (int w = 1057; w < kQrecWords; ++w) rec[w] = 0u;
+    for (int m = 0; m < kMaxGqa; ++m) {
+      const float a = acc[m] * s2k * inv_f;
+      const __half hi = __float2half_rn(a);
+      hs[0][m][c] = hi;
+      hs[1][m][c] = __float2half_rn(a - __half2float(hi));
+    }
+    uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
+    // group sums of q~ per head, scaled like the mma results (2^(k-24) sum q~),
+    // split into fp16 hi + lo: the A operand of the zero-point mma
+    const float gscale = ldexpf(1.f, k - 24);
+#pragma unroll
+    for (int m = 0; m < kMaxGqa; ++m) {
+      const float sm = warp_sum(acc[m]) * gscale;
+      if ((c & 31) == 0) {
+        const __half hi = __float2half_rn(sm);
+        gsum[0][m][c >> 5] = hi;
+        gsum[1][m][c >> 5] = __float2half_rn(sm - __half2float(hi));
+      }
+    }
+    if (c == 0) {
+      rec[1088] = __float_as_uint(ldexpf(1.f, 24 - k));
+      for (int w = 1089; w < kQrecWords; ++w) rec[w] = 0u;
+    }
   }
   __syncthreads();
   // A fragments of m16n8k16: rows 0-7 = head hi parts, rows 8-15 = lo parts
+  uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
 #pragma unroll
-  for (int n = 0; n < 8; ++n) {
-    const int widx = c + 128 * n;
+  for (int n = 0; n < 4; ++n) {
+    const int widx = tid + kRotThreads * n;
     const int r = widx & 3, lane = (widx >> 2) & 31, kb = widx >> 7;
     const int gid = lane >> 2, tig = lane & 3;
     const int col = kb * 16 + 2 * tig + (r >= 2 ? 8 : 0);
@@ -172,73 +202,97 @@ __global__ void __launch_bounds__(128) oscar_rotate_q_kernel(DecodeParams p) {
     const uint32_t hi = __half_as_ushort(src[col + 1]);
     rec[widx] = lo | (hi << 16);
   }
+  // zero-point A fragment: row gid = head gid (hi), row gid + 8 = lo; k = group
+  if (tid < 64) {
+    const int lane = tid >> 1, r = tid & 1, gid = lane >> 2, tig = lane & 3;
+    uint32_t w = 0u;
+    if (tig < 2)
+      w = (uint32_t)__half_as_ushort(gsum[r][gid][2 * tig]) |
+          ((uint32_t)__half_as_ushort(gsum[r][gid][2 * tig + 1]) << 16);
+    rec[1024 + tid] = w;
+  }
 }
 
 // --------------------------------------------------------------------------
-// 2a. BF16 sink + recent ring (CTA x = 0)
+// 2a. BF16 sink + recent ring: CTA x < win_slots attends over window tokens
+//     [64 x, 64 x + 64) (sink first, then the ring in position order)
 // --------------------------------------------------------------------------
-__device__ void window_attention(const DecodeParams& p, int b, int h, uint8_t* smem) {
+__device__ void window_attention(const DecodeParams& p, int b, int h, int chunk, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = p.gqa, S = p.sink, W = p.recent;
-  float* qs = reinterpret_cast<float*>(smem);                 // [8][128]
-  float* sc = qs + kMaxGqa * kHeadDim;                        // [8][kMaxWindow]
-  float* stat = sc + kMaxGqa * kMaxWindow;                    // [8][2]
-  float* part = p.part + (((size_t)b * p.num_kv_heads + h) * (p.splits + 1)) * g * kPartFloats;
+  __nv_bfloat16* krows = reinterpret_cast<__nv_bfloat16*>(smem);             // [64][128]
+  __nv_bfloat16* vrows = krows + kWinChunk * kHeadDim;                        // [64][128]
+  float* sc = reinterpret_cast<float*>(vrows + kWinChunk * kHeadDim);         // [8][64]
+  float* stat = sc + kMaxGqa * kWinChunk;                                     // [8][2]
+  const int nslots = p.win_slots + p.splits;
+  float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots + chunk) * g * kPartFloats;
 
   const oscar_seq_state st = p.state[b];
+  const bool ok = state_ok(st, S, W, p.max_batch);
   const int L = st.seq_len, E = st.int2_end;
-  const bool ok = state_ok(L, E, S, W);
   const int ns = ok ? min(S, L) : 0;
   const int rb = max(E, S);
   const int nr = ok && L > rb ? L - rb : 0;
-  const int nw = ns + nr;
+  const int t0 = chunk * kWinChunk;
+  const int n = max(0, min(kWinChunk, ns + nr - t0));
   const size_t slots = (size_t)(S + W);
-  const __nv_bfloat16* wk = p.window + (((size_t)b * p.num_kv_heads + h) * 2 + 0) * slots * kHeadDim;
-  const __nv_bfloat16* wv = p.window + (((size_t)b * p.num_kv_heads + h) * 2 + 1) * slots * kHeadDim;
+  const size_t wrow = ok ? (size_t)st.window_row : 0;
+  const __nv_bfloat16* wk = p.window + ((wrow * p.num_kv_heads + h) * 2 + 0) * slots * kHeadDim;
+  const __nv_bfloat16* wv = p.window + ((wrow * p.num_kv_heads + h) * 2 + 1) * slots * kHeadDim;
 
-  for (int i = tid; i < g * kHeadDim; i += kThreads)
-    qs[i] = __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g) * kHeadDim + i]) * p.scale_log2;
-  __syncthreads();
-  // scores: thread per token, all heads
-  for (int t = tid; t < nw; t += kThreads) {
+  for (int idx = tid; idx < n * 16; idx += kThreads) {
+    const int r = idx >> 4, u = idx & 15, t = t0 + r;
     const int slot = t < ns ? t : S + (rb + t - ns) % W;
-    const uint4* row = reinterpret_cast<const uint4*>(wk + (size_t)slot * kHeadDim);
-    float acc[kMaxGqa];
+    cp_async16(krows + r * kHeadDim + 8 * u, wk + (size_t)slot * kHeadDim + 8 * u);
+    cp_async16(vrows + r * kHeadDim + 8 * u, wv + (size_t)slot * kHeadDim + 8 * u);
+  }
+  cp_commit();
+  // query channels 4*lane .. 4*lane+3 of every head, in registers
+  float qr[kMaxGqa][4];
 #pragma unroll
-    for (int m = 0; m < kMaxGqa; ++m) acc[m] = 0.f;
-#pragma unroll 4
-    for (int u = 0; u < kHeadDim / 8; ++u) {
-      const uint4 w = row[u];
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  for (int m = 0; m < kMaxGqa; ++m) {
+    if (m < g) {
+      const uint2 w = *reinterpret_cast<const uint2*>(
+          p.q + ((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + 4 * lane);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+      qr[m][0] = a.x * p.scale_log2;
+      qr[m][1] = a.y * p.scale_log2;
+      qr[m][2] = c.x * p.scale_log2;
+      qr[m][3] = c.y * p.scale_log2;
+    } else {
+      qr[m][0] = qr[m][1] = qr[m][2] = qr[m][3] = 0.f;
+    }
+  }
+  cp_wait<0>();
+  __syncthreads();
+  // scores: one warp per token, lanes over channels
+  for (int r = warp; r < n; r += kWarps) {
+    const uint2 w = reinterpret_cast<const uint2*>(krows + r * kHeadDim)[lane];
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[e]));
-        const int cidx = u * 8 + 2 * e;
-#pragma unroll
-        for (int m = 0; m < kMaxGqa; ++m) {
-          if (m < g) {
-            acc[m] = fmaf(qs[m * kHeadDim + cidx], kv.x, acc[m]);
-            acc[m] = fmaf(qs[m * kHeadDim + cidx + 1], kv.y, acc[m]);
-          }
-        }
+    for (int m = 0; m < kMaxGqa; ++m) {
+      if (m < g) {
+        float d = qr[m][0] * a.x;
+        d = fmaf(qr[m][1], a.y, d);
+        d = fmaf(qr[m][2], c.x, d);
+        d = fmaf(qr[m][3], c.y, d);
+        d = warp_sum(d);
+        if (lane == 0) sc[m * kWinChunk + r] = d;
       }
     }
-#pragma unroll
-    for (int m = 0; m < kMaxGqa; ++m)
-      if (m < g) sc[m * kMaxWindow + t] = acc[m];
   }
   __syncthreads();
   if (warp < g) {
     float mx = -INFINITY;
-    for (int t = lane; t < nw; t += 32) mx = fmaxf(mx, sc[warp * kMaxWindow + t]);
+    for (int t = lane; t < n; t += 32) mx = fmaxf(mx, sc[warp * kWinChunk + t]);
     mx = warp_maxf(mx);
     float l = 0.f;
-    if (nw > 0) {
-      for (int t = lane; t < nw; t += 32) {
-        const float e = exp2f(sc[warp * kMaxWindow + t] - mx);
-        sc[warp * kMaxWindow + t] = e;
-        l += e;
-      }
+    for (int t = lane; t < n; t += 32) {
+      const float e = exp2f(sc[warp * kWinChunk + t] - mx);
+      sc[warp * kWinChunk + t] = e;
+      l += e;
     }
     l = warp_sum(l);
     if (lane == 0) {
@@ -247,34 +301,146 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, uint8_t* s
     }
   }
   __syncthreads();
-  for (int i = tid; i < g * kHeadDim; i += kThreads) {
-    const int m = i / kHeadDim, c = i % kHeadDim;
-    float acc = 0.f;
-    for (int t = 0; t < nw; ++t) {
-      const int slot = t < ns ? t : S + (rb + t - ns) % W;
-      acc = fmaf(sc[m * kMaxWindow + t], __bfloat162float(wv[(size_t)slot * kHeadDim + c]), acc);
+  // values: thread per (head, channel)
+  const int c = tid & (kHeadDim - 1), m0 = tid >> 7;
+  float acc[kMaxGqa / 2] = {0.f, 0.f, 0.f, 0.f};
+  for (int r = 0; r < n; ++r) {
+    const float v = __bfloat162float(vrows[r * kHeadDim + c]);
+#pragma unroll
+    for (int i = 0; i < kMaxGqa / 2; ++i) {
+      const int m = m0 + 2 * i;
+      if (m < g) acc[i] = fmaf(sc[m * kWinChunk + r], v, acc[i]);
     }
-    float* dst = part + (size_t)m * kPartFloats;
-    dst[c] = acc;
-    if (c == 0) {
-      dst[kHeadDim] = stat[2 * m];
-      dst[kHeadDim + 1] = stat[2 * m + 1];
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxGqa / 2; ++i) {
+    const int m = m0 + 2 * i;
+    if (m < g) {
+      float* dst = part + (size_t)m * kPartFloats;
+      dst[c] = acc[i];
+      if (c == 0) {
+        dst[kHeadDim] = stat[2 * m];
+        dst[kHeadDim + 1] = stat[2 * m + 1];
+      }
     }
   }
 }
 
 // --------------------------------------------------------------------------
-// 2b. INT2 pages (CTA x >= 1)
+// 2b. INT2 pages: CTA x >= win_slots streams split x - win_slots of the pages
 // --------------------------------------------------------------------------
+// 2^x on the SFU (inputs here are <= 15; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Lazy rescaling: the running maximum moves only when a score exceeds it by more
+// than kLazyLog2 (log2 units), so probabilities relative to it stay <= 2^8.
+constexpr float kLazyLog2 = 8.f;
+
+// scores of two staged pages A, B for my tokens (t0, t0+1, t0+8, t0+9), head gid,
+// in units u: u = sum_gq s_k (q~ . code) + sum_gq z_k sum q~ (scaled by 2^(k-24)).
+// u[0..3] page A, u[4..7] page B. qs: the CTA's q~ fragments in shared memory.
+__device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* sbB, const uint4* qs,
+                                            uint2 zq, int lane, float (&u)[8]) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint4 kwA = *reinterpret_cast<const uint4*>(sbA + lane * 16);
+  const uint4 kwB = *reinterpret_cast<const uint4*>(sbB + lane * 16);
+  {
+    // K zeros of tokens gid and gid + 8, groups (2 tig, 2 tig + 1), as mma B operands
+    const int zo = 8 * gid + 4 * tig;
+    const uint32_t kzA0 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbA + 1152 + zo) : 0u;
+    const uint32_t kzA1 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbA + 1216 + zo) : 0u;
+    const uint32_t kzB0 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbB + 1152 + zo) : 0u;
+    const uint32_t kzB1 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbB + 1216 + zo) : 0u;
+    float c[4][4] = {};
+    mma16816(c[0], zq.x, zq.y, 0u, 0u, kzA0, 0u);
+    mma16816(c[1], zq.x, zq.y, 0u, 0u, kzA1, 0u);
+    mma16816(c[2], zq.x, zq.y, 0u, 0u, kzB0, 0u);
+    mma16816(c[3], zq.x, zq.y, 0u, 0u, kzB1, 0u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      u[2 * i] = c[i][0] + c[i][2];
+      u[2 * i + 1] = c[i][1] + c[i][3];
+    }
+  }
+#pragma unroll
+  for (int gq = 0; gq < 4; ++gq) {
+    float a[4][4] = {};
+#define OSCAR_QK(KB)                                                                 \
+  {                                                                                  \
+    const uint4 q4 = qs[(KB) * 32 + lane];                                           \
+    mma16816(a[0], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwA.x), slot_bits<KB>(kwA.y)); \
+    mma16816(a[1], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwA.z), slot_bits<KB>(kwA.w)); \
+    mma16816(a[2], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwB.x), slot_bits<KB>(kwB.y)); \
+    mma16816(a[3], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwB.z), slot_bits<KB>(kwB.w)); \
+  }
+    if (gq == 0) { OSCAR_QK(0) OSCAR_QK(1) }
+    if (gq == 1) { OSCAR_QK(2) OSCAR_QK(3) }
+    if (gq == 2) { OSCAR_QK(4) OSCAR_QK(5) }
+    if (gq == 3) { OSCAR_QK(6) OSCAR_QK(7) }
+#undef OSCAR_QK
+    // K scales of my tokens for this group: (t0, t0+1) and (t0+8, t0+9)
+    const uint2 kA = *reinterpret_cast<const uint2*>(sbA + 1024 + 32 * tig + 8 * gq);
+    const uint2 kB = *reinterpret_cast<const uint2*>(sbB + 1024 + 32 * tig + 8 * gq);
+    const float2 sA01 = h2_bits_to_f2(kA.x), sA23 = h2_bits_to_f2(kA.y);
+    const float2 sB01 = h2_bits_to_f2(kB.x), sB23 = h2_bits_to_f2(kB.y);
+    u[0] = fmaf(sA01.x, a[0][0] + a[0][2], u[0]);
+    u[1] = fmaf(sA01.y, a[0][1] + a[0][3], u[1]);
+    u[2] = fmaf(sA23.x, a[1][0] + a[1][2], u[2]);
+    u[3] = fmaf(sA23.y, a[1][1] + a[1][3], u[3]);
+    u[4] = fmaf(sB01.x, a[2][0] + a[2][2], u[4]);
+    u[5] = fmaf(sB01.y, a[2][1] + a[2][3], u[5]);
+    u[6] = fmaf(sB23.x, a[3][0] + a[3][2], u[6]);
+    u[7] = fmaf(sB23.y, a[3][1] + a[3][3], u[7]);
+  }
+}
+
+// acc[cb] += codes^T (p * s_v) and oz += z_v^T p for one staged page; P01 / P23
+// hold fp16 p * pscale of my tokens; with MASKED, m01 / m23 zero the metadata of
+// masked token slots (whose bytes may be stale)
+template <bool MASKED>
+__device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_t P01, uint32_t P23,
+                                            uint32_t m01, uint32_t m23, float (&acc)[8][4],
+                                            float (&oz)[4]) {
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint4 vw = *reinterpret_cast<const uint4*>(sb + 512 + lane * 16);
+#pragma unroll
+  for (int gq = 0; gq < 4; ++gq) {
+    const uint2 mv = *reinterpret_cast<const uint2*>(sb + 1280 + 16 * (4 * gq + tig));
+    const uint2 mv2 = *reinterpret_cast<const uint2*>(sb + 1280 + 16 * (4 * gq + tig) + 8);
+    const uint32_t B0 = hmul2_bits(P01, MASKED ? (mv.x & m01) : mv.x);
+    const uint32_t B1 = hmul2_bits(P23, MASKED ? (mv2.x & m23) : mv2.x);
+#define OSCAR_PV(CB)                                                                          \
+  mma16816(acc[CB], slot_bits<CB>(vw.x), slot_bits<CB>(vw.y), slot_bits<CB>(vw.z), slot_bits<CB>(vw.w), \
+           B0, B1);
+    if (gq == 0) { OSCAR_PV(0) OSCAR_PV(1) }
+    if (gq == 1) { OSCAR_PV(2) OSCAR_PV(3) }
+    if (gq == 2) { OSCAR_PV(4) OSCAR_PV(5) }
+    if (gq == 3) { OSCAR_PV(6) OSCAR_PV(7) }
+#undef OSCAR_PV
+  }
+  const uint8_t* mz = sb + 1280 + 16 * (4 * (gid & 3) + tig);
+  uint32_t za0 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 4) : 0u;
+  uint32_t za2 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 12) : 0u;
+  if (MASKED) {
+    za0 &= m01;
+    za2 &= m23;
+  }
+  mma16816(oz, za0, 0u, za2, 0u, P01, P23);
+}
+
 __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int g = p.gqa, S = p.sink, W = p.recent;
-  __shared__ int ids[kWarps][kStages];
+  __shared__ uint4 qs[8 * 32];  // q~ fragments of this (request, KV head), shared by all warps
 
   const oscar_seq_state st = p.state[b];
   const int L = st.seq_len, E = st.int2_end;
-  const bool ok = state_ok(L, E, S, W);
+  const bool ok = state_ok(st, S, W, p.max_batch);
   const int lo = S, hi = min(E, L);
   int npages = 0, first = 0;
   if (ok && hi > lo) {
@@ -282,54 +448,53 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     npages = (hi - 1) / kPage - first + 1;
   }
   const int chunk = (npages + p.splits - 1) / p.splits;
-  const int pbeg = first + (split - 1) * chunk;
+  const int pbeg = first + split * chunk;
   const int pend = min(pbeg + chunk, first + npages);
   const int nmine = pend - pbeg - warp > 0 ? (pend - pbeg - warp + kWarps - 1) / kWarps : 0;
 
-  // query operand fragments, group sums, score scale
+  // query operand fragments (see oscar_rotate_q_kernel)
   const uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
-  uint32_t qa[8][4];
-#pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
-    const uint4 w = reinterpret_cast<const uint4*>(rec)[kb * 32 + lane];
-    qa[kb][0] = w.x;
-    qa[kb][1] = w.y;
-    qa[kb][2] = w.z;
-    qa[kb][3] = w.w;
-  }
-  float qsum[4];
-#pragma unroll
-  for (int gq = 0; gq < 4; ++gq) qsum[gq] = __uint_as_float(rec[1024 + gq * 8 + gid]);
-  const float uscale = __uint_as_float(rec[1056]);
-  // probabilities enter the value product as fp16 p * pscale; pscale is the
-  // largest power of two keeping p * pscale * s_v (s_v <= 2 clip_V / 3) finite
+  qs[tid] = reinterpret_cast<const uint4*>(rec)[tid];
+  const uint2 zq = reinterpret_cast<const uint2*>(rec + 1024)[lane];
+  const float uscale = __uint_as_float(rec[1088]);
+  const float tau_u = kLazyLog2 / uscale;
+  // probabilities enter the value product as fp16 p * pscale with p <= 2^8 (lazy
+  // maximum); pv_scale is the largest power of two keeping 2^8 * pv_scale * s_v
+  // (s_v <= 2 clip_V / 3) below the fp16 maximum
   const float pscale = p.pv_scale[h];
+  const float lg_ps = log2f(pscale);
 
   uint8_t* sbuf = smem + warp * kStages * kBlockBytes;
-  const int32_t* ptrow = p.page_table + (size_t)b * p.pt_stride;
+  const int32_t* ptrow = p.page_table + (size_t)b * p.pt_stride + pbeg + warp;
+  const uint8_t* pool_h = p.pool + (size_t)h * kBlockBytes + lane * 16;
+  const size_t page_stride = (size_t)p.num_kv_heads * kBlockBytes;
+  unsigned valid_bits = 0;  // bit (j & 3): page j of this warp has a valid id
 
-  auto issue = [&](int stage, int pidx) {
-    int id = ptrow[pidx];
-    if (id < 0 || id >= p.num_pages) {
-      if (lane == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
-      id = -1;
-    }
-    if (lane == 0) ids[warp][stage] = id;
-    if (id >= 0) {
-      const uint8_t* src = p.pool + ((int64_t)id * p.num_kv_heads + h) * kBlockBytes;
-      uint8_t* dst = sbuf + stage * kBlockBytes;
-      cp_async16(dst + lane * 16, src + lane * 16);
-      cp_async16(dst + 512 + lane * 16, src + 512 + lane * 16);
-      cp_async16(dst + 1024 + lane * 16, src + 1024 + lane * 16);
+  auto issue = [&](int j) {
+    const int id = ptrow[kWarps * j];
+    const bool good = id >= 0 && id < p.num_pages;
+    const unsigned bit = 1u << (j & (kStages - 1));
+    valid_bits = good ? (valid_bits | bit) : (valid_bits & ~bit);
+    if (good) {
+      const uint8_t* src = pool_h + (size_t)id * page_stride;
+      uint8_t* dst = sbuf + (j & (kStages - 1)) * kBlockBytes + lane * 16;
+      cp_async16(dst, src);
+      cp_async16(dst + 512, src + 512);
+      cp_async16(dst + 1024, src + 1024);
+    } else if (lane == 0) {
+      atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
     }
   };
 
 #pragma unroll
   for (int s = 0; s < kStages; ++s) {
-    if (s < nmine) issue(s, pbeg + warp + kWarps * s);
+    if (s < nmine) issue(s);
     cp_commit();
   }
+  __syncthreads();  // q~ fragments visible to every warp
 
+  // running (lazy) max in score units u (log2 units = u * uscale), running sum and
+  // accumulators in units of pscale
   float m_run = -INFINITY, l_run = 0.f;
   float acc[8][4];
   float oz[4] = {0.f, 0.f, 0.f, 0.f};
@@ -338,108 +503,83 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
   const int t0 = 2 * tig;  // my tokens: t0, t0+1, t0+8, t0+9
 
-  for (int it = 0; it < nmine; ++it) {
-    cp_wait<kStages - 1>();
+  // pages are consumed two at a time (one softmax update per pair)
+  for (int j = 0; j < nmine; j += 2) {
+    const bool two = j + 1 < nmine;
+    if (two) cp_wait<kStages - 2>(); else cp_wait<kStages - 1>();
     __syncwarp();
-    const int stage = it % kStages;
-    const int pidx = pbeg + warp + kWarps * it;
-    const uint8_t* sb = sbuf + stage * kBlockBytes;
-    const int id = ids[warp][stage];
-    const int pos0 = pidx * kPage;
-    const bool full = id >= 0 && pos0 >= lo && pos0 + kPage <= hi;
-    bool vld[4] = {true, true, true, true};
+    const uint8_t* sbA = sbuf + (j & (kStages - 1)) * kBlockBytes;
+    const uint8_t* sbB = sbuf + ((j + 1) & (kStages - 1)) * kBlockBytes;
+    const bool okA = (valid_bits >> (j & (kStages - 1))) & 1u;
+    const bool okB = two && ((valid_bits >> ((j + 1) & (kStages - 1))) & 1u);
+    const int posA = (pbeg + warp + kWarps * j) * kPage;
+    const int posB = posA + kWarps * kPage;
+    const bool full = okA && okB && posA >= lo && posA + kPage <= hi && posB >= lo && posB + kPage <= hi;
+
+    float u[8];
+    pair_scores(sbA, sbB, qs, zq, lane, u);
+    uint32_t mA01 = 0xffffffffu, mA23 = 0xffffffffu, mB01 = 0xffffffffu, mB23 = 0xffffffffu;
     if (!full) {
+      bool v[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int pos = pos0 + t0 + (i & 1) + 8 * (i >> 1);
-        vld[i] = id >= 0 && pos >= lo && pos < hi;
+        const int off = t0 + (i & 1) + 8 * (i >> 1);
+        v[i] = okA && posA + off >= lo && posA + off < hi;
+        v[4 + i] = okB && posB + off >= lo && posB + off < hi;
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = v[i] ? u[i] : -INFINITY;
+      mA01 = (v[0] ? 0x0000ffffu : 0u) | (v[1] ? 0xffff0000u : 0u);
+      mA23 = (v[2] ? 0x0000ffffu : 0u) | (v[3] ? 0xffff0000u : 0u);
+      mB01 = (v[4] ? 0x0000ffffu : 0u) | (v[5] ? 0xffff0000u : 0u);
+      mB23 = (v[6] ? 0x0000ffffu : 0u) | (v[7] ? 0xffff0000u : 0u);
     }
-    if (id >= 0) {
-      const uint4 kw = *reinterpret_cast<const uint4*>(sb + lane * 16);
-      const uint4 vw = *reinterpret_cast<const uint4*>(sb + 512 + lane * 16);
 
-      // ---- scores: u = sum_gq s_k * (q~ . code) + z_k * sum q~ -------------
-      float u[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- online softmax over the pair, per head gid (lazy maximum) -------------
+    float mx = fmaxf(fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3])), fmaxf(fmaxf(u[4], u[5]), fmaxf(u[6], u[7])));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    // (mx and m_run are both -inf only while nothing valid was seen: warp-uniform)
+    if (!(mx == -INFINITY && m_run == -INFINITY)) {
+    const bool bump = mx > m_run + tau_u;
+    if (__any_sync(0xffffffffu, bump)) {
+      const float m_new = bump ? mx : m_run;
+      const float alpha = bump ? ex2((m_run - m_new) * uscale) : 1.f;
+      m_run = m_new;
+      l_run *= alpha;
+      const float ae = __shfl_sync(0xffffffffu, alpha, 8 * tig);
+      const float ao = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
 #pragma unroll
-      for (int gq = 0; gq < 4; ++gq) {
-        const uint4 mk = *reinterpret_cast<const uint4*>(sb + 1024 + 16 * (4 * gq + tig));
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#define OSCAR_QK(KB)                                                                              \
-  mma16816(c0, qa[KB][0], qa[KB][1], qa[KB][2], qa[KB][3], slot_bits<KB>(kw.x), slot_bits<KB>(kw.y)); \
-  mma16816(c1, qa[KB][0], qa[KB][1], qa[KB][2], qa[KB][3], slot_bits<KB>(kw.z), slot_bits<KB>(kw.w));
-        if (gq == 0) { OSCAR_QK(0) OSCAR_QK(1) }
-        if (gq == 1) { OSCAR_QK(2) OSCAR_QK(3) }
-        if (gq == 2) { OSCAR_QK(4) OSCAR_QK(5) }
-        if (gq == 3) { OSCAR_QK(6) OSCAR_QK(7) }
-#undef OSCAR_QK
-        const float2 s01 = h2_bits_to_f2(mk.x), z01 = h2_bits_to_f2(mk.y);
-        const float2 s23 = h2_bits_to_f2(mk.z), z23 = h2_bits_to_f2(mk.w);
-        u[0] += s01.x * (c0[0] + c0[2]) + z01.x * qsum[gq];
-        u[1] += s01.y * (c0[1] + c0[3]) + z01.y * qsum[gq];
-        u[2] += s23.x * (c1[0] + c1[2]) + z23.x * qsum[gq];
-        u[3] += s23.y * (c1[1] + c1[3]) + z23.y * qsum[gq];
+      for (int cb = 0; cb < 8; ++cb) {
+        acc[cb][0] *= ae;
+        acc[cb][1] *= ao;
+        acc[cb][2] *= ae;
+        acc[cb][3] *= ao;
       }
-
-      // ---- online softmax (log2 domain), per head gid -----------------------
-      float s[4];
+      oz[0] *= ae;
+      oz[1] *= ao;
+      oz[2] *= ae;
+      oz[3] *= ao;
+    }
+    const float nb = fmaf(-m_run, uscale, lg_ps);
+    float pr[8];  // p * pscale, p <= 2^8
 #pragma unroll
-      for (int i = 0; i < 4; ++i) s[i] = vld[i] ? u[i] * uscale : -INFINITY;
-      float mx = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      if (m_new != -INFINITY) {
-        const float alpha = exp2f(m_run - m_new);
-        float pr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) pr[i] = exp2f(s[i] - m_new);
-        l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-        m_run = m_new;
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const float ae = __shfl_sync(0xffffffffu, alpha, 8 * tig);
-          const float ao = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
-#pragma unroll
-          for (int cb = 0; cb < 8; ++cb) {
-            acc[cb][0] *= ae;
-            acc[cb][1] *= ao;
-            acc[cb][2] *= ae;
-            acc[cb][3] *= ao;
-          }
-          oz[0] *= ae;
-          oz[1] *= ao;
-          oz[2] *= ae;
-          oz[3] *= ao;
-        }
-        const uint32_t P01 = f2_to_h2_bits(pr[0] * pscale, pr[1] * pscale);
-        const uint32_t P23 = f2_to_h2_bits(pr[2] * pscale, pr[3] * pscale);
-        const uint32_t m01 = (vld[0] ? 0x0000ffffu : 0u) | (vld[1] ? 0xffff0000u : 0u);
-        const uint32_t m23 = (vld[2] ? 0x0000ffffu : 0u) | (vld[3] ? 0xffff0000u : 0u);
-
-        // ---- values: acc[cb] += codes^T (p * s_v) ; oz += z_v^T p -------------
-#pragma unroll
-        for (int gq = 0; gq < 4; ++gq) {
-          const uint4 mv = *reinterpret_cast<const uint4*>(sb + 1024 + 16 * (4 * (4 + gq) + tig));
-          const uint32_t B0 = hmul2_bits(P01, mv.x & m01);
-          const uint32_t B1 = hmul2_bits(P23, mv.z & m23);
-#define OSCAR_PV(CB)                                                                          \
-  mma16816(acc[CB], slot_bits<CB>(vw.x), slot_bits<CB>(vw.y), slot_bits<CB>(vw.z), slot_bits<CB>(vw.w), \
-           B0, B1);
-          if (gq == 0) { OSCAR_PV(0) OSCAR_PV(1) }
-          if (gq == 1) { OSCAR_PV(2) OSCAR_PV(3) }
-          if (gq == 2) { OSCAR_PV(4) OSCAR_PV(5) }
-          if (gq == 3) { OSCAR_PV(6) OSCAR_PV(7) }
-#undef OSCAR_PV
-        }
-        const uint4 mz = *reinterpret_cast<const uint4*>(sb + 1024 + 16 * (4 * (4 + (gid & 3)) + tig));
-        const uint32_t za0 = gid < 4 ? (mz.y & m01) : 0u;
-        const uint32_t za2 = gid < 4 ? (mz.w & m23) : 0u;
-        mma16816(oz, za0, 0u, za2, 0u, P01, P23);
-      }
+    for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], uscale, nb));
+    l_run += ((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
+    const uint32_t PA01 = f2_to_h2_bits(pr[0], pr[1]), PA23 = f2_to_h2_bits(pr[2], pr[3]);
+    const uint32_t PB01 = f2_to_h2_bits(pr[4], pr[5]), PB23 = f2_to_h2_bits(pr[6], pr[7]);
+    if (full) {
+      page_values<false>(sbA, lane, PA01, PA23, 0u, 0u, acc, oz);
+      page_values<false>(sbB, lane, PB01, PB23, 0u, 0u, acc, oz);
+    } else {
+      page_values<true>(sbA, lane, PA01, PA23, mA01, mA23, acc, oz);
+      page_values<true>(sbB, lane, PB01, PB23, mB01, mB23, acc, oz);
+    }
     }
     __syncwarp();
-    const int nxt = it + kStages;
-    if (nxt < nmine) issue(stage, pbeg + warp + kWarps * nxt);
+    if (j + kStages < nmine) issue(j + kStages);
+    cp_commit();
+    if (j + 1 + kStages < nmine) issue(j + 1 + kStages);
     cp_commit();
   }
   cp_wait<0>();
@@ -447,29 +587,31 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   // ---- per-warp partial -> shared memory, then CTA merge --------------------
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  const float inv_ps = 1.f / pscale;
   __syncthreads();  // staging buffers are reused below
   float* wpart = reinterpret_cast<float*>(smem);              // [8 warps][8 heads][128]
   float* wml = wpart + kWarps * kMaxGqa * kHeadDim;           // [8 warps][8 heads][2]
   if (tig == 0) {
-    wml[(warp * kMaxGqa + gid) * 2] = m_run;
-    wml[(warp * kMaxGqa + gid) * 2 + 1] = l_run;
+    wml[(warp * kMaxGqa + gid) * 2] = m_run * uscale;           // log2 units
+    wml[(warp * kMaxGqa + gid) * 2 + 1] = l_run * inv_ps;
   }
 #pragma unroll
   for (int cb = 0; cb < 8; ++cb) {
     const int gq = cb >> 1;
-    const float ze = __shfl_sync(0xffffffffu, oz[0], 4 * gq + tig) / pscale;
-    const float zo = __shfl_sync(0xffffffffu, oz[1], 4 * gq + tig) / pscale;
-    const float sc = 16777216.f / (slot_factor(cb) * pscale);
+    const float ze = __shfl_sync(0xffffffffu, oz[0], 4 * gq + tig) * inv_ps;
+    const float zo = __shfl_sync(0xffffffffu, oz[1], 4 * gq + tig) * inv_ps;
+    const float sc = 16777216.f / slot_factor(cb) * inv_ps;
     const int ch = 16 * cb + gid;
     const int he = 2 * tig, ho = 2 * tig + 1;
     float* base = wpart + warp * kMaxGqa * kHeadDim;
-    base[he * kHeadDim + ch] = acc[cb][0] * sc + ze;
-    base[ho * kHeadDim + ch] = acc[cb][1] * sc + zo;
-    base[he * kHeadDim + ch + 8] = acc[cb][2] * sc + ze;
-    base[ho * kHeadDim + ch + 8] = acc[cb][3] * sc + zo;
+    base[he * kHeadDim + ch] = fmaf(acc[cb][0], sc, ze);
+    base[ho * kHeadDim + ch] = fmaf(acc[cb][1], sc, zo);
+    base[he * kHeadDim + ch + 8] = fmaf(acc[cb][2], sc, ze);
+    base[ho * kHeadDim + ch + 8] = fmaf(acc[cb][3], sc, zo);
   }
   __syncthreads();
-  float* part = p.part + (((size_t)b * p.num_kv_heads + h) * (p.splits + 1) + split) * g * kPartFloats;
+  float* part = p.part + (((size_t)b * p.num_kv_heads + h) * (p.win_slots + p.splits) + p.win_slots +
+                           split) * g * kPartFloats;
   for (int i = tid; i < g * kHeadDim; i += kThreads) {
     const int m = i / kHeadDim, c = i % kHeadDim;
     float M = -INFINITY;
@@ -481,8 +623,8 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
       for (int w = 0; w < kWarps; ++w) {
         const float mw = wml[(w * kMaxGqa + m) * 2];
         const float sw = mw == -INFINITY ? 0.f : exp2f(mw - M);
-        o += sw * wpart[(w * kMaxGqa + m) * kHeadDim + c];
-        l += sw * wml[(w * kMaxGqa + m) * 2 + 1];
+        o = fmaf(sw, wpart[(w * kMaxGqa + m) * kHeadDim + c], o);
+        l = fmaf(sw, wml[(w * kMaxGqa + m) * 2 + 1], l);
       }
     }
     float* dst = part + (size_t)m * kPartFloats;
@@ -496,75 +638,102 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
 __global__ void __launch_bounds__(kThreads, 2) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  if (split == 0)
-    window_attention(p, b, h, smem);
+  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (x < p.win_slots)
+    window_attention(p, b, h, x, smem);
   else
-    int2_attention(p, b, h, split, smem);
+    int2_attention(p, b, h, x - p.win_slots, smem);
 }
 
 // --------------------------------------------------------------------------
 // 3. merge of the partials, un-rotation, normalisation
 // --------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) oscar_merge_kernel(DecodeParams p) {
-  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
-  const int g = p.gqa, nslots = p.splits + 1;
-  __shared__ float orot[kMaxGqa][kHeadDim];
+constexpr int kMergeThreads = 256;
+constexpr int kMaxSlots = 256 + kMaxWindow / kWinChunk;   // INT2 splits + window chunks
+constexpr int kMergeSmem = kRotSmem + kMaxSlots * kMaxGqa * 2 * 4 + kMaxGqa * kHeadDim * 4;
+
+__global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  float* RT = reinterpret_cast<float*>(dsm);                   // R_V^T[h], [128][128]
+  float* wts = RT + kHeadDim * kHeadDim;                        // [slots][8] weights, then l
+  float* orot = wts + kMaxSlots * kMaxGqa * 2;                  // [8][128]
+  __shared__ float lsum_s[kMaxGqa];
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int g = p.gqa, nslots = p.win_slots + p.splits, nwin = p.win_slots;
   const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
-  float ow[kMaxGqa], lsum[kMaxGqa];
-#pragma unroll
-  for (int m = 0; m < kMaxGqa; ++m) {
-    ow[m] = 0.f;
-    lsum[m] = 0.f;
-    if (m >= g) continue;
-    float M = -INFINITY;
-    for (int s = 0; s < nslots; ++s) M = fmaxf(M, part[((size_t)s * g + m) * kPartFloats + kHeadDim]);
-    float orr = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < nslots; ++s) {
-        const float* ps = part + ((size_t)s * g + m) * kPartFloats;
-        const float ms = ps[kHeadDim];
-        if (ms == -INFINITY) continue;
-        const float w = exp2f(ms - M);
-        lsum[m] += w * ps[kHeadDim + 1];
-        const float v = w * ps[c];
-        if (s == 0)
-          ow[m] = v;
-        else
-          orr += v;
-      }
-    }
-    orot[m][c] = orr;
+  if (!p.fold_rv) stage_matrix(RT, p.R_VT + (size_t)h * kHeadDim * kHeadDim, tid, kMergeThreads);
+  else cp_commit();
+  // (m, l) of every slot and head
+  float* ml = wts + kMaxSlots * kMaxGqa;                        // [slots][8] l values
+  for (int i = tid; i < nslots * g; i += kMergeThreads) {
+    const int sidx = i / g, m = i % g;
+    const float* ps = part + ((size_t)sidx * g + m) * kPartFloats;
+    wts[sidx * kMaxGqa + m] = ps[kHeadDim];
+    ml[sidx * kMaxGqa + m] = ps[kHeadDim + 1];
   }
   __syncthreads();
-  const float* RT = p.R_VT + (size_t)h * kHeadDim * kHeadDim;
-  float oi[kMaxGqa];
-#pragma unroll
-  for (int m = 0; m < kMaxGqa; ++m) oi[m] = 0.f;
-  if (p.fold_rv) {
-#pragma unroll
-    for (int m = 0; m < kMaxGqa; ++m)
-      if (m < g) oi[m] = orot[m][c];
-  } else {
-#pragma unroll 4
-    for (int i = 0; i < kHeadDim; ++i) {
-      const float r = __ldg(&RT[i * kHeadDim + c]);
-#pragma unroll
-      for (int m = 0; m < kMaxGqa; ++m)
-        if (m < g) oi[m] = fmaf(orot[m][i], r, oi[m]);
+  // weights exp2(m_s - M) per head, one warp per head
+  if (warp < g) {
+    float M = -INFINITY;
+    for (int sidx = lane; sidx < nslots; sidx += 32) M = fmaxf(M, wts[sidx * kMaxGqa + warp]);
+    M = warp_maxf(M);
+    float l = 0.f;
+    for (int sidx = lane; sidx < nslots; sidx += 32) {
+      const float ms = wts[sidx * kMaxGqa + warp];
+      const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      wts[sidx * kMaxGqa + warp] = w;
+      l += w * ml[sidx * kMaxGqa + warp];
     }
+    l = warp_sum(l);
+    if (lane == 0) lsum_s[warp] = l;
   }
+  __syncthreads();
+  // thread (channel c, heads m0, m0 + 2, ...): weighted sums of the partials
+  const int c = tid & (kHeadDim - 1), m0 = tid >> 7;
+  float ow[kMaxGqa / 2];
 #pragma unroll
-  for (int m = 0; m < kMaxGqa; ++m) {
+  for (int i = 0; i < kMaxGqa / 2; ++i) {
+    const int m = m0 + 2 * i;
+    ow[i] = 0.f;
     if (m >= g) continue;
-    const float val = lsum[m] > 0.f ? (oi[m] + ow[m]) / lsum[m] : 0.f;
-    p.o[((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + c] = val;
+    float owin = 0.f;
+    for (int sidx = 0; sidx < nwin; ++sidx)
+      owin = fmaf(wts[sidx * kMaxGqa + m], part[((size_t)sidx * g + m) * kPartFloats + c], owin);
+    ow[i] = owin;
+    // INT2 slots: independent loads, eight in flight per thread
+    float o8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int sidx = nwin;
+    for (; sidx + 8 <= nslots; sidx += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        o8[u] = fmaf(wts[(sidx + u) * kMaxGqa + m], part[((size_t)(sidx + u) * g + m) * kPartFloats + c], o8[u]);
+    }
+    for (; sidx < nslots; ++sidx)
+      o8[0] = fmaf(wts[sidx * kMaxGqa + m], part[((size_t)sidx * g + m) * kPartFloats + c], o8[0]);
+    orot[m * kHeadDim + c] = ((o8[0] + o8[1]) + (o8[2] + o8[3])) + ((o8[4] + o8[5]) + (o8[6] + o8[7]));
+  }
+  cp_wait<0>();
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kMaxGqa / 2; ++i) {
+    const int m = m0 + 2 * i;
+    if (m >= g) continue;
+    float oi;
+    if (p.fold_rv) {
+      oi = orot[m * kHeadDim + c];
+    } else {
+      oi = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < kHeadDim; ++j) oi = fmaf(orot[m * kHeadDim + j], RT[j * kHeadDim + c], oi);
+    }
+    const float l = lsum_s[m];
+    p.o[((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + c] = l > 0.f ? (oi + ow[i]) / l : 0.f;
   }
 }
 
-
 int decode_smem_bytes() {
-  const int window = (kMaxGqa * kHeadDim + kMaxGqa * kMaxWindow + 2 * kMaxGqa) * 4;
+  const int window = 2 * kWinChunk * kHeadDim * 2 + (kMaxGqa * kWinChunk + 2 * kMaxGqa) * 4;
   const int merge = (kWarps * kMaxGqa * kHeadDim + kWarps * kMaxGqa * 2) * 4;
   int m = kStageBytes;
   if (window > m) m = window;
@@ -577,12 +746,17 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s) {
   const int smem = decode_smem_bytes();
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(oscar_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(oscar_rotate_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(oscar_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  oscar_rotate_q_kernel<<<dim3(p.num_kv_heads, batch), 128, 0, s>>>(p);
-  oscar_decode_kernel<<<dim3(p.splits + 1, p.num_kv_heads, batch), kThreads, smem, s>>>(p);
-  oscar_merge_kernel<<<dim3(p.num_kv_heads, batch), 128, 0, s>>>(p);
+  if (p.win_slots + p.splits > kMaxSlots) return cudaErrorInvalidValue;
+  oscar_rotate_q_kernel<<<dim3(p.num_kv_heads, batch), kRotThreads, kRotSmem, s>>>(p);
+  oscar_decode_kernel<<<dim3(p.win_slots + p.splits, p.num_kv_heads, batch), kThreads, smem, s>>>(p);
+  oscar_merge_kernel<<<dim3(p.num_kv_heads, batch), kMergeThreads, kMergeSmem, s>>>(p);
   return cudaGetLastError();
 }
 

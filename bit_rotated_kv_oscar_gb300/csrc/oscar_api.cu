@@ -73,6 +73,10 @@ int check_config_msg(const oscar_config* c, std::string* msg) {
     *msg = "query group size must be 1, 2, 4 or 8";
     return OSCAR_ERR_UNSUPPORTED;
   }
+  if (c->num_splits > 256) {
+    *msg = "num_splits must not exceed 256";
+    return OSCAR_ERR_UNSUPPORTED;
+  }
   if (c->sink + c->recent > 1024) {
     *msg = "sink + recent must not exceed 1024";
     return OSCAR_ERR_UNSUPPORTED;
@@ -94,9 +98,12 @@ int auto_splits(const oscar_ctx* ctx, int batch) {
   int64_t s = by_wave > by_pages ? by_wave : by_pages;
   const int64_t cap = (pages + 7) / 8;  // keep >= 8 pages per split
   if (s > cap) s = cap;
+  if (s > 256) s = 256;
   if (s < 1) s = 1;
   return (int)s;
 }
+
+int win_slots(const oscar_config* c) { return (c->sink + c->recent + kWindowChunk - 1) / kWindowChunk; }
 
 template <class T>
 cudaError_t dalloc(T** p, size_t bytes) {
@@ -182,8 +189,8 @@ int oscar_create(const oscar_config* cfg, oscar_ctx** out) {
     e = dalloc(&ctx->qrec, (size_t)cfg->max_batch * hkv * kQrecWords * sizeof(uint32_t));
   }
   if (e == cudaSuccess)
-    e = dalloc(&ctx->part, (size_t)cfg->max_batch * hkv * (ctx->max_splits + 1) * g * kPartFloats *
-                               sizeof(float));
+    e = dalloc(&ctx->part, (size_t)cfg->max_batch * hkv * (ctx->max_splits + win_slots(cfg)) * g *
+                               kPartFloats * sizeof(float));
   if (e == cudaSuccess) e = dalloc(&ctx->flags, 2 * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(ctx->flags, 0, 2 * sizeof(uint32_t));
   if (e != cudaSuccess) {
@@ -226,10 +233,11 @@ int oscar_load_rotations(oscar_ctx* ctx, const float* R_K, const float* R_V, con
           return fail(ctx, OSCAR_ERR_INVALID_ARG, "load_rotations: non-finite rotation entry");
         rvt[((size_t)h * kHeadDim + j) * kHeadDim + i] = bv;
       }
-    // largest power of two with pscale * (2 clip_V / 3) * 1.01 <= 65504, at most 2^15
-    const double smax = 2.0 * clip_V[h] / 3.0 * 1.01;
+    // largest power of two with 2^8 * pscale * (2 clip_V / 3) * 1.01 <= 65504, at most
+    // 2^7: decode feeds fp16 p * pscale * s_v to the tensor cores with p <= 2^8
+    const double smax = 2.0 * clip_V[h] / 3.0 * 1.01 * 256.0;
     int ex = (int)floor(log2(65504.0 / smax));
-    if (ex > 15) ex = 15;
+    if (ex > 7) ex = 7;
     if (ex < -30) ex = -30;
     ps[h] = ldexpf(1.f, ex);
   }
@@ -278,6 +286,7 @@ static int append_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_stat
   p.recent = ctx->cfg.recent;
   p.n_new = n_new;
   p.batch = batch;
+  p.max_batch = ctx->cfg.max_batch;
   p.fold_rv = ctx->cfg.fold_rv;
   p.trace = trace;
   p.trace_positions = trace ? trace_positions : 0;
@@ -334,7 +343,9 @@ int oscar_decode_attn(oscar_ctx* ctx, const void* q, const int32_t* page_table,
   p.sink = ctx->cfg.sink;
   p.recent = ctx->cfg.recent;
   p.splits = auto_splits(ctx, batch);
+  p.win_slots = win_slots(&ctx->cfg);
   p.fold_rv = ctx->cfg.fold_rv;
+  p.max_batch = ctx->cfg.max_batch;
   p.scale_log2 = ctx->cfg.softmax_scale * 1.4426950408889634f;
   p.err_flags = ctx->flags;
   cudaError_t e = launch_decode(p, batch, static_cast<cudaStream_t>(stream));

@@ -10,6 +10,13 @@
 
 namespace oscar {
 
+// a sequence state the kernels accept (see the invariants in oscar.h)
+__host__ __device__ __forceinline__ bool state_ok(const oscar_seq_state& st, int S, int W, int max_batch) {
+  const int L = st.seq_len, E = st.int2_end;
+  return L >= 0 && E >= S && E <= (L > S ? L : S) && L - E <= W && st.window_row >= 0 &&
+         st.window_row < max_batch;
+}
+
 constexpr int kHeadDim = 128;
 constexpr int kPage = 16;
 constexpr int kGroup = 32;
@@ -17,9 +24,11 @@ constexpr int kGroups = kHeadDim / kGroup;   // 4 quantisation groups per token
 constexpr int kBlockBytes = OSCAR_PAGE_BLOCK_BYTES;
 constexpr int kMaxGqa = 8;
 // per-(request, KV head) record written by the query-rotation kernel:
-// 1024 words of fp16x2 mma A fragments, 32 floats of group sums, 1 float scale
-constexpr int kQrecWords = 1088;
+// [0, 1024) fp16x2 mma A fragments of q~ (hi/lo), [1024, 1088) A fragments of the
+// per-group sums of q~ (hi/lo), [1088] the score scale, rest zero
+constexpr int kQrecWords = 1104;
 constexpr int kPartFloats = kHeadDim + 2;    // o[128], m, l
+constexpr int kWindowChunk = 64;             // BF16 window tokens per decode CTA
 
 struct AppendParams {
   const int32_t* page_table;
@@ -34,7 +43,7 @@ struct AppendParams {
   const float* R_V;
   const float* clip_K;      // [Hkv]
   const float* clip_V;
-  int32_t num_kv_heads, sink, recent, n_new, batch;
+  int32_t num_kv_heads, sink, recent, n_new, batch, max_batch;
   int32_t fold_rv;          // 1: V arrives already rotated (R_V folded into the projection)
   float* trace;             // optional [B][trace_positions][Hkv][2][128]
   int32_t trace_positions;
@@ -53,10 +62,11 @@ struct DecodeParams {
   const float* R_K;         // [Hkv][128][128]
   const float* R_VT;        // [Hkv][128][128], R_VT[h][i][j] = R_V[h][j][i]
   uint32_t* qrec;           // [B][Hkv][kQrecWords]
-  float* part;              // [B][Hkv][splits + 1][gqa][kPartFloats]
+  float* part;              // [B][Hkv][win_slots + splits][gqa][kPartFloats]
   float* o;                 // [B][Hq][128]
   const float* pv_scale;    // [Hkv] power of two applied to p * s_v before fp16 rounding
-  int32_t num_q_heads, num_kv_heads, gqa, sink, recent, splits, fold_rv;
+  int32_t num_q_heads, num_kv_heads, gqa, sink, recent, splits, fold_rv, max_batch;
+  int32_t win_slots;        // CTAs over the BF16 window, 64 tokens each
   float scale_log2;         // softmax_scale * log2(e)
   uint32_t* err_flags;
 };

@@ -26,18 +26,13 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
-__device__ __forceinline__ bool state_ok(int L, int E, int S, int W) {
-  return L >= 0 && E >= S && E <= (L > S ? L : S) && L - E <= W;
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem));
 }
 
-// page block of (request b, position pos, KV head h) or nullptr (flag raised)
-__device__ __forceinline__ uint8_t* block_of(const AppendParams& p, int b, int64_t pos, int h) {
-  int64_t pidx = pos / kPage;
-  if (pidx >= p.pt_stride) {
-    atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
-    return nullptr;
-  }
-  int32_t id = p.page_table[(int64_t)b * p.pt_stride + pidx];
+// page block for page-table entry `id` (nullptr and a flag when out of range)
+__device__ __forceinline__ uint8_t* block_of(const AppendParams& p, int32_t id, int h) {
   if (id < 0 || id >= p.num_pages) {
     atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
     return nullptr;
@@ -45,156 +40,201 @@ __device__ __forceinline__ uint8_t* block_of(const AppendParams& p, int b, int64
   return p.pool + ((int64_t)id * p.num_kv_heads + h) * kBlockBytes;
 }
 
-__global__ void __launch_bounds__(kThreads)
+constexpr int kTokensPerCta = 16;
+constexpr int kAppendSmem = 2 * kHeadDim * kHeadDim * 4;  // R_K[h] and R_V[h]
+
+__global__ void __launch_bounds__(kThreads, 1)
 oscar_quant_append_kernel(AppendParams p) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  float* Rs = reinterpret_cast<float*>(dsm);  // [2][128][128]: R_K[h], R_V[h]
   const int tid = threadIdx.x;
-  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int j0 = blockIdx.x * kTokensPerCta;
+  const int j1 = min(j0 + kTokensPerCta, p.n_new);
   const int S = p.sink, W = p.recent;
   const int Hkv = p.num_kv_heads;
 
-  __shared__ int s_L, s_E, s_last;
+  __shared__ oscar_seq_state s_st;
+  __shared__ int s_last, s_page;
   __shared__ float xs[2][kHeadDim];            // token being quantised, K and V
   __shared__ float red[2][2][kHeadDim];        // partial dot products
   __shared__ uint8_t codes[2][kHeadDim];
   __shared__ __half meta[2][kGroups][2];
 
   if (tid == 0) {
-    oscar_seq_state st = p.state[b];
-    s_L = st.seq_len;
-    s_E = st.int2_end;
+    s_st = p.state[b];
     __threadfence();
-    unsigned total = gridDim.x * gridDim.y * gridDim.z;
+    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
     s_last = (atomicAdd(p.counter, 1u) == total - 1u);
   }
   __syncthreads();
-  const int L = s_L, E = s_E;
-  const bool ok = state_ok(L, E, S, W);
-  if (!ok && tid == 0 && j == 0 && h == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_STATE);
+  const oscar_seq_state st = s_st;
+  const int L = st.seq_len, E = st.int2_end;
+  const bool ok = state_ok(st, S, W, p.max_batch);
+  if (!ok && tid == 0 && blockIdx.x == 0 && h == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_STATE);
 
   if (ok) {
-    const int64_t q = (int64_t)L + j;
     int64_t E2 = (int64_t)L + p.n_new - W;
     if (E2 < E) E2 = E;
     if (E2 < S) E2 = S;
     const size_t slots = (size_t)(S + W);
-    __nv_bfloat16* win_k = p.window + (((size_t)b * Hkv + h) * 2 + 0) * slots * kHeadDim;
-    __nv_bfloat16* win_v = p.window + (((size_t)b * Hkv + h) * 2 + 1) * slots * kHeadDim;
-    const size_t in_off = (((size_t)b * p.n_new + j) * Hkv + h) * kHeadDim;
+    const size_t wrow = (size_t)st.window_row;
+    __nv_bfloat16* win_k = p.window + ((wrow * Hkv + h) * 2 + 0) * slots * kHeadDim;
+    __nv_bfloat16* win_v = p.window + ((wrow * Hkv + h) * 2 + 1) * slots * kHeadDim;
 
-    // what this CTA quantises: -1 none, else the position; and where it comes from
-    int64_t qpos = -1;
-    const __nv_bfloat16* src_k = nullptr;
-    const __nv_bfloat16* src_v = nullptr;
-    int64_t ring_slot_new = -1;
-    if (q < S) {
-      // sink token: BF16 copy
-      if (tid < kHeadDim) {
-        win_k[(size_t)q * kHeadDim + tid] = p.k[in_off + tid];
-        win_v[(size_t)q * kHeadDim + tid] = p.v[in_off + tid];
+    // stage the rotations once for all tokens of this CTA if any is quantised
+    bool any_q = false;
+    for (int j = j0; j < j1; ++j) {
+      const int64_t q = (int64_t)L + j;
+      if (q >= S && q < E2) any_q = true;
+      if (q >= E2) {
+        const int64_t pe = q - (int64_t)W * ((q - L) / W + 1);
+        if (pe >= E && pe < E2 && pe >= S) any_q = true;
       }
-    } else if (q < E2) {
-      qpos = q;
-      src_k = p.k + in_off;
-      src_v = p.v + in_off;
-    } else {
-      // ring occupant; the entry at its slot may have to be quantised first
-      const int64_t pe = q - (int64_t)W * ((q - L) / W + 1);
-      if (pe >= E && pe < E2 && pe >= S) {
-        qpos = pe;
-        const size_t sl = (size_t)(S + pe % W) * kHeadDim;
-        src_k = win_k + sl;
-        src_v = win_v + sl;
+    }
+    if (any_q) {
+      // cp.async: every copy in flight at once, no register round trip
+      const float* rk = p.R_K + (size_t)h * kHeadDim * kHeadDim;
+      const float* rv = p.R_V + (size_t)h * kHeadDim * kHeadDim;
+      constexpr int n4 = kHeadDim * kHeadDim / 4;
+      for (int i = tid; i < n4; i += kThreads) {
+        cp_async16(Rs + 4 * i, rk + 4 * i);
+        if (!p.fold_rv) cp_async16(Rs + kHeadDim * kHeadDim + 4 * i, rv + 4 * i);
       }
-      ring_slot_new = S + q % W;
+      asm volatile("cp.async.commit_group;\n" ::);
+      asm volatile("cp.async.wait_group 0;\n" ::);
     }
 
-    if (qpos >= 0 && tid < 2 * kHeadDim) {
-      const int kind = tid >> 7, c = tid & 127;
-      const __nv_bfloat16* src = kind ? src_v : src_k;
-      xs[kind][c] = __bfloat162float(src[c]);
-    }
-    __syncthreads();  // ring entry read before it is overwritten below
+    for (int j = j0; j < j1; ++j) {
+      const int64_t q = (int64_t)L + j;
+      const size_t in_off = (((size_t)b * p.n_new + j) * Hkv + h) * kHeadDim;
+      // what this token quantises: -1 none, else the position, and where it comes from
+      int64_t qpos = -1;
+      const __nv_bfloat16* src_k = nullptr;
+      const __nv_bfloat16* src_v = nullptr;
+      int64_t ring_slot_new = -1;
+      if (q < S) {
+        // sink token: BF16 copy
+        if (tid < kHeadDim) {
+          win_k[(size_t)q * kHeadDim + tid] = p.k[in_off + tid];
+          win_v[(size_t)q * kHeadDim + tid] = p.v[in_off + tid];
+        }
+      } else if (q < E2) {
+        qpos = q;
+        src_k = p.k + in_off;
+        src_v = p.v + in_off;
+      } else {
+        // ring occupant; the entry at its slot may have to be quantised first
+        const int64_t pe = q - (int64_t)W * ((q - L) / W + 1);
+        if (pe >= E && pe < E2 && pe >= S) {
+          qpos = pe;
+          const size_t sl = (size_t)(S + pe % W) * kHeadDim;
+          src_k = win_k + sl;
+          src_v = win_v + sl;
+        }
+        ring_slot_new = S + q % W;
+      }
 
-    if (ring_slot_new >= 0 && tid < 2 * kHeadDim) {
-      const int kind = tid >> 7, c = tid & 127;
-      __nv_bfloat16* dst = (kind ? win_v : win_k) + (size_t)ring_slot_new * kHeadDim;
-      dst[c] = (kind ? p.v : p.k)[in_off + c];
-    }
+      if (qpos >= 0) {
+        if (tid == 2 * kHeadDim) {
+          // page-table entry of the quantised position, fetched while the token loads
+          const int64_t pidx = qpos / kPage;
+          s_page = pidx < p.pt_stride ? p.page_table[(int64_t)b * p.pt_stride + pidx] : -1;
+        }
+        if (tid < 2 * kHeadDim) {
+          const int kind = tid >> 7, c = tid & 127;
+          xs[kind][c] = __bfloat162float((kind ? src_v : src_k)[c]);
+        }
+      }
+      __syncthreads();  // ring entry read (and rotations staged) before the ring write
 
-    if (qpos >= 0) {
-      // rotation x @ R: thread (kind, half, c) sums 64 terms, two halves added in order
-      {
-        const int kind = tid >> 8, half = (tid >> 7) & 1, c = tid & 127;
-        const float* R = (kind ? p.R_V : p.R_K) + (size_t)h * kHeadDim * kHeadDim;
-        const int i0 = half * 64;
-        float acc = 0.f;
-        if (kind == 1 && p.fold_rv) {
-          acc = half ? 0.f : xs[1][c];  // identity: V is already in the R_V basis
-        } else {
+      if (ring_slot_new >= 0 && tid < 2 * kHeadDim) {
+        const int kind = tid >> 7, c = tid & 127;
+        __nv_bfloat16* dst = (kind ? win_v : win_k) + (size_t)ring_slot_new * kHeadDim;
+        dst[c] = (kind ? p.v : p.k)[in_off + c];
+      }
+
+      if (qpos >= 0) {
+        // rotation x @ R: thread (kind, half, c) sums 64 terms, the halves added in order
+        {
+          const int kind = tid >> 8, half = (tid >> 7) & 1, c = tid & 127;
+          const float* R = Rs + kind * kHeadDim * kHeadDim + c;
+          const int i0 = half * 64;
+          float acc = 0.f;
+          if (kind == 1 && p.fold_rv) {
+            acc = half ? 0.f : xs[1][c];  // identity: V is already in the R_V basis
+          } else {
 #pragma unroll 16
-          for (int i = 0; i < 64; ++i) acc = fmaf(xs[kind][i0 + i], __ldg(&R[(i0 + i) * kHeadDim + c]), acc);
-        }
-        red[kind][half][c] = acc;
-      }
-      __syncthreads();
-      if ((tid & 255) < kHeadDim) {
-        const int kind = tid >> 8, c = tid & 127;
-        const float x_rot = red[kind][0][c] + red[kind][1][c];
-        if (p.trace && qpos < p.trace_positions) {
-          p.trace[((((size_t)b * p.trace_positions + qpos) * Hkv + h) * 2 + kind) * kHeadDim + c] = x_rot;
-        }
-        const float clip = (kind ? p.clip_V : p.clip_K)[h];
-        const float x = fminf(fmaxf(x_rot, -clip), clip);
-        // one warp = one group of 32 channels
-        const float mn = warp_min(x), mx = warp_max(x);
-        const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-        const __half z16 = __float2half_rn(mn);
-        const float sf = __half2float(s16), zf = __half2float(z16);
-        int code = 0;
-        if (sf != 0.f) {
-          float u = rintf(__fdiv_rn(__fsub_rn(x, zf), sf));
-          u = fminf(fmaxf(u, 0.f), 3.f);
-          code = (int)u;
-        }
-        codes[kind][c] = (uint8_t)code;
-        if ((c & 31) == 0) {
-          meta[kind][c >> 5][0] = s16;
-          meta[kind][c >> 5][1] = z16;
-        }
-      }
-      __syncthreads();
-      uint8_t* blk = tid < 72 ? block_of(p, b, qpos, h) : nullptr;
-      if (blk) {
-        const int t = (int)(qpos % kPage);
-        if (tid < 8) {
-          // K: 8 words of this token
-          const int bb = tid >> 1, x = tid & 1;
-          uint32_t w = 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int ch = 16 * i + 2 * bb + 8 * x;
-            w |= (uint32_t)codes[0][ch] << (2 * i);
-            w |= (uint32_t)codes[0][ch + 1] << (16 + 2 * i);
+            for (int i = 0; i < 64; ++i) acc = fmaf(xs[kind][i0 + i], R[(i0 + i) * kHeadDim], acc);
           }
-          const int a = t & 7, th = t >> 3;
-          *reinterpret_cast<uint32_t*>(blk + 16 * (4 * a + bb) + 4 * (2 * th + x)) = w;
-        } else if (tid >= 32 && tid < 48) {
-          // V: 16 half-words of this token
-          const int u = tid - 32, a = u >> 1, x = u & 1;
-          uint32_t hw = 0;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) hw |= (uint32_t)codes[1][16 * i + a + 8 * x] << (2 * i);
-          const int tt = t >> 3, bb = (t & 7) >> 1, hi = t & 1;
-          *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a + bb) + 4 * (2 * tt + x) + 2 * hi) =
-              (uint16_t)hw;
-        } else if (tid >= 64 && tid < 72) {
-          // scale / zero of each group, K and V
-          const int u = tid - 64, kind = u >> 2, gq = u & 3;
-          const int jj = 4 * kind + gq, bb = (t & 7) >> 1;
-          uint8_t* m = blk + 1024 + 16 * (4 * jj + bb) + 4 * (2 * (t >> 3)) + 2 * (t & 1);
-          *reinterpret_cast<__half*>(m) = meta[kind][gq][0];
-          *reinterpret_cast<__half*>(m + 4) = meta[kind][gq][1];
+          red[kind][half][c] = acc;
         }
+        __syncthreads();
+        if ((tid & 255) < kHeadDim) {
+          const int kind = tid >> 8, c = tid & 127;
+          const float x_rot = red[kind][0][c] + red[kind][1][c];
+          if (p.trace && qpos < p.trace_positions) {
+            p.trace[((((size_t)b * p.trace_positions + qpos) * Hkv + h) * 2 + kind) * kHeadDim + c] = x_rot;
+          }
+          const float clip = (kind ? p.clip_V : p.clip_K)[h];
+          const float x = fminf(fmaxf(x_rot, -clip), clip);
+          // one warp = one group of 32 channels
+          const float mn = warp_min(x), mx = warp_max(x);
+          const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+          const __half z16 = __float2half_rn(mn);
+          const float sf = __half2float(s16), zf = __half2float(z16);
+          int code = 0;
+          if (sf != 0.f) {
+            float u = rintf(__fdiv_rn(__fsub_rn(x, zf), sf));
+            u = fminf(fmaxf(u, 0.f), 3.f);
+            code = (int)u;
+          }
+          codes[kind][c] = (uint8_t)code;
+          if ((c & 31) == 0) {
+            meta[kind][c >> 5][0] = s16;
+            meta[kind][c >> 5][1] = z16;
+          }
+        }
+        __syncthreads();
+        uint8_t* blk = tid < 72 ? block_of(p, s_page, h) : nullptr;
+        if (blk) {
+          const int t = (int)(qpos % kPage);
+          if (tid < 8) {
+            // K: 8 words of this token
+            const int bb = tid >> 1, x = tid & 1;
+            uint32_t w = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int ch = 16 * i + 2 * bb + 8 * x;
+              w |= (uint32_t)codes[0][ch] << (2 * i);
+              w |= (uint32_t)codes[0][ch + 1] << (16 + 2 * i);
+            }
+            const int a = t & 7, th = t >> 3;
+            *reinterpret_cast<uint32_t*>(blk + 16 * (4 * a + bb) + 4 * (2 * th + x)) = w;
+          } else if (tid >= 32 && tid < 48) {
+            // V: 16 half-words of this token
+            const int u = tid - 32, a = u >> 1, x = u & 1;
+            uint32_t hw = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hw |= (uint32_t)codes[1][16 * i + a + 8 * x] << (2 * i);
+            const int tt = t >> 3, bb = (t & 7) >> 1, hi = t & 1;
+            *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a + bb) + 4 * (2 * tt + x) + 2 * hi) =
+                (uint16_t)hw;
+          } else if (tid >= 64 && tid < 72) {
+            // scale / zero of each group, K and V
+            const int u = tid - 64, kind = u >> 2, gq = u & 3;
+            const int bb = (t & 7) >> 1, pair = t >> 3, half = t & 1;
+            if (kind == 0) {
+              *reinterpret_cast<__half*>(blk + 1024 + 32 * bb + 8 * gq + 4 * pair + 2 * half) = meta[0][gq][0];
+              *reinterpret_cast<__half*>(blk + 1152 + 4 * (2 * t + (gq >> 1)) + 2 * (gq & 1)) = meta[0][gq][1];
+            } else {
+              uint8_t* m = blk + 1280 + 16 * (4 * gq + bb) + 4 * (2 * pair) + 2 * half;
+              *reinterpret_cast<__half*>(m) = meta[1][gq][0];
+              *reinterpret_cast<__half*>(m + 4) = meta[1][gq][1];
+            }
+          }
+        }
+        __syncthreads();  // codes / meta / xs reused by the next token
       }
     }
   }
@@ -203,25 +243,32 @@ oscar_quant_append_kernel(AppendParams p) {
   if (s_last && tid == 0) {
     __threadfence();
     for (int bb = 0; bb < p.batch; ++bb) {
-      oscar_seq_state st = p.state[bb];
-      if (!state_ok(st.seq_len, st.int2_end, S, W)) continue;
-      int64_t nl = (int64_t)st.seq_len + p.n_new;
+      oscar_seq_state sb = p.state[bb];
+      if (!state_ok(sb, S, W, p.max_batch)) continue;
+      const int64_t nl = (int64_t)sb.seq_len + p.n_new;
       int64_t ne = nl - W;
-      if (ne < st.int2_end) ne = st.int2_end;
+      if (ne < sb.int2_end) ne = sb.int2_end;
       if (ne < S) ne = S;
-      st.seq_len = (int32_t)nl;
-      st.int2_end = (int32_t)ne;
-      p.state[bb] = st;
+      sb.seq_len = (int32_t)nl;
+      sb.int2_end = (int32_t)ne;
+      p.state[bb] = sb;
     }
     *p.counter = 0u;
     __threadfence();
   }
 }
 
-
 cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s) {
-  dim3 grid((unsigned)p.n_new, (unsigned)p.num_kv_heads, (unsigned)p.batch);
-  oscar_quant_append_kernel<<<grid, kThreads, 0, s>>>(p);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(oscar_quant_append_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid((unsigned)((p.n_new + kTokensPerCta - 1) / kTokensPerCta), (unsigned)p.num_kv_heads,
+            (unsigned)p.batch);
+  oscar_quant_append_kernel<<<grid, kThreads, kAppendSmem, s>>>(p);
   return cudaGetLastError();
 }
 

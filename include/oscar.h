@@ -44,15 +44,16 @@
  *     V code of slot t, channel c (bytes [512, 1024)):
  *       i = c/16, r = c%16, x = r/8, a = r%8, tt = t/8, b = (t%8)/2, hi = t%2;
  *       word at byte 512 + 16*(4a+b) + 4*(2*tt+x), bit 16*hi+2*i.
- *     fp16 scale (field 0) / zero (field 1) of group gq (channels 32gq..32gq+31)
- *       of slot t, kind 0 = K, 1 = V (bytes [1024, 1536)):
- *       j = 4*kind + gq, b = (t%8)/2; half at byte
- *       1024 + 16*(4j+b) + 4*(2*(t/8)+field) + 2*(t%2).
+ *     fp16 scale and zero of group gq (channels 32gq..32gq+31) of slot t, with
+ *       b = (t%8)/2, pair = t/8, half = t%2 (bytes [1024, 1536)):
+ *       K scale at byte 1024 + 32*b + 8*gq + 4*pair + 2*half;
+ *       K zero  at byte 1152 + 4*(2*t + gq/2) + 2*(gq%2);
+ *       V scale at byte 1280 + 16*(4*gq + b) + 4*(2*pair) + 2*half, V zero 4 bytes later.
  *   Slots of positions outside [sink, int2_end) are never read.
  *
- *   Window: bf16 [max_batch][num_kv_heads][2 (K, V)][sink + recent][128].
- *   Slot s < sink holds position s; slot sink + (pos % recent) holds a recent
- *   position pos.
+ *   Window: bf16 [max_batch][num_kv_heads][2 (K, V)][sink + recent][128],
+ *   row r = window_row of a request. Slot s < sink holds position s; slot
+ *   sink + (pos % recent) holds a recent position pos.
  *
  *   Page table: int32 [batch][max_pages_per_seq]; entry n maps positions
  *   [16n, 16n+16) of the request to a page id. Several requests may map the
@@ -60,9 +61,12 @@
  *
  *   Sequence state: oscar_seq_state [batch] in device memory. seq_len = cached
  *   tokens L; int2_end = E, the first position still held in BF16 after the
- *   sink. A new request is {0, sink}. Invariants: sink <= E, E <= max(L, sink),
- *   L - E <= recent. Positions [0, min(sink, L)) are in the sink, [sink, E) are
- *   INT2, [E, L) are in the recent ring.
+ *   sink; window_row = the request's row of the BF16 window. A new request is
+ *   {0, sink, row, 0}. Invariants: sink <= E, E <= max(L, sink), L - E <= recent,
+ *   0 <= window_row < max_batch. Positions [0, min(sink, L)) are in the sink,
+ *   [sink, E) are INT2, [E, L) are in the recent ring. Because every request
+ *   carries its own window row, a call may pass any subset of requests (for
+ *   example page_table + b * max_pages_per_seq and state + b with batch 1).
  */
 #ifndef OSCAR_H
 #define OSCAR_H
@@ -110,8 +114,10 @@ typedef struct oscar_config {
 } oscar_config;
 
 typedef struct oscar_seq_state {
-  int32_t seq_len;  /* L */
-  int32_t int2_end; /* E */
+  int32_t seq_len;    /* L */
+  int32_t int2_end;   /* E */
+  int32_t window_row; /* row of the BF16 window that holds this request, [0, max_batch) */
+  int32_t reserved;   /* 0 */
 } oscar_seq_state;
 
 typedef struct oscar_ctx oscar_ctx;

@@ -17,9 +17,11 @@ every 32-bit word is little-endian.
       tt = t // 8, b = (t % 8) // 2, hi = t % 2
       byte = 512 + 16 * (4a + b) + 4 * (2 tt + x) + (16 hi + 2 i) // 8
   bit inside that byte = (16 hi + 2 i) % 8
-  metadata, bytes [1024, 1536): for kind (0 = K, 1 = V), group gq, field
-      (0 = scale, 1 = zero): j = 4 kind + gq, b = (t % 8) // 2,
-      byte = 1024 + 16 * (4 j + b) + 4 * (2 (t // 8) + field) + 2 (t % 2), an fp16.
+  metadata, bytes [1024, 1536), one fp16 each; b = (t % 8) // 2, pair = t // 8,
+      half = t % 2, group gq:
+      K scale: 1024 + 32 b + 8 gq + 4 pair + 2 half
+      K zero:  1152 + 4 (2 t + gq // 2) + 2 (gq % 2)
+      V scale: 1280 + 16 (4 gq + b) + 4 (2 pair) + 2 half;  V zero: 4 bytes after it
 """
 
 from __future__ import annotations
@@ -54,10 +56,14 @@ def v_code_location(t: int, c: int):
 
 
 def meta_location(kind: int, t: int, gq: int, field: int) -> int:
-    """Byte offset of an fp16 scale (field 0) or zero (field 1)."""
-    j = 4 * kind + gq
-    b = (t % 8) // 2
-    return 1024 + 16 * (4 * j + b) + 4 * (2 * (t // 8) + field) + 2 * (t % 2)
+    """Byte offset of the fp16 scale (field 0) or zero (field 1) of group gq,
+    token slot t, kind 0 = K / 1 = V."""
+    b, pair, half = (t % 8) // 2, t // 8, t % 2
+    if kind == 0 and field == 0:
+        return 1024 + 32 * b + 8 * gq + 4 * pair + 2 * half
+    if kind == 0:
+        return 1152 + 4 * (2 * t + gq // 2) + 2 * (gq % 2)
+    return 1280 + 16 * (4 * gq + b) + 4 * (2 * pair + field) + 2 * half
 
 
 def _tables():

@@ -25,6 +25,48 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
 
 
+def _fp16_interval(lo, hi):
+    """fp16 values (RNE) reachable by rounding any real in [lo, hi] (as the set of the two ends)."""
+    return np.float16(lo), np.float16(hi)
+
+
+def resolve_group_ties(x64, clip, eps, g_codes, g_s16, g_z16, group=32):
+    """Validate GPU quantisation decisions against exact rotated values x64 known to
+    +-eps, and return them (codes, scales, zeros) for use by the oracle.
+
+    A GPU fp16 scale / zero is valid if it is the fp16 rounding of some value
+    within the error interval of the exact quantity; a code is valid if it is the
+    rounding of (x - z) / s for some x within +-eps (either neighbour at a tie)."""
+    n, hkv, d = x64.shape
+    xc = np.clip(x64, -clip, clip)
+    xg = xc.reshape(n, hkv, d // group, group)
+    eg = eps.reshape(n, hkv, 1)
+    mn, mx = xg.min(-1), xg.max(-1)
+    # scale: fp16((mx - mn) / 3), the float32 steps are exact to ~1e-7 relative
+    rng_lo = (mx - mn - 2 * eg) / 3 * (1 - 1e-6)
+    rng_hi = (mx - mn + 2 * eg) / 3 * (1 + 1e-6)
+    s_lo, s_hi = _fp16_interval(rng_lo, rng_hi)
+    gs = g_s16.astype(np.float64)
+    assert np.all((gs >= np.minimum(s_lo, s_hi).astype(np.float64)) &
+                  (gs <= np.maximum(s_lo, s_hi).astype(np.float64))), "scale outside its tie interval"
+    z_lo, z_hi = _fp16_interval(mn - eg * (1 + 1e-6), mn + eg * (1 + 1e-6))
+    gz = g_z16.astype(np.float64)
+    assert np.all((gz >= z_lo.astype(np.float64)) & (gz <= z_hi.astype(np.float64))), \
+        "zero outside its tie interval"
+    sf = np.repeat(gs, group, axis=-1)
+    zf = np.repeat(gz, group, axis=-1)
+    safe = np.where(sf == 0, 1.0, sf)
+    u_lo = (xc - eps - zf) / safe
+    u_hi = (xc + eps - zf) / safe
+    want_lo = np.clip(np.rint(u_lo), 0, 3)
+    want_hi = np.clip(np.rint(u_hi), 0, 3)
+    gc = g_codes.astype(np.float64)
+    ok = (gc >= np.minimum(want_lo, want_hi)) & (gc <= np.maximum(want_lo, want_hi))
+    ok = np.where(sf == 0, gc == 0, ok)
+    assert np.all(ok), "code outside its tie interval at %d elements" % int((~ok).sum())
+    return g_codes.copy(), g_s16.copy(), g_z16.copy()
+
+
 class Layer:
     """One layer: calibration (oracle), device context + cache, host copies of
     every token appended so the oracle can rebuild the same cache."""
@@ -109,8 +151,34 @@ class Layer:
         return oracle.OracleCache(r_k, self.r_v32, self.cal["clip_K32"], self.cal["clip_V32"],
                                   self.sink).build(self.k_host[b], self.v_host[b], self.len[b], self.e[b])
 
-    def oracle_decode(self, q, b):
-        return oracle.decode_attention(np.asarray(q, dtype=np.float64), self.oracle_cache(b))
+    def oracle_decode(self, q, b, resolve_ties=True):
+        cache = self.oracle_cache_resolved(b) if resolve_ties else self.oracle_cache(b)
+        return oracle.decode_attention(np.asarray(q, dtype=np.float64), cache)
+
+    def oracle_cache_resolved(self, b):
+        """The oracle's own cache of request b in which every decision that sits at
+        a rounding tie of the oracle's float64 rotation (within the 1e-5 rotation
+        bound) takes the GPU's choice, after checking that the choice is one of
+        the valid ones there. Every other code, scale and zero must already be
+        equal; a GPU decision that is neither raises AssertionError."""
+        cache = self.oracle_cache(b)
+        S, E = self.sink, min(self.e[b], self.len[b])
+        if E <= S:
+            return cache
+        dec = self.int2_codes(b, S, E)
+        for kind in range(2):
+            x = (cache.k if kind == 0 else cache.v)[S:E]
+            r = cache.r_k if kind == 0 else cache.r_v
+            clip = (cache.clip_k if kind == 0 else cache.clip_v).reshape(1, -1, 1).astype(np.float64)
+            x64 = np.einsum("nhi,hij->nhj", x, r)
+            eps = ROT_REL * np.abs(x64).max(-1, keepdims=True)                 # [n, hkv, 1]
+            codes, s16, z16 = resolve_group_ties(x64, clip, eps, dec[kind], dec[2 + 2 * kind],
+                                                 dec[3 + 2 * kind])
+            if kind == 0:
+                cache.k_codes, cache.k_scale, cache.k_zero = codes, s16, z16
+            else:
+                cache.v_codes, cache.v_scale, cache.v_zero = codes, s16, z16
+        return cache
 
     def device_state(self):
         return self.cache.state.cpu().numpy()
