@@ -74,6 +74,8 @@ _SIGS = {
     "oscar_decode_splits": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "oscar_error_flags": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]),
     "oscar_last_error": (ctypes.c_char_p, [_P]),
+    "oscar_decode_attn_noalloc": (ctypes.c_int, [ctypes.POINTER(OscarConfig), _P, _P, _P, _P, ctypes.c_int32,
+                                                 _P, ctypes.c_int64, _P, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -134,6 +136,19 @@ def _stream(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def decode_attn_noalloc(cfg, q, page_table, state, o, batch, pool, num_pages, window, r_k, r_v, clip_v,
+                        err_flags=None, stream=None):
+    """oscar_decode_attn_noalloc: decode attention without a context and without any
+    device allocation (device tensors in, device output out)."""
+    _check(lib().oscar_decode_attn_noalloc(ctypes.byref(cfg), _ptr(q), _ptr(page_table), _ptr(state),
+                                           _ptr(o), batch, _ptr(pool), num_pages, _ptr(window),
+                                           _ptr(r_k), _ptr(r_v), _ptr(clip_v), _ptr(err_flags),
+                                           _stream(stream)))
 
 
 class Context:

@@ -207,6 +207,43 @@ int oscar_error_flags(oscar_ctx* ctx, uint32_t* flags, int32_t clear);
 /* Message of the last failure on ctx ("" if none; a static text for NULL). */
 const char* oscar_last_error(const oscar_ctx* ctx);
 
+/* Size of the fixed device array behind oscar_decode_attn_noalloc. */
+#define OSCAR_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* Decode attention that allocates nothing (no counterpart on the method's pages:
+ * this is an integration aid of this library).
+ *
+ * For callers that cannot call cudaMalloc: code recorded into a CUDA graph that
+ * must not contain allocations, plug-ins whose device memory is budgeted by a
+ * host framework, or runtimes without a device allocator. The call needs no
+ * context: it computes exactly what oscar_decode_attn computes, from buffers the
+ * caller passes, with its split-K workspace in a fixed array of
+ * OSCAR_NOALLOC_SCRATCH_BYTES inside this library's device image. That array
+ * exists on every GPU that loads the library, for the life of the process.
+ *
+ * cfg: HOST configuration (as for oscar_create). q, page_table, state, o: as for
+ * oscar_decode_attn. int2_pool (num_pages pages), window: the cache buffers, laid
+ * out as for oscar_bind_cache (16-byte aligned). R_K, R_V: DEVICE float32
+ * [num_kv_heads][128][128] (16-byte aligned); clip_V: DEVICE float32
+ * [num_kv_heads]. err_flags: optional DEVICE uint32 that the kernels OR
+ * OSCAR_FLAG_* bits into (never cleared by the call); NULL sends the flags to a
+ * word of the fixed array that each call clears and no caller can read.
+ *
+ * Returns OSCAR_ERR_OUT_OF_RANGE when batch exceeds cfg->max_batch or when the
+ * workspace of this call (growing with batch, num_kv_heads, the query group and
+ * the number of splits) does not fit in OSCAR_NOALLOC_SCRATCH_BYTES; the other
+ * statuses as for oscar_decode_attn. No cudaMalloc or cudaFree is ever made.
+ *
+ * The first call on each device looks up the array's device address with that
+ * device current; make it before any stream capture. All calls on a device share
+ * the array and it keeps the last call's contents (each call rewrites what it
+ * reads); calls whose kernels can overlap on the GPU race on it. */
+int oscar_decode_attn_noalloc(const oscar_config* cfg, const void* q, const int32_t* page_table,
+                              const oscar_seq_state* state, float* o, int32_t batch,
+                              const void* int2_pool, int64_t num_pages, const void* window,
+                              const float* R_K, const float* R_V, const float* clip_V,
+                              uint32_t* err_flags, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
