@@ -129,7 +129,12 @@ def cache_bytes(cfg: OscarConfig, num_pages: int):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device pointer of a tensor; the library reads dense row-major buffers only."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("liboscar takes contiguous tensors (got strides %s)" % (tuple(t.stride()),))
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
