@@ -182,7 +182,7 @@ class Workload:
         self._populate()
         # per-step inputs (a small ring of distinct draws, resident on the device)
         self.n_inputs = 8
-        self.q = [draw_queries(seed, 100 + i, B, hq, hkv, D, device=device).to(torch.bfloat16)
+        self.q = [draw_queries(seed, 100 + i, B, hq, hkv, D, device=device).to(torch.bfloat16).contiguous()
                   for i in range(self.n_inputs)]
         kv = [draw_kv(seed, 100 + i, B, hkv, D, spec.token_spikes, device=device) for i in range(self.n_inputs)]
         self.k = [a.to(torch.bfloat16).view(B, 1, hkv, D).contiguous() for a, _ in kv]
@@ -247,6 +247,11 @@ class Workload:
         s = self.spec
         return float(self.B * s.num_kv_heads * (512 + 512 + 96 + 512))
 
+    def decode_only(self, i, stream):
+        ctx, cache = self.layers[i % len(self.layers)]
+        j = i % self.n_inputs
+        ctx.decode_attn(self.q[j], cache.page_table, cache.state, self.o, self.B, stream)
+
     def step(self, i, stream, ev=None):
         ctx, cache = self.layers[i % len(self.layers)]
         j = i % self.n_inputs
@@ -261,7 +266,7 @@ class Workload:
 
 
 def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True):
-    n_total = 2 * args.warmup + 3 * args.steps + 4096 + 64
+    n_total = 2 * args.warmup + 6 * args.steps + 4096 + 64
     wl = Workload(name, device, n_total, rank, batch_override=getattr(args, 'batch', 0))
     stream = torch.cuda.current_stream(device)
     # warm-up: at least W steps and about half a second under load
@@ -274,27 +279,48 @@ def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True
         i += 1
         if i % 256 == 0:
             torch.cuda.synchronize()
-        if i > n_total - 2 * args.steps - 2 * args.warmup - 32:
+        if i > n_total - 5 * args.steps - 2 * args.warmup - 32:
             break
     torch.cuda.synchronize()
-    warm_done = i
+    # two CUDA graphs, captured once and warmed once:
+    #   g_time - K full steps (append + decode): the timed region, the headline value;
+    #   g_dec  - K decode_attn calls over the same layers (decode leaves the cache
+    #            unchanged), timed right after it: the decode call's duration
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    g_time = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g_time, stream=cap):
+            for k in range(args.steps):
+                wl.step(i + k, cap)
+    g_dec = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g_dec, stream=cap):
+            for k in range(args.steps):
+                wl.decode_only(i + k, cap)
+    g_time.replay()
+    g_dec.replay()
+    torch.cuda.synchronize()
+    i += args.steps
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for k in range(args.steps):
-        wl.step(i + k, stream, evs[k])
-    end.record(stream)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record(stream)
+    g_time.replay()
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    ev[2].record(stream)
+    g_dec.replay()
+    ev[3].record(stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    total_ms = start.elapsed_time(end)
-    app_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    dec_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    total_ms = ev[0].elapsed_time(ev[1])
+    dec_ms = ev[2].elapsed_time(ev[3]) / args.steps
+    app_ms = max(total_ms / args.steps - dec_ms, 0.0)
+    warm_done = i
     i += args.steps
     if dist:
         t = torch.tensor([total_ms, app_ms, dec_ms], dtype=torch.float64, device=device)

@@ -121,7 +121,9 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
   __shared__ __half hs[2][kMaxGqa][kHeadDim];
   __shared__ __half gsum[2][kMaxGqa][kGroups];
   __shared__ float wmax[4];
-  stage_matrix(Rs, p.R_K + (size_t)h * kHeadDim * kHeadDim, tid, kRotThreads);
+  stage_matrix(Rs, p.R_K + (size_t)h * kHeadDim * kHeadDim, tid, kRotThreads);  // constant data
+  pdl_trigger();
+  pdl_wait();  // q may come from the previous kernel; qrec is read by the previous decode
   for (int i = tid; i < g * kHeadDim; i += kRotThreads)
     qs[i >> 7][i & 127] = __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g) * kHeadDim + i]);
   cp_wait<0>();
@@ -638,6 +640,8 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
 __global__ void __launch_bounds__(kThreads, 2) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_trigger();
+  pdl_wait();  // cache, state and q~ come from earlier kernels
   const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   if (x < p.win_slots)
     window_attention(p, b, h, x, smem);
@@ -646,89 +650,95 @@ __global__ void __launch_bounds__(kThreads, 2) oscar_decode_kernel(DecodeParams 
 }
 
 // --------------------------------------------------------------------------
-// 3. merge of the partials, un-rotation, normalisation
+// 3. merge of the partials, un-rotation, normalisation; CTA z handles query
+//    heads 2z and 2z + 1 of (request y, KV head x)
 // --------------------------------------------------------------------------
 constexpr int kMergeThreads = 256;
 constexpr int kMaxSlots = 256 + kMaxWindow / kWinChunk;   // INT2 splits + window chunks
-constexpr int kMergeSmem = kRotSmem + kMaxSlots * kMaxGqa * 2 * 4 + kMaxGqa * kHeadDim * 4;
+constexpr int kMergeChunk = 32;                            // partial rows staged per round
+constexpr int kMergeSmem = kRotSmem + kMergeChunk * 2 * kPartFloats * 4 + kMaxSlots * 4 * 4 +
+                           2 * kHeadDim * 4;
 
 __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
   float* RT = reinterpret_cast<float*>(dsm);                   // R_V^T[h], [128][128]
-  float* wts = RT + kHeadDim * kHeadDim;                        // [slots][8] weights, then l
-  float* orot = wts + kMaxSlots * kMaxGqa * 2;                  // [8][128]
-  __shared__ float lsum_s[kMaxGqa];
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  float* rows = RT + kHeadDim * kHeadDim;                       // [32 slots][2 heads][kPartFloats]
+  float* wts = rows + kMergeChunk * 2 * kPartFloats;            // [slots][2] max, then weight
+  float* lsl = wts + kMaxSlots * 2;                             // [slots][2] row sums
+  float* orot = lsl + kMaxSlots * 2;                            // [2][128]
+  __shared__ float lsum_s[2];
+  const int h = blockIdx.x, b = blockIdx.y, m0 = 2 * blockIdx.z, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int g = p.gqa, nslots = p.win_slots + p.splits, nwin = p.win_slots;
-  const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
+  const int nh = min(2, g - m0);
   if (!p.fold_rv) stage_matrix(RT, p.R_VT + (size_t)h * kHeadDim * kHeadDim, tid, kMergeThreads);
   else cp_commit();
-  // (m, l) of every slot and head
-  float* ml = wts + kMaxSlots * kMaxGqa;                        // [slots][8] l values
-  for (int i = tid; i < nslots * g; i += kMergeThreads) {
-    const int sidx = i / g, m = i % g;
-    const float* ps = part + ((size_t)sidx * g + m) * kPartFloats;
-    wts[sidx * kMaxGqa + m] = ps[kHeadDim];
-    ml[sidx * kMaxGqa + m] = ps[kHeadDim + 1];
+  pdl_trigger();
+  pdl_wait();  // the partials come from the decode kernel
+  const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
+  for (int i = tid; i < nslots * nh; i += kMergeThreads) {
+    const int sidx = i / nh, hh = i % nh;
+    const float* ps = part + ((size_t)sidx * g + m0 + hh) * kPartFloats;
+    wts[sidx * 2 + hh] = ps[kHeadDim];
+    lsl[sidx * 2 + hh] = ps[kHeadDim + 1];
   }
   __syncthreads();
-  // weights exp2(m_s - M) per head, one warp per head
-  if (warp < g) {
+  // weights exp2(m_s - M), one warp per head
+  if (warp < nh) {
     float M = -INFINITY;
-    for (int sidx = lane; sidx < nslots; sidx += 32) M = fmaxf(M, wts[sidx * kMaxGqa + warp]);
+    for (int sidx = lane; sidx < nslots; sidx += 32) M = fmaxf(M, wts[sidx * 2 + warp]);
     M = warp_maxf(M);
     float l = 0.f;
     for (int sidx = lane; sidx < nslots; sidx += 32) {
-      const float ms = wts[sidx * kMaxGqa + warp];
+      const float ms = wts[sidx * 2 + warp];
       const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wts[sidx * kMaxGqa + warp] = w;
-      l += w * ml[sidx * kMaxGqa + warp];
+      wts[sidx * 2 + warp] = w;
+      l += w * lsl[sidx * 2 + warp];
     }
     l = warp_sum(l);
     if (lane == 0) lsum_s[warp] = l;
   }
   __syncthreads();
-  // thread (channel c, heads m0, m0 + 2, ...): weighted sums of the partials
-  const int c = tid & (kHeadDim - 1), m0 = tid >> 7;
-  float ow[kMaxGqa / 2];
-#pragma unroll
-  for (int i = 0; i < kMaxGqa / 2; ++i) {
-    const int m = m0 + 2 * i;
-    ow[i] = 0.f;
-    if (m >= g) continue;
-    float owin = 0.f;
-    for (int sidx = 0; sidx < nwin; ++sidx)
-      owin = fmaf(wts[sidx * kMaxGqa + m], part[((size_t)sidx * g + m) * kPartFloats + c], owin);
-    ow[i] = owin;
-    // INT2 slots: independent loads, eight in flight per thread
-    float o8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int sidx = nwin;
-    for (; sidx + 8 <= nslots; sidx += 8) {
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        o8[u] = fmaf(wts[(sidx + u) * kMaxGqa + m], part[((size_t)(sidx + u) * g + m) * kPartFloats + c], o8[u]);
+  // thread (head hh, channel c): weighted sums of the window and INT2 partials
+  const int c = tid & (kHeadDim - 1), hh = tid >> 7;
+  float owin = 0.f, orr = 0.f;
+  constexpr int kChunks16 = kPartFloats / 4;  // 16-byte pieces per row
+  for (int s0 = 0; s0 < nslots; s0 += kMergeChunk) {
+    const int n = min(kMergeChunk, nslots - s0);
+    for (int i = tid; i < n * nh * kChunks16; i += kMergeThreads) {
+      const int r = i / kChunks16, u = i % kChunks16;
+      const int sidx = s0 + r / nh, h2 = r % nh;
+      cp_async16(rows + r * kPartFloats + 4 * u, part + ((size_t)sidx * g + m0 + h2) * kPartFloats + 4 * u);
     }
-    for (; sidx < nslots; ++sidx)
-      o8[0] = fmaf(wts[sidx * kMaxGqa + m], part[((size_t)sidx * g + m) * kPartFloats + c], o8[0]);
-    orot[m * kHeadDim + c] = ((o8[0] + o8[1]) + (o8[2] + o8[3])) + ((o8[4] + o8[5]) + (o8[6] + o8[7]));
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+    if (hh < nh) {
+      for (int r = 0; r < n; ++r) {
+        const int sidx = s0 + r;
+        const float v = wts[sidx * 2 + hh] * rows[(r * nh + hh) * kPartFloats + c];
+        if (sidx < nwin)
+          owin += v;
+        else
+          orr += v;
+      }
+    }
+    __syncthreads();
   }
+  if (hh < nh) orot[hh * kHeadDim + c] = orr;
   cp_wait<0>();
   __syncthreads();
-#pragma unroll
-  for (int i = 0; i < kMaxGqa / 2; ++i) {
-    const int m = m0 + 2 * i;
-    if (m >= g) continue;
+  if (hh < nh) {
     float oi;
     if (p.fold_rv) {
-      oi = orot[m * kHeadDim + c];
+      oi = orr;
     } else {
       oi = 0.f;
 #pragma unroll 8
-      for (int j = 0; j < kHeadDim; ++j) oi = fmaf(orot[m * kHeadDim + j], RT[j * kHeadDim + c], oi);
+      for (int j = 0; j < kHeadDim; ++j) oi = fmaf(orot[hh * kHeadDim + j], RT[j * kHeadDim + c], oi);
     }
-    const float l = lsum_s[m];
-    p.o[((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + c] = l > 0.f ? (oi + ow[i]) / l : 0.f;
+    const float l = lsum_s[hh];
+    p.o[((size_t)b * p.num_q_heads + h * g + m0 + hh) * kHeadDim + c] = l > 0.f ? (oi + owin) / l : 0.f;
   }
 }
 
@@ -754,9 +764,15 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s) {
     attr_set = true;
   }
   if (p.win_slots + p.splits > kMaxSlots) return cudaErrorInvalidValue;
-  oscar_rotate_q_kernel<<<dim3(p.num_kv_heads, batch), kRotThreads, kRotSmem, s>>>(p);
-  oscar_decode_kernel<<<dim3(p.win_slots + p.splits, p.num_kv_heads, batch), kThreads, smem, s>>>(p);
-  oscar_merge_kernel<<<dim3(p.num_kv_heads, batch), kMergeThreads, kMergeSmem, s>>>(p);
+  cudaError_t e = launch_pdl(oscar_rotate_q_kernel, dim3(p.num_kv_heads, batch), dim3(kRotThreads), kRotSmem,
+                             s, p);
+  if (e == cudaSuccess)
+    e = launch_pdl(oscar_decode_kernel, dim3(p.win_slots + p.splits, p.num_kv_heads, batch), dim3(kThreads),
+                   smem, s, p);
+  if (e == cudaSuccess)
+    e = launch_pdl(oscar_merge_kernel, dim3(p.num_kv_heads, batch, (p.gqa + 1) / 2), dim3(kMergeThreads),
+                   kMergeSmem, s, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -88,12 +88,16 @@ int check_config_msg(const oscar_config* c, std::string* msg) {
   return OSCAR_OK;
 }
 
+int win_slots(const oscar_config* c) { return (c->sink + c->recent + kWindowChunk - 1) / kWindowChunk; }
+
 int auto_splits(const oscar_ctx* ctx, int batch) {
   if (ctx->cfg.num_splits > 0) return ctx->cfg.num_splits;
   const int64_t units = (int64_t)batch * ctx->cfg.num_kv_heads;
   const int64_t pages = ctx->cfg.max_pages_per_seq;
-  // at least one wave of two CTAs per SM; at most 256 pages (32 per warp) per CTA
-  int64_t by_wave = (2 * (int64_t)ctx->num_sms + units - 1) / units;
+  // fill one wave of two CTAs per SM together with the BF16-window CTAs; at most
+  // 256 pages (32 per warp) per CTA
+  const int64_t wins = units * win_slots(&ctx->cfg);
+  int64_t by_wave = (2 * (int64_t)ctx->num_sms - wins) / units;
   int64_t by_pages = (pages + 255) / 256;
   int64_t s = by_wave > by_pages ? by_wave : by_pages;
   const int64_t cap = (pages + 7) / 8;  // keep >= 8 pages per split
@@ -102,8 +106,6 @@ int auto_splits(const oscar_ctx* ctx, int batch) {
   if (s < 1) s = 1;
   return (int)s;
 }
-
-int win_slots(const oscar_config* c) { return (c->sink + c->recent + kWindowChunk - 1) / kWindowChunk; }
 
 template <class T>
 cudaError_t dalloc(T** p, size_t bytes) {

@@ -27,7 +27,7 @@ constexpr int kMaxGqa = 8;
 // [0, 1024) fp16x2 mma A fragments of q~ (hi/lo), [1024, 1088) A fragments of the
 // per-group sums of q~ (hi/lo), [1088] the score scale, rest zero
 constexpr int kQrecWords = 1104;
-constexpr int kPartFloats = kHeadDim + 2;    // o[128], m, l
+constexpr int kPartFloats = kHeadDim + 4;    // o[128], m, l, 2 pad (rows stay 16-byte aligned)
 constexpr int kWindowChunk = 64;             // BF16 window tokens per decode CTA
 
 struct AppendParams {
@@ -70,6 +70,29 @@ struct DecodeParams {
   float scale_log2;         // softmax_scale * log2(e)
   uint32_t* err_flags;
 };
+
+// Programmatic dependent launch: kernels launched with launch_pdl may start
+// while the previous kernel on the stream is still running. Each of them stages
+// constant data first, lets its own dependents start (pdl_trigger) and calls
+// pdl_wait before it touches anything an earlier kernel writes or reads.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // launchers (return cudaGetLastError())
 cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s);

@@ -61,12 +61,26 @@ oscar_quant_append_kernel(AppendParams p) {
   __shared__ uint8_t codes[2][kHeadDim];
   __shared__ __half meta[2][kGroups][2];
 
+  // the rotations are constant: stage them before waiting for earlier kernels
+  {
+    const float* rk = p.R_K + (size_t)h * kHeadDim * kHeadDim;
+    const float* rv = p.R_V + (size_t)h * kHeadDim * kHeadDim;
+    constexpr int n4 = kHeadDim * kHeadDim / 4;
+    for (int i = tid; i < n4; i += kThreads) {
+      cp_async16(Rs + 4 * i, rk + 4 * i);
+      if (!p.fold_rv) cp_async16(Rs + kHeadDim * kHeadDim + 4 * i, rv + 4 * i);
+    }
+    asm volatile("cp.async.commit_group;\n" ::);
+  }
+  pdl_trigger();
+  pdl_wait();
   if (tid == 0) {
     s_st = p.state[b];
     __threadfence();
     const unsigned total = gridDim.x * gridDim.y * gridDim.z;
     s_last = (atomicAdd(p.counter, 1u) == total - 1u);
   }
+  asm volatile("cp.async.wait_group 0;\n" ::);  // rotations staged, visible after the barrier
   __syncthreads();
   const oscar_seq_state st = s_st;
   const int L = st.seq_len, E = st.int2_end;
@@ -82,28 +96,6 @@ oscar_quant_append_kernel(AppendParams p) {
     __nv_bfloat16* win_k = p.window + ((wrow * Hkv + h) * 2 + 0) * slots * kHeadDim;
     __nv_bfloat16* win_v = p.window + ((wrow * Hkv + h) * 2 + 1) * slots * kHeadDim;
 
-    // stage the rotations once for all tokens of this CTA if any is quantised
-    bool any_q = false;
-    for (int j = j0; j < j1; ++j) {
-      const int64_t q = (int64_t)L + j;
-      if (q >= S && q < E2) any_q = true;
-      if (q >= E2) {
-        const int64_t pe = q - (int64_t)W * ((q - L) / W + 1);
-        if (pe >= E && pe < E2 && pe >= S) any_q = true;
-      }
-    }
-    if (any_q) {
-      // cp.async: every copy in flight at once, no register round trip
-      const float* rk = p.R_K + (size_t)h * kHeadDim * kHeadDim;
-      const float* rv = p.R_V + (size_t)h * kHeadDim * kHeadDim;
-      constexpr int n4 = kHeadDim * kHeadDim / 4;
-      for (int i = tid; i < n4; i += kThreads) {
-        cp_async16(Rs + 4 * i, rk + 4 * i);
-        if (!p.fold_rv) cp_async16(Rs + kHeadDim * kHeadDim + 4 * i, rv + 4 * i);
-      }
-      asm volatile("cp.async.commit_group;\n" ::);
-      asm volatile("cp.async.wait_group 0;\n" ::);
-    }
 
     for (int j = j0; j < j1; ++j) {
       const int64_t q = (int64_t)L + j;
@@ -268,7 +260,8 @@ cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s) {
   }
   dim3 grid((unsigned)((p.n_new + kTokensPerCta - 1) / kTokensPerCta), (unsigned)p.num_kv_heads,
             (unsigned)p.batch);
-  oscar_quant_append_kernel<<<grid, kThreads, kAppendSmem, s>>>(p);
+  cudaError_t e = launch_pdl(oscar_quant_append_kernel, grid, dim3(kThreads), kAppendSmem, s, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

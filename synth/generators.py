@@ -148,7 +148,7 @@ def draw_kv(seed: int, stream: int, n_tokens: int, num_kv_heads: int, head_dim: 
         if token_spikes:
             u = torch.rand(n_tokens, generator=g, device=device)
             x = torch.where((u < spike_prob)[:, None, None], x * spike_mult, x)
-        res.append(x.to(torch.bfloat16).to(torch.float32))
+        res.append(x.to(torch.bfloat16).to(torch.float32).contiguous())
     return res[0], res[1]
 
 
@@ -162,7 +162,7 @@ def draw_queries(seed: int, stream: int, n_tokens: int, num_q_heads: int, num_kv
     grp = num_q_heads // num_kv_heads
     bmat = basis.to(device)[torch.arange(num_q_heads, device=device) // grp]  # [Hq, d, d]
     q = torch.einsum("nhi,hji->nhj", z * sd.to(device), bmat)
-    return q.to(torch.bfloat16).to(torch.float32)
+    return q.to(torch.bfloat16).to(torch.float32).contiguous()
 
 
 # --------------------------------------------------------------------------
