@@ -24,6 +24,7 @@ STATUS = {
 }
 FLAG_BAD_PAGE_ID = 1
 FLAG_BAD_STATE = 2
+FLAG_TIMEOUT = 4
 PAGE_BLOCK_BYTES = 1536
 
 

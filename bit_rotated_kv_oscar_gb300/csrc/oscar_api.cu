@@ -27,6 +27,7 @@ struct oscar_ctx {
   float* clip_K = nullptr;
   float* clip_V = nullptr;
   float* pv_scale = nullptr;
+  uint8_t* images = nullptr;    // per KV head: R_K hi/lo, R_V hi/lo as swizzled bf16 tensor-core operands
   uint32_t* qrec = nullptr;
   float* part = nullptr;
   uint32_t* flags = nullptr;    // [0] error flags, [1] append ticket counter
@@ -107,6 +108,37 @@ int auto_splits(const oscar_ctx* ctx, int batch) {
   return (int)s;
 }
 
+// bf16 bits of a finite float, round to nearest even
+uint16_t bf16_bits(float x) {
+  uint32_t u;
+  memcpy(&u, &x, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+float bf16_value(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float x;
+  memcpy(&x, &u, 4);
+  return x;
+}
+
+// Tensor-core operand images of one 128 x 128 rotation R: B[n][k] = R[k][n]
+// (K-major, output channel n per row), split R = hi + lo in bf16, laid out in
+// 128-byte-swizzle atoms of 64 columns: element (n, k) at atom k / 64, row n,
+// 16-byte chunk ((k % 64) / 8) ^ (n % 8), position k % 8.
+void rotation_images(const float* R, bool identity, uint16_t* hi, uint16_t* lo) {
+  for (int k = 0; k < kHeadDim; ++k)
+    for (int n = 0; n < kHeadDim; ++n) {
+      const float r = identity ? (k == n ? 1.f : 0.f) : R[k * kHeadDim + n];
+      const uint16_t bh = bf16_bits(r);
+      const uint16_t bl = bf16_bits(r - bf16_value(bh));
+      const int atom = k >> 6, cc = (k & 63) >> 3;
+      const size_t off = (size_t)atom * 8192 + (size_t)n * 64 + (size_t)((cc ^ (n & 7)) * 8) + (k & 7);
+      hi[off] = bh;
+      lo[off] = bl;
+    }
+}
+
 template <class T>
 cudaError_t dalloc(T** p, size_t bytes) {
   return cudaMalloc(reinterpret_cast<void**>(p), bytes);
@@ -156,6 +188,7 @@ void oscar_destroy(oscar_ctx* ctx) {
   cudaFree(ctx->clip_K);
   cudaFree(ctx->clip_V);
   cudaFree(ctx->pv_scale);
+  cudaFree(ctx->images);
   cudaFree(ctx->qrec);
   cudaFree(ctx->part);
   cudaFree(ctx->flags);
@@ -182,6 +215,7 @@ int oscar_create(const oscar_config* cfg, oscar_ctx** out) {
   if (e == cudaSuccess) e = dalloc(&ctx->clip_K, hkv * sizeof(float));
   if (e == cudaSuccess) e = dalloc(&ctx->clip_V, hkv * sizeof(float));
   if (e == cudaSuccess) e = dalloc(&ctx->pv_scale, hkv * sizeof(float));
+  if (e == cudaSuccess) e = dalloc(&ctx->images, (size_t)hkv * prefill_image_bytes());
   if (e == cudaSuccess) {
     ctx->max_splits = auto_splits(ctx, cfg->max_batch);
     for (int b = 1; b < cfg->max_batch; ++b) {
@@ -243,7 +277,16 @@ int oscar_load_rotations(oscar_ctx* ctx, const float* R_K, const float* R_V, con
     if (ex < -30) ex = -30;
     ps[h] = ldexpf(1.f, ex);
   }
-  cudaError_t e = cudaMemcpy(ctx->R_K, R_K, n * sizeof(float), cudaMemcpyHostToDevice);
+  // prefill operands: 4 images of 128 x 128 bf16 per head
+  std::vector<uint16_t> img((size_t)hkv * 4 * kHeadDim * kHeadDim);
+  for (int h = 0; h < hkv; ++h) {
+    uint16_t* base = img.data() + (size_t)h * 4 * kHeadDim * kHeadDim;
+    const size_t m = (size_t)kHeadDim * kHeadDim;
+    rotation_images(R_K + (size_t)h * m, false, base, base + m);
+    rotation_images(R_V + (size_t)h * m, ctx->cfg.fold_rv != 0, base + 2 * m, base + 3 * m);
+  }
+  cudaError_t e = cudaMemcpy(ctx->images, img.data(), img.size() * sizeof(uint16_t), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(ctx->R_K, R_K, n * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(ctx->R_V, R_V, n * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(ctx->R_VT, rvt.data(), n * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemcpy(ctx->clip_K, clip_K, hkv * sizeof(float), cudaMemcpyHostToDevice);
@@ -294,7 +337,39 @@ static int append_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_stat
   p.trace_positions = trace ? trace_positions : 0;
   p.err_flags = ctx->flags;
   p.counter = ctx->flags + 1;
-  cudaError_t e = launch_quant_append(p, static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // long appends: the tokens that go straight to INT2 run on the tensor cores,
+  // the sink / ring / eviction tokens on the per-token kernel right after
+  if (n_new >= ctx->cfg.sink + ctx->cfg.recent + 128) {
+    PrefillParams pp{};
+    pp.page_table = page_table;
+    pp.pt_stride = ctx->cfg.max_pages_per_seq;
+    pp.state = state;
+    pp.k = p.k;
+    pp.v = p.v;
+    pp.pool = ctx->pool;
+    pp.num_pages = ctx->num_pages;
+    pp.images = ctx->images;
+    pp.clip_K = ctx->clip_K;
+    pp.clip_V = ctx->clip_V;
+    pp.num_kv_heads = ctx->cfg.num_kv_heads;
+    pp.sink = ctx->cfg.sink;
+    pp.recent = ctx->cfg.recent;
+    pp.n_new = n_new;
+    pp.batch = batch;
+    pp.max_batch = ctx->cfg.max_batch;
+    pp.trace = p.trace;
+    pp.trace_positions = p.trace_positions;
+    pp.err_flags = ctx->flags;
+    const int tiles = (n_new + 127) / 128 + 1;
+    int cph = ctx->num_sms / (ctx->cfg.num_kv_heads * batch);
+    if (cph < 1) cph = 1;
+    if (cph > tiles) cph = tiles;
+    cudaError_t e = launch_prefill_append(pp, cph, st);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "quant_append (tensor-core part) launch");
+    p.tail_only = 1;
+  }
+  cudaError_t e = launch_quant_append(p, st);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "quant_append launch");
   return OSCAR_OK;
 }

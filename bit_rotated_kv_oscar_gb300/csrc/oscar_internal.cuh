@@ -49,6 +49,28 @@ struct AppendParams {
   int32_t trace_positions;
   uint32_t* err_flags;
   uint32_t* counter;        // zero between launches
+  // prefill split: when set, this launch handles only the first `sink` and the
+  // last `recent` new tokens (virtual index v < sink -> token v, else token
+  // n_new - recent + (v - sink)) and skips tokens that go straight to INT2
+  int32_t tail_only;
+};
+
+// tokens that go straight from the input to INT2 during a long append
+struct PrefillParams {
+  const int32_t* page_table;
+  int32_t pt_stride;
+  const oscar_seq_state* state;
+  const __nv_bfloat16* k;   // [B][n_new][Hkv][128]
+  const __nv_bfloat16* v;
+  uint8_t* pool;
+  int64_t num_pages;
+  const uint8_t* images;    // [Hkv][4][32 KiB]: R_K hi, R_K lo, R_V hi, R_V lo (bf16, swizzled)
+  const float* clip_K;
+  const float* clip_V;
+  int32_t num_kv_heads, sink, recent, n_new, batch, max_batch;
+  float* trace;
+  int32_t trace_positions;
+  uint32_t* err_flags;
 };
 
 struct DecodeParams {
@@ -96,6 +118,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // launchers (return cudaGetLastError())
 cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_prefill_append(const PrefillParams& p, int ctas_per_head, cudaStream_t s);
+int prefill_image_bytes();
 cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s);
 int decode_smem_bytes();
 

@@ -49,8 +49,11 @@ oscar_quant_append_kernel(AppendParams p) {
   float* Rs = reinterpret_cast<float*>(dsm);  // [2][128][128]: R_K[h], R_V[h]
   const int tid = threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
+  // token indices of this CTA: all new tokens, or with tail_only only the first
+  // `sink` and the last `recent` of them (virtual indices, see AppendParams)
+  const int nvirt = p.tail_only ? p.sink + p.recent : p.n_new;
   const int j0 = blockIdx.x * kTokensPerCta;
-  const int j1 = min(j0 + kTokensPerCta, p.n_new);
+  const int j1 = min(j0 + kTokensPerCta, nvirt);
   const int S = p.sink, W = p.recent;
   const int Hkv = p.num_kv_heads;
 
@@ -97,8 +100,11 @@ oscar_quant_append_kernel(AppendParams p) {
     __nv_bfloat16* win_v = p.window + ((wrow * Hkv + h) * 2 + 1) * slots * kHeadDim;
 
 
-    for (int j = j0; j < j1; ++j) {
+    for (int jv = j0; jv < j1; ++jv) {
+      const int j = !p.tail_only ? jv : (jv < S ? jv : p.n_new - W + (jv - S));
       const int64_t q = (int64_t)L + j;
+      // with tail_only the tokens going straight to INT2 belong to the prefill kernel
+      if (p.tail_only && q >= S && q < E2) continue;
       const size_t in_off = (((size_t)b * p.n_new + j) * Hkv + h) * kHeadDim;
       // what this token quantises: -1 none, else the position, and where it comes from
       int64_t qpos = -1;
@@ -258,7 +264,8 @@ cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid((unsigned)((p.n_new + kTokensPerCta - 1) / kTokensPerCta), (unsigned)p.num_kv_heads,
+  const int nvirt = p.tail_only ? p.sink + p.recent : p.n_new;
+  dim3 grid((unsigned)((nvirt + kTokensPerCta - 1) / kTokensPerCta), (unsigned)p.num_kv_heads,
             (unsigned)p.batch);
   cudaError_t e = launch_pdl(oscar_quant_append_kernel, grid, dim3(kThreads), kAppendSmem, s, p);
   if (e != cudaSuccess) return e;

@@ -94,6 +94,7 @@ typedef enum oscar_status {
 /* Device-side error flags (bit set = condition seen since the last clear). */
 #define OSCAR_FLAG_BAD_PAGE_ID 1u   /* a page-table entry outside [0, num_pages); access skipped */
 #define OSCAR_FLAG_BAD_STATE 2u     /* a sequence state breaking the invariants; request skipped */
+#define OSCAR_FLAG_TIMEOUT 4u       /* a bounded wait inside a kernel expired; its remaining work skipped */
 
 typedef struct oscar_config {
   int32_t num_q_heads;
