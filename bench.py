@@ -385,6 +385,101 @@ def run_e2e(wl, args, device, i0, dist):
             "d2h_bytes_per_step": d2h}
 
 
+def run_prefill(args, device, rank, dist):
+    """131072-token prefill quant-append into a fresh request, then 16 requests
+    sharing its first 65536 tokens through aliased pages, each with a private
+    4096-token suffix, decoded for one step."""
+    from bit_rotated_kv_oscar_gb300 import abi
+    from bit_rotated_kv_oscar_gb300.cache import PagedCache
+    from bit_rotated_kv_oscar_gb300.calibrate import calibrate
+
+    spec = WORKLOADS["prefill_128k_prefix16"]
+    hq, hkv, S, W = spec.num_q_heads, spec.num_kv_heads, spec.sink, spec.recent
+    n, fork, suf, nreq = spec.context, spec.prefix_shared, spec.suffix, spec.batch
+    seed = spec.seed + 1000 * rank
+    q_cal = draw_queries(seed, 900, spec.calib_tokens, hq, hkv, D).numpy()
+    k_cal, v_cal = (t.numpy() for t in draw_kv(seed, 900, spec.calib_tokens, hkv, D))
+    cal = calibrate(q_cal, k_cal, v_cal)
+    max_pages = (n + 15) // 16 + 8
+    cfg = abi.make_config(hq, hkv, S, W, nreq + 1, max_pages)
+    ctx = abi.Context(cfg)
+    ctx.load_rotations(cal["R_K"], cal["R_V"], cal["clip_K"], cal["clip_V"])
+    num_pages = (n + 15) // 16 + nreq * (suf // 16 + 2) + 16
+    cache = PagedCache(ctx, num_pages, device=device,
+                       page_order=draw_page_pool(seed, num_pages, True))
+    cache.reserve(0, n)
+    k, v = (t.to(torch.bfloat16).view(1, n, hkv, D).contiguous()
+            for t in draw_kv(seed, 1, n, hkv, D, device=device))
+    stream = torch.cuda.current_stream(device)
+    fresh = torch.tensor([0, S, 0, 0], dtype=torch.int32, device=device)
+    times = []
+    for it in range(max(3, args.warmup) + args.steps):
+        cache.state[0].copy_(fresh)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ctx.quant_append(cache.page_table, cache.state, k, v, 1, n, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if it >= max(3, args.warmup):
+            times.append(e0.elapsed_time(e1))
+    pre_us = float(np.mean(times)) * 1000.0
+    n_int2 = max(n - W, S) - S
+    pre_bytes = float(n * hkv * 2 * D * 2 + n_int2 * hkv * 96 + (S + W) * hkv * 2 * D * 2)
+    # 16 forks at 65536 tokens with private suffixes
+    for r in range(1, nreq + 1):
+        cache.fork(0, r, fork)
+        cache.reserve(r, fork + suf, upload=False)
+    cache.upload()
+    ks, vs = (t.to(torch.bfloat16).view(nreq, suf, hkv, D).contiguous()
+              for t in draw_kv(seed, 2, nreq * suf, hkv, D, device=device))
+    ctx.quant_append(cache.page_table[1:], cache.state[1:], ks, vs, nreq, suf, stream)
+    q = draw_queries(seed, 3, nreq, hq, hkv, D, device=device).to(torch.bfloat16).contiguous()
+    o = torch.empty(nreq, hq, D, device=device)
+    for _ in range(max(3, args.warmup)):
+        ctx.decode_attn(q, cache.page_table[1:], cache.state[1:], o, nreq, stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(args.steps):
+                ctx.decode_attn(q, cache.page_table[1:], cache.state[1:], o, nreq, cap)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dec_us = e0.elapsed_time(e1) * 1000.0 / args.steps
+    L = fork + suf
+    E = L - W
+    logical = float(nreq * (hkv * (96 * (E - S) + 512 * (S + W)) + 4 * ((E + 15) // 16)) + nreq * hq * D * 6)
+    unique = float(hkv * 96 * (fork - S) + nreq * hkv * (96 * (E - fork) + 512 * (S + W)) + nreq * hq * D * 6)
+    if dist:
+        t = torch.tensor([pre_us, dec_us], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        pre_us, dec_us = (float(x) for x in t.tolist())
+    return {"prefill_tokens": n, "prefill_us": pre_us, "prefill_bytes": pre_bytes,
+            "prefix_decode_us": dec_us, "prefix_logical_bytes": logical, "prefix_unique_bytes": unique}
+
+
+def footprint(name):
+    """Cache bytes of one layer of a workload: BF16 cache against this INT2 cache."""
+    s = WORKLOADS[name]
+    L = s.context
+    bf16 = s.batch * L * s.num_kv_heads * 2 * D * 2
+    n_int2 = max(L - s.recent, s.sink) - s.sink
+    pages = (L + 15) // 16
+    oscar = s.batch * (pages * s.num_kv_heads * 1536 + (s.sink + s.recent) * s.num_kv_heads * 2 * D * 2)
+    bits = {}
+    for g in (32, 64, 128):
+        bits["G%d_bits_per_int2_element" % g] = 2 + 32 / g
+    return {"workload": name, "bf16_bytes": bf16, "oscar_bytes": oscar, "ratio": round(bf16 / oscar, 3),
+            "int2_tokens_per_request": n_int2, **bits}
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline leg)
 # ---------------------------------------------------------------------------
@@ -451,7 +546,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_bs1_32k")
-    ap.add_argument("--extra", default="qwen3_32b_bs28_100k", help="second workload ('' to skip)")
+    ap.add_argument("--extra", default="qwen3_32b_bs28_100k,qwen3_8b_bs16_ragged",
+                    help="further decode workloads, comma separated ('' to skip)")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill / prefix-sharing measurement")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="measure only the prefill / prefix-sharing workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch (smaller cases for profiling captures)")
@@ -480,12 +579,20 @@ def main():
     if dist:
         dist.barrier()
     peak, peak_kind = peaks()
+    if args.prefill_only:
+        pre = run_prefill(args, device, rank, dist)
+        if rank == 0:
+            print(json.dumps({"prefill_only": True, **pre}))
+        if dist:
+            dist.destroy_process_group()
+        return
     main_res = run_oscar(args.workload, args, device, rank, world, dist, local)
     extras = []
     if args.extra:
         for name in args.extra.split(","):
             r = run_oscar(name, args, device, rank, world, dist, local, with_e2e=False)
             extras.append(r)
+    pre = None if args.no_prefill else run_prefill(args, device, rank, dist)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         dt, scale = oracle_step_sample(args.workload, 2)
@@ -530,6 +637,21 @@ def main():
                 "decode_gbs": round(r["decode_bytes"] / (r["decode_us"] * 1e-6) / 1e9, 1),
                 "roofline": roof(r), "clocks": r["clocks"], "layers_cycled": r["layers_cycled"],
             })
+        if pre is not None:
+            ach = pre["prefill_bytes"] / (pre["prefill_us"] * 1e-6) / 1e9
+            out["prefill"] = {
+                "workload": "prefill_128k_prefix16", "tokens": pre["prefill_tokens"],
+                "quant_append_us": round(pre["prefill_us"], 2),
+                "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                             "frac": round(ach / peak, 4), "traffic": None,
+                             "kernel": "quant_append call (tensor-core prefill + tail launches)",
+                             "algorithmic_bytes_per_launch": pre["prefill_bytes"]},
+                "prefix16_decode_us": round(pre["prefix_decode_us"], 2),
+                "prefix16_logical_gbs": round(pre["prefix_logical_bytes"] / (pre["prefix_decode_us"] * 1e-6) / 1e9, 1),
+                "prefix16_unique_bytes": pre["prefix_unique_bytes"],
+                "prefix16_logical_bytes": pre["prefix_logical_bytes"],
+            }
+        out["footprint"] = [footprint("qwen3_32b_bs28_100k"), footprint("qwen3_8b_bs1_32k")]
         print(json.dumps(out))
     if dist:
         dist.destroy_process_group()

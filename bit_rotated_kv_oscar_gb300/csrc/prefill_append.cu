@@ -114,16 +114,132 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// exact code of the quantiser: clamp(rint(fp32(x - zf) / sf), 0, 3) with the
-// quotient correctly rounded. A reciprocal product decides the code unless it
-// lands within a safety margin of a half-integer, where the IEEE division runs.
-__device__ __forceinline__ int quant_code(float x, float zf, float sf, float rsf) {
-  const float d = __fsub_rn(x, zf);
-  float u = __fmul_rn(d, rsf);
-  const float fr = u - floorf(u);
-  if (fabsf(fr - 0.5f) < 1e-4f) u = __fdiv_rn(d, sf);
-  u = fminf(fmaxf(rintf(u), 0.f), 3.f);
-  return (int)u;
+// Scale, zero and the 2-bit codes of one group of 32 rotated values, packed in
+// place into the page-block words (kw: K words, vh: V half-words) of the token.
+//
+// The quantiser is code = clamp(rint(fp32(fp32(xc - zf) * fp32(1 / sf))), 0, 3)
+// on the clipped value xc. Every step is monotone in x and the clip bounds map
+// to the extreme codes (they are the group's min / max after clipping), so the
+// code of the unclipped value clamped to [0, 3] is the same and only the min /
+// max are clipped. rint (nearest, ties to even) is an add of 1.5 * 2^23.
+template <int KIND, int GQ>
+__device__ __forceinline__ void group_quantise(const float (&v)[32], float clip, __half& s16, __half& z16,
+                                               uint32_t (&kw)[8], uint32_t (&vh)[16]) {
+  float mn = v[0], mx = v[0];
+#pragma unroll
+  for (int i = 1; i < 32; ++i) {
+    mn = fminf(mn, v[i]);
+    mx = fmaxf(mx, v[i]);
+  }
+  mn = fminf(fmaxf(mn, -clip), clip);
+  mx = fminf(fmaxf(mx, -clip), clip);
+  s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+  z16 = __float2half_rn(mn);
+  const float sf = __half2float(s16), zf = __half2float(z16);
+  const float rsf = sf != 0.f ? __frcp_rn(sf) : 0.f;  // sf == 0: every code is 0
+  constexpr float kMagic = 12582912.f;                 // 1.5 * 2^23
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float u = fminf(fmaxf(__fmul_rn(__fsub_rn(v[i], zf), rsf), 0.f), 3.f);
+    const uint32_t code = __float_as_uint(__fadd_rn(u, kMagic)) & 3u;
+    constexpr int kCh0 = 32 * GQ;
+    const int ch = kCh0 + i;                            // compile-time
+    const int si = ch >> 4, r = ch & 15;
+    if (KIND == 0)
+      kw[2 * ((r & 7) >> 1) + (r >> 3)] |= code << (16 * (r & 1) + 2 * si);
+    else
+      vh[2 * (r & 7) + (r >> 3)] |= code << (2 * si);
+  }
+}
+
+// Quantise job j from tensor memory: the warp reads TMEM lanes 32 (warp % 4) ..
+// (one token per thread) and the 64 columns of its HALF (two groups); codes go
+// to the partial-word scratch, scale / zero straight to the page block. All
+// channel indices are compile-time, so the packing stays in registers.
+template <int HALF, int KIND>
+__device__ __forceinline__ void pf_epilogue(const PrefillParams& p, int j, int c, int warp, int lane, int h,
+                                            int b, int64_t P0, int64_t d0, int64_t d1, uint32_t tmem,
+                                            uint32_t* kpart, uint16_t* vpart) {
+  const int tile = c + (j >> 1) * (int)gridDim.x;
+  constexpr int kind = KIND;
+  const int row = 32 * (warp & 3) + lane;
+  const int64_t pos = P0 + (int64_t)tile * kTileM + row;
+  const bool valid = pos >= d0 && pos < d1;
+  const uint32_t acc = tmem + (uint32_t)((j & 1) * kHeadDim) + ((uint32_t)(32 * (warp & 3)) << 16);
+  const float clip = (kind ? p.clip_V : p.clip_K)[h];
+  const int Hkv = p.num_kv_heads;
+  uint8_t* blk = nullptr;
+  if (valid) {
+    const int64_t pidx = pos / kPage;
+    const int32_t id = pidx < p.pt_stride ? p.page_table[(int64_t)b * p.pt_stride + pidx] : -1;
+    if (id >= 0 && id < p.num_pages)
+      blk = p.pool + ((int64_t)id * Hkv + h) * kBlockBytes;
+    else
+      atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
+  }
+  const int t = (int)(pos % kPage);
+  const int bb = (t & 7) >> 1, pair = t >> 3, th = t & 1;
+  uint32_t kw[8];
+  uint32_t vh[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) kw[i] = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) vh[i] = 0u;
+#pragma unroll
+  for (int gg = 0; gg < 2; ++gg) {
+    const int gq = 2 * HALF + gg;
+    float v[32];
+    tmem_ld32(acc + (uint32_t)(32 * gq), v);
+    if (valid && p.trace && pos < p.trace_positions) {
+      float* tr = p.trace + ((((size_t)b * p.trace_positions + pos) * Hkv + h) * 2 + kind) * kHeadDim + 32 * gq;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) tr[i] = v[i];
+    }
+    __half s16, z16;
+    if (gg == 0)
+      group_quantise<KIND, 2 * HALF>(v, clip, s16, z16, kw, vh);
+    else
+      group_quantise<KIND, 2 * HALF + 1>(v, clip, s16, z16, kw, vh);
+    if (blk) {
+      if (kind == 0) {
+        *reinterpret_cast<__half*>(blk + 1024 + 32 * bb + 8 * gq + 4 * pair + 2 * th) = s16;
+        *reinterpret_cast<__half*>(blk + 1152 + 4 * (2 * t + (gq >> 1)) + 2 * (gq & 1)) = z16;
+      } else {
+        uint8_t* m = blk + 1280 + 16 * (4 * gq + bb) + 4 * (2 * pair) + 2 * th;
+        *reinterpret_cast<__half*>(m) = s16;
+        *reinterpret_cast<__half*>(m + 4) = z16;
+      }
+    }
+  }
+  // combine the two column halves of every token, then store its codes
+  if (kind == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) kpart[(HALF * kTileM + row) * 8 + i] = kw[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) vpart[(HALF * kTileM + row) * 16 + i] = (uint16_t)vh[i];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (HALF == 0 && blk) {
+    const int a = t & 7, tt = t >> 3;
+    if (kind == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int b2 = i >> 1, x = i & 1;
+        const uint32_t w = kpart[row * 8 + i] | kpart[(kTileM + row) * 8 + i];
+        *reinterpret_cast<uint32_t*>(blk + 16 * (4 * a + b2) + 4 * (2 * tt + x)) = w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int a2 = i >> 1, x = i & 1;
+        const uint16_t w = (uint16_t)(vpart[row * 16 + i] | vpart[(kTileM + row) * 16 + i]);
+        *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a2 + bb) + 4 * (2 * tt + x) + 2 * th) = w;
+      }
+    }
+  }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(PrefillParams p) {
@@ -206,104 +322,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(Pre
   if (njobs > 0) load_job(0);
 
   auto epilogue = [&](int j) {
-    const int tile = c + (j >> 1) * (int)gridDim.x, kind = j & 1;
-    const int row = 32 * (warp & 3) + lane, half = warp >> 2;
-    const int64_t pos = P0 + (int64_t)tile * kTileM + row;
-    const bool valid = pos >= d0 && pos < d1;
-    const uint32_t acc = tmem + (uint32_t)((j & 1) * kHeadDim) + ((uint32_t)(32 * (warp & 3)) << 16);
-    const float clip = (kind ? p.clip_V : p.clip_K)[h];
-    uint32_t kw[8];
-    uint32_t vh[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) kw[i] = 0u;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) vh[i] = 0u;
-    // page block and slot of this token
-    uint8_t* blk = nullptr;
-    if (valid) {
-      const int64_t pidx = pos / kPage;
-      const int32_t id = pidx < p.pt_stride ? p.page_table[(int64_t)b * p.pt_stride + pidx] : -1;
-      if (id >= 0 && id < p.num_pages)
-        blk = p.pool + ((int64_t)id * Hkv + h) * kBlockBytes;
+    if (warp < 4) {
+      if (j & 1)
+        pf_epilogue<0, 1>(p, j, c, warp, lane, h, b, P0, d0, d1, tmem, kpart, vpart);
       else
-        atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
-    }
-    const int t = (int)(pos % kPage);
-    const int bb = (t & 7) >> 1, pair = t >> 3, th = t & 1;
-#pragma unroll
-    for (int gg = 0; gg < 2; ++gg) {
-      const int gq = 2 * half + gg;
-      float v[32];
-      tmem_ld32(acc + (uint32_t)(32 * gq), v);
-      if (valid && p.trace && pos < p.trace_positions) {
-        float* tr = p.trace + ((((size_t)b * p.trace_positions + pos) * Hkv + h) * 2 + kind) * kHeadDim + 32 * gq;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) tr[i] = v[i];
-      }
-      float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        v[i] = fminf(fmaxf(v[i], -clip), clip);
-        mn = fminf(mn, v[i]);
-        mx = fmaxf(mx, v[i]);
-      }
-      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-      const __half z16 = __float2half_rn(mn);
-      const float sf = __half2float(s16), zf = __half2float(z16);
-      const float rsf = sf != 0.f ? __frcp_rn(sf) : 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int code = sf != 0.f ? quant_code(v[i], zf, sf, rsf) : 0;
-        const int ch = 32 * gq + i;
-        const int si = ch >> 4, r = ch & 15;
-        if (kind == 0) {
-          const int x = r >> 3, b2 = (r & 7) >> 1, hi = r & 1;
-          kw[2 * b2 + x] |= (uint32_t)code << (16 * hi + 2 * si);
-        } else {
-          const int x = r >> 3, a = r & 7;
-          vh[2 * a + x] |= (uint32_t)code << (2 * si);
-        }
-      }
-      if (blk) {
-        if (kind == 0) {
-          *reinterpret_cast<__half*>(blk + 1024 + 32 * bb + 8 * gq + 4 * pair + 2 * th) = s16;
-          *reinterpret_cast<__half*>(blk + 1152 + 4 * (2 * t + (gq >> 1)) + 2 * (gq & 1)) = z16;
-        } else {
-          uint8_t* m = blk + 1280 + 16 * (4 * gq + bb) + 4 * (2 * pair) + 2 * th;
-          *reinterpret_cast<__half*>(m) = s16;
-          *reinterpret_cast<__half*>(m + 4) = z16;
-        }
-      }
-    }
-    // combine the two column halves of every token, then store its codes
-    if (kind == 0) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) kpart[(half * kTileM + row) * 8 + i] = kw[i];
+        pf_epilogue<0, 0>(p, j, c, warp, lane, h, b, P0, d0, d1, tmem, kpart, vpart);
     } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) vpart[(half * kTileM + row) * 16 + i] = (uint16_t)vh[i];
+      if (j & 1)
+        pf_epilogue<1, 1>(p, j, c, warp, lane, h, b, P0, d0, d1, tmem, kpart, vpart);
+      else
+        pf_epilogue<1, 0>(p, j, c, warp, lane, h, b, P0, d0, d1, tmem, kpart, vpart);
     }
-    tc_fence_before();
-    __syncthreads();
-    if (half == 0 && blk) {
-      const int a = t & 7, tt = t >> 3;
-      if (kind == 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int b2 = i >> 1, x = i & 1;
-          const uint32_t w = kpart[row * 8 + i] | kpart[(kTileM + row) * 8 + i];
-          *reinterpret_cast<uint32_t*>(blk + 16 * (4 * a + b2) + 4 * (2 * tt + x)) = w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int a2 = i >> 1, x = i & 1;
-          const uint16_t w = (uint16_t)(vpart[row * 16 + i] | vpart[(kTileM + row) * 16 + i]);
-          *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a2 + bb) + 4 * (2 * tt + x) + 2 * th) = w;
-        }
-      }
-    }
-    __syncthreads();
   };
 
   for (int j = 0; j < njobs && alive; ++j) {

@@ -183,7 +183,7 @@ oscar_quant_append_kernel(AppendParams p) {
           const float sf = __half2float(s16), zf = __half2float(z16);
           int code = 0;
           if (sf != 0.f) {
-            float u = rintf(__fdiv_rn(__fsub_rn(x, zf), sf));
+            float u = rintf(__fmul_rn(__fsub_rn(x, zf), __frcp_rn(sf)));
             u = fminf(fmaxf(u, 0.f), 3.f);
             code = (int)u;
           }

@@ -169,7 +169,7 @@ int oscar_load_rotations(oscar_ctx* ctx, const float* R_K, const float* R_V,
  * With E' = max(E, sink, L + n_new - recent): positions below sink go to the
  * sink, positions in [E, E') are rotated (x @ R), clipped to [-c, c],
  * quantised per group of 32 channels with s = fp16((max-min)/3), z = fp16(min),
- * code = clamp(rint((x - z)/s), 0, 3) (0 when s == 0), and packed; taken from
+ * code = clamp(rint((x - z) * fp32(1/s)), 0, 3) (0 when s == 0), and packed; taken from
  * the ring when already cached, else from k/v. The remaining new positions go
  * to the ring. Afterwards state = {L + n_new, E'}. */
 int oscar_quant_append(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,

@@ -197,9 +197,12 @@ def quantize_groups(x_rot32: np.ndarray, clip32, group: int = 32):
     The exact float32 sequence (our reading; the pages give no formula):
         x  = min(max(x_rot, -c), c)
         s  = fp16((mx - mn) / 3)      z = fp16(mn)      (fp32 divide, then RNE to fp16)
-        q  = 0 if s == 0 else clamp(rint_half_even((x - z) / s), 0, 3)
-    with z and s taken back to float32 before use. Returns (codes uint8
-    [..., d], scale float16 [..., d/group], zero float16 [..., d/group]).
+        r  = fp32(1 / s)                                (correctly rounded reciprocal)
+        q  = 0 if s == 0 else clamp(rint_half_even(fp32(fp32(x - z) * r)), 0, 3)
+    with z and s taken back to float32 before use: dividing by the scale is
+    taken as multiplying by its float32 reciprocal, one fixed rounding per
+    value. Returns (codes uint8 [..., d], scale float16 [..., d/group], zero
+    float16 [..., d/group]).
     """
     x = np.asarray(x_rot32, dtype=F32)
     c = np.asarray(clip32, dtype=F32)
@@ -217,7 +220,8 @@ def quantize_groups(x_rot32: np.ndarray, clip32, group: int = 32):
     diff = (xg - zf[..., None]).astype(F32)
     safe = np.where(sf == 0, F32(1.0), sf).astype(F32)
     with np.errstate(over="ignore", invalid="ignore"):
-        u = (diff / safe[..., None]).astype(F32)
+        rinv = (F32(1.0) / safe).astype(F32)
+        u = (diff * rinv[..., None]).astype(F32)
     code = np.clip(np.rint(u), 0, 3)
     code = np.where((sf == 0)[..., None], 0, code)
     return code.reshape(x.shape).astype(np.uint8), s16, z16
