@@ -340,7 +340,7 @@ static int append_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_stat
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // long appends: the tokens that go straight to INT2 run on the tensor cores,
   // the sink / ring / eviction tokens on the per-token kernel right after
-  if (n_new >= ctx->cfg.sink + ctx->cfg.recent + 128) {
+  if (n_new >= ctx->cfg.sink + ctx->cfg.recent + 128 && prefill_supported(k, v)) {
     PrefillParams pp{};
     pp.page_table = page_table;
     pp.pt_stride = ctx->cfg.max_pages_per_seq;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the CUDA translation units of liboscar.
 #pragma once
 
+#include <cuda.h>   // CUtensorMap (header only: the encoder is fetched from the driver at run time)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -57,6 +58,8 @@ struct AppendParams {
 
 // tokens that go straight from the input to INT2 during a long append
 struct PrefillParams {
+  CUtensorMap tmap_k;       // 4-D TMA maps of k / v: (channel, KV head, token, request), 64 x 1 x 128 x 1
+  CUtensorMap tmap_v;       // boxes with a 128-byte swizzle (written by launch_prefill_append)
   const int32_t* page_table;
   int32_t pt_stride;
   const oscar_seq_state* state;
@@ -119,6 +122,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // launchers (return cudaGetLastError())
 cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_prefill_append(const PrefillParams& p, int ctas_per_head, cudaStream_t s);
+bool prefill_supported(const void* k, const void* v);   // TMA needs 16-byte aligned inputs
 int prefill_image_bytes();
 cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s);
 int decode_smem_bytes();

@@ -11,33 +11,47 @@
 // [max(L, S), E') of an append) are handled here; sink tokens, ring occupants
 // and the ring entries they evict stay with oscar_quant_append_kernel. Tiles are
 // 128 page-aligned positions (8 pages) of one KV head of one request; a CTA
-// owns a strided set of tiles of one (request, KV head) and walks them as jobs
-// (tile, K) and (tile, V).
+// (one per SM) owns a strided set of tiles of one (request, KV head) and walks
+// them as jobs (tile, K), (tile, V), ...
 //
-// Per CTA (256 threads, one per SM): shared memory holds the four rotation
-// images (R_K hi/lo, R_V hi/lo; bf16, K-major, 128-byte swizzle, 32 KiB each),
-// two 32 KiB token-tile buffers and the packing scratch. Thread 0 issues the 16
-// tcgen05.mma (M 128, N 128, K 16; hi then lo) of a job into one of two
-// 128-column TMEM accumulators and commits them to an mbarrier; while they run,
-// all eight warps quantise the previous job: warp w reads TMEM lanes
-// 32 (w % 4) .. +31 (one token each) and columns 64 (w / 4) .. +63 (two groups),
-// and the next tile streams in with cp.async. Every mbarrier wait is bounded:
-// on expiry the kernel raises OSCAR_FLAG_TIMEOUT and stops issuing work.
+// Warp roles (320 threads), all hand-offs on mbarriers, no CTA-wide barrier in
+// the steady state:
+//   warp 8 (one lane)  TMA producer: each job's 128 x 128 bf16 token tile, as two
+//                      64-channel boxes with a 128-byte swizzle, into a 3-stage
+//                      ring of 32 KiB shared-memory slots;
+//   warp 9 (one lane)  MMA issuer: 16 tcgen05.mma (M 128, N 128, K 16; R_hi then
+//                      R_lo) per job into one of four 128-column accumulators
+//                      (512 TMEM columns), committed to the slot's "empty" and
+//                      the accumulator's "full" barrier;
+//   warps 0-3 / 4-7    K / V epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31,
+//                      one token per thread and all 128 columns, frees the
+//                      accumulator, then quantises and packs whole page-block
+//                      words, so no partial words are combined across warps.
+// The four rotation images (R_K hi/lo, R_V hi/lo; bf16, K-major, 128-byte
+// swizzle) stay in shared memory for the whole kernel. Every mbarrier wait is
+// bounded: on expiry the kernel raises OSCAR_FLAG_TIMEOUT, the other roles stop
+// at their next wait, copies and MMAs already issued are waited for (again with
+// a limit) and tensor memory is released.
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "oscar_internal.cuh"
 
 namespace oscar {
 
-constexpr int kPfThreads = 256;
+constexpr int kPfThreads = 320;
 constexpr int kTileM = 128;
 constexpr int kImageBytes = kHeadDim * kHeadDim * 2;     // one bf16 128 x 128 operand: 32 KiB
 constexpr int kAtomBytes = kTileM * 128;                 // 64 bf16 columns of 128 rows: 16 KiB
+constexpr int kStages = 3;                                // token-tile slots
+constexpr int kAccBufs = 4;                               // 128-column accumulators
 constexpr int kPfSmemImages = 4 * kImageBytes;            // R_K hi, R_K lo, R_V hi, R_V lo
-constexpr int kPfSmemX = 2 * kImageBytes;                 // two token tiles
-constexpr int kPfSmemPack = 2 * kTileM * 8 * 4 + 2 * kTileM * 16 * 2;  // partial K words, V half-words
-constexpr int kPfSmem = 1024 + kPfSmemImages + kPfSmemX + kPfSmemPack + 64;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kPfSmemStages = kStages * kImageBytes;
+constexpr int kPfSmemBars = 2 * (kStages + kAccBufs) * 8 + 16;
+constexpr int kPfSmem = 1024 + kPfSmemImages + kPfSmemStages + kPfSmemBars;
+constexpr uint32_t kTmemCols = kAccBufs * kHeadDim;       // 512
 constexpr long kSpinLimit = 1L << 20;
 
 // ---- PTX wrappers ------------------------------------------------------------
@@ -49,7 +63,6 @@ __device__ __forceinline__ void cp16(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_commit_pf() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_wait_all_pf() { asm volatile("cp.async.wait_group 0;\n" ::); }
-__device__ __forceinline__ void cp_wait_one_pf() { asm volatile("cp.async.wait_group 1;\n" ::); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
@@ -57,19 +70,48 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(addr), "r"(count));
 }
-// bounded wait on an mbarrier phase; false when the limit expires
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
+__device__ __forceinline__ void mbar_arrive(uint32_t addr) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(addr), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// bounded wait on an mbarrier phase; false when the limit expires or another
+// role has given up (abort set)
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, const volatile int* abort) {
   for (long it = 0; it < kSpinLimit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (done) return true;
+    if (mbar_test(addr, parity)) return true;
+    if ((it & 31) == 31 && *abort) return false;
   }
   return false;
+}
+// bounded wait used while tearing down after an abort
+__device__ __forceinline__ bool mbar_drain(uint32_t addr, uint32_t parity) {
+  for (long it = 0; it < kSpinLimit; ++it)
+    if (mbar_test(addr, parity)) return true;
+  return false;
+}
+
+// one 64-channel x 128-token box of a 4-D tensor map into shared memory,
+// completing on an mbarrier; the input is read once, so it is marked for early
+// eviction from L2
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                             uint32_t mbar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(mbar), "l"(policy)
+      : "memory");
 }
 
 // shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
@@ -98,8 +140,9 @@ __device__ __forceinline__ void umma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+
+// 32 consecutive accumulator columns of the warp's 32 TMEM lanes (no wait)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
@@ -109,27 +152,52 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// the registers of a tcgen05.ld are defined only after tcgen05.wait::ld; tying
+// them to an asm statement placed after the wait keeps every use behind it
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                 "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-// Scale, zero and the 2-bit codes of one group of 32 rotated values, packed in
-// place into the page-block words (kw: K words, vh: V half-words) of the token.
+// ---- quantiser -----------------------------------------------------------------
+// The code of a value is clamp(rint(fp32(fp32(xc - zf) * fp32(1 / sf))), 0, 3) on
+// the clipped value xc (rint: nearest, ties to even). Adding 1.5 * 2^23 rounds a
+// float in (-2^22, 2^22) to the nearest integer with ties to even and leaves
+// that integer in the low mantissa bits, so the code is carried as the float
+// kMagic + code. Every step is monotone in x, so clipping x and clamping to
+// [0, 3] together equal clamping the unclipped value's code to
+// [code(min_c), code(max_c)], the codes of the group's clipped extremes; that
+// is the only clamp applied per element.
 //
-// The quantiser is code = clamp(rint(fp32(fp32(xc - zf) * fp32(1 / sf))), 0, 3)
-// on the clipped value xc. Every step is monotone in x and the clip bounds map
-// to the extreme codes (they are the group's min / max after clipping), so the
-// code of the unclipped value clamped to [0, 3] is the same and only the min /
-// max are clipped. rint (nearest, ties to even) is an add of 1.5 * 2^23.
-template <int KIND, int GQ>
-__device__ __forceinline__ void group_quantise(const float (&v)[32], float clip, __half& s16, __half& z16,
-                                               uint32_t (&kw)[8], uint32_t (&vh)[16]) {
-  float mn = v[0], mx = v[0];
+// Packing: the bits of kMagic + code are kMagicBits + code, and each code goes to
+// a fixed 2-bit field of a word (shift s), so a word is accumulated as
+// sum (bits << s) and corrected once by the constant sum (kMagicBits << s).
+// For K every 32-bit word holds 16 codes (shifts 0, 2, ..., 30); for V every
+// 16-bit half-word holds 8 codes (shifts 0, 2, ..., 14) and the constant has no
+// bits below 16.
+constexpr float kMagic = 12582912.f;        // 1.5 * 2^23
+constexpr uint32_t kMagicBits = 0x4B400000u;
+
+__host__ __device__ constexpr uint32_t k_word_bias() {
+  uint32_t c = 0;
+  for (int s = 0; s < 32; s += 2) c += kMagicBits << s;
+  return c;
+}
+constexpr uint32_t kKWordBias = k_word_bias();
+
+template <int KIND, int GQ, int NW>
+__device__ __forceinline__ void group_quantise(const uint32_t (&r)[32], float clip, __half& s16, __half& z16,
+                                               uint32_t (&acc)[NW]) {
+  float mn = __uint_as_float(r[0]), mx = mn;
 #pragma unroll
   for (int i = 1; i < 32; ++i) {
-    mn = fminf(mn, v[i]);
-    mx = fmaxf(mx, v[i]);
+    mn = fminf(mn, __uint_as_float(r[i]));
+    mx = fmaxf(mx, __uint_as_float(r[i]));
   }
   mn = fminf(fmaxf(mn, -clip), clip);
   mx = fminf(fmaxf(mx, -clip), clip);
@@ -137,37 +205,29 @@ __device__ __forceinline__ void group_quantise(const float (&v)[32], float clip,
   z16 = __float2half_rn(mn);
   const float sf = __half2float(s16), zf = __half2float(z16);
   const float rsf = sf != 0.f ? __frcp_rn(sf) : 0.f;  // sf == 0: every code is 0
-  constexpr float kMagic = 12582912.f;                 // 1.5 * 2^23
+  const float lo = fminf(fmaxf(__fadd_rn(__fmul_rn(__fsub_rn(mn, zf), rsf), kMagic), kMagic), kMagic + 3.f);
+  const float hi = fminf(fmaxf(__fadd_rn(__fmul_rn(__fsub_rn(mx, zf), rsf), kMagic), kMagic), kMagic + 3.f);
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const float u = fminf(fmaxf(__fmul_rn(__fsub_rn(v[i], zf), rsf), 0.f), 3.f);
-    const uint32_t code = __float_as_uint(__fadd_rn(u, kMagic)) & 3u;
+    float m = __fadd_rn(__fmul_rn(__fsub_rn(__uint_as_float(r[i]), zf), rsf), kMagic);
+    m = fminf(fmaxf(m, lo), hi);
+    const uint32_t bits = __float_as_uint(m);
     constexpr int kCh0 = 32 * GQ;
     const int ch = kCh0 + i;                            // compile-time
-    const int si = ch >> 4, r = ch & 15;
+    const int si = ch >> 4, rr = ch & 15;
     if (KIND == 0)
-      kw[2 * ((r & 7) >> 1) + (r >> 3)] |= code << (16 * (r & 1) + 2 * si);
+      acc[2 * ((rr & 7) >> 1) + (rr >> 3)] += bits << (16 * (rr & 1) + 2 * si);
     else
-      vh[2 * (r & 7) + (r >> 3)] |= code << (2 * si);
+      acc[2 * (rr & 7) + (rr >> 3)] += bits << (2 * si);
   }
 }
 
-// Quantise job j from tensor memory: the warp reads TMEM lanes 32 (warp % 4) ..
-// (one token per thread) and the 64 columns of its HALF (two groups); codes go
-// to the partial-word scratch, scale / zero straight to the page block. All
-// channel indices are compile-time, so the packing stays in registers.
-template <int HALF, int KIND>
-__device__ __forceinline__ void pf_epilogue(const PrefillParams& p, int j, int c, int warp, int lane, int h,
-                                            int b, int64_t P0, int64_t d0, int64_t d1, uint32_t tmem,
-                                            uint32_t* kpart, uint16_t* vpart) {
-  const int tile = c + (j >> 1) * (int)gridDim.x;
-  constexpr int kind = KIND;
-  const int row = 32 * (warp & 3) + lane;
-  const int64_t pos = P0 + (int64_t)tile * kTileM + row;
-  const bool valid = pos >= d0 && pos < d1;
-  const uint32_t acc = tmem + (uint32_t)((j & 1) * kHeadDim) + ((uint32_t)(32 * (warp & 3)) << 16);
-  const float clip = (kind ? p.clip_V : p.clip_K)[h];
+// ---- epilogue: one token of one kind per thread ----------------------------------
+template <int KIND>
+__device__ __forceinline__ void pf_token(const PrefillParams& p, uint32_t (&r)[4][32], int64_t pos, bool valid,
+                                         int h, int b) {
   const int Hkv = p.num_kv_heads;
+  const float clip = (KIND ? p.clip_V : p.clip_K)[h];
   uint8_t* blk = nullptr;
   if (valid) {
     const int64_t pidx = pos / kPage;
@@ -177,85 +237,72 @@ __device__ __forceinline__ void pf_epilogue(const PrefillParams& p, int j, int c
     else
       atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
   }
-  const int t = (int)(pos % kPage);
-  const int bb = (t & 7) >> 1, pair = t >> 3, th = t & 1;
-  uint32_t kw[8];
-  uint32_t vh[16];
+  if (valid && p.trace && pos < p.trace_positions) {
+    float* tr = p.trace + ((((size_t)b * p.trace_positions + pos) * Hkv + h) * 2 + KIND) * kHeadDim;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) kw[i] = 0u;
+    for (int g = 0; g < kGroups; ++g)
 #pragma unroll
-  for (int i = 0; i < 16; ++i) vh[i] = 0u;
-#pragma unroll
-  for (int gg = 0; gg < 2; ++gg) {
-    const int gq = 2 * HALF + gg;
-    float v[32];
-    tmem_ld32(acc + (uint32_t)(32 * gq), v);
-    if (valid && p.trace && pos < p.trace_positions) {
-      float* tr = p.trace + ((((size_t)b * p.trace_positions + pos) * Hkv + h) * 2 + kind) * kHeadDim + 32 * gq;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) tr[i] = v[i];
-    }
-    __half s16, z16;
-    if (gg == 0)
-      group_quantise<KIND, 2 * HALF>(v, clip, s16, z16, kw, vh);
-    else
-      group_quantise<KIND, 2 * HALF + 1>(v, clip, s16, z16, kw, vh);
-    if (blk) {
-      if (kind == 0) {
-        *reinterpret_cast<__half*>(blk + 1024 + 32 * bb + 8 * gq + 4 * pair + 2 * th) = s16;
-        *reinterpret_cast<__half*>(blk + 1152 + 4 * (2 * t + (gq >> 1)) + 2 * (gq & 1)) = z16;
-      } else {
-        uint8_t* m = blk + 1280 + 16 * (4 * gq + bb) + 4 * (2 * pair) + 2 * th;
-        *reinterpret_cast<__half*>(m) = s16;
-        *reinterpret_cast<__half*>(m + 4) = z16;
-      }
-    }
+      for (int i = 0; i < 32; ++i) tr[32 * g + i] = __uint_as_float(r[g][i]);
   }
-  // combine the two column halves of every token, then store its codes
-  if (kind == 0) {
+  constexpr int NW = KIND == 0 ? 8 : 16;
+  uint32_t acc[NW];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) kpart[(HALF * kTileM + row) * 8 + i] = kw[i];
+  for (int i = 0; i < NW; ++i) acc[i] = 0u;
+  __half s16[kGroups], z16[kGroups];
+  group_quantise<KIND, 0>(r[0], clip, s16[0], z16[0], acc);
+  group_quantise<KIND, 1>(r[1], clip, s16[1], z16[1], acc);
+  group_quantise<KIND, 2>(r[2], clip, s16[2], z16[2], acc);
+  group_quantise<KIND, 3>(r[3], clip, s16[3], z16[3], acc);
+  if (!blk) return;
+  const int t = (int)(pos % kPage);
+  const int a = t & 7, bb = (t & 7) >> 1, pair = t >> 3, th = t & 1, tt = t >> 3;
+  if (KIND == 0) {
+    // codes: words (b2, x) at 16 (4 a + b2) + 4 (2 tt + x)
+#pragma unroll
+    for (int b2 = 0; b2 < 4; ++b2)
+      *reinterpret_cast<uint2*>(blk + 16 * (4 * a + b2) + 8 * tt) =
+          make_uint2(acc[2 * b2] - kKWordBias, acc[2 * b2 + 1] - kKWordBias);
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g)
+      *reinterpret_cast<__half*>(blk + 1024 + 32 * bb + 8 * g + 4 * pair + 2 * th) = s16[g];
+    // zeros of the four groups are contiguous: 1152 + 8 t + 2 g
+    const uint32_t z01 = (uint32_t)__half_as_ushort(z16[0]) | ((uint32_t)__half_as_ushort(z16[1]) << 16);
+    const uint32_t z23 = (uint32_t)__half_as_ushort(z16[2]) | ((uint32_t)__half_as_ushort(z16[3]) << 16);
+    *reinterpret_cast<uint2*>(blk + 1152 + 8 * t) = make_uint2(z01, z23);
   } else {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) vpart[(HALF * kTileM + row) * 16 + i] = (uint16_t)vh[i];
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (HALF == 0 && blk) {
-    const int a = t & 7, tt = t >> 3;
-    if (kind == 0) {
+    for (int i = 0; i < 16; ++i) {
+      const int a2 = i >> 1, x = i & 1;
+      *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a2 + bb) + 4 * (2 * tt + x) + 2 * th) = (uint16_t)acc[i];
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int b2 = i >> 1, x = i & 1;
-        const uint32_t w = kpart[row * 8 + i] | kpart[(kTileM + row) * 8 + i];
-        *reinterpret_cast<uint32_t*>(blk + 16 * (4 * a + b2) + 4 * (2 * tt + x)) = w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int a2 = i >> 1, x = i & 1;
-        const uint16_t w = (uint16_t)(vpart[row * 16 + i] | vpart[(kTileM + row) * 16 + i]);
-        *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a2 + bb) + 4 * (2 * tt + x) + 2 * th) = w;
-      }
+    for (int g = 0; g < kGroups; ++g) {
+      uint8_t* m = blk + 1280 + 16 * (4 * g + bb) + 4 * (2 * pair) + 2 * th;
+      *reinterpret_cast<__half*>(m) = s16[g];
+      *reinterpret_cast<__half*>(m + 4) = z16[g];
     }
   }
-  __syncthreads();
 }
 
-__global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(PrefillParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t dsm_raw[];
   // 1024-byte alignment for the swizzled operands
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* img = dsm;                                     // 4 rotation images
-  uint8_t* xbuf = img + kPfSmemImages;                    // 2 token tiles
-  uint32_t* kpart = reinterpret_cast<uint32_t*>(xbuf + kPfSmemX);       // [2][128][8]
-  uint16_t* vpart = reinterpret_cast<uint16_t*>(kpart + 2 * kTileM * 8);  // [2][128][16]
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(vpart + 2 * kTileM * 16);  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mbar + 2);
+  uint8_t* img = dsm;                                      // 4 rotation images
+  uint8_t* slot = img + kPfSmemImages;                     // kStages token tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(slot + kPfSmemStages);
+  uint64_t* full = bars;                                   // [kStages] tile landed (TMA bytes)
+  uint64_t* empty = full + kStages;                        // [kStages] tile consumed (MMA commit)
+  uint64_t* accf = empty + kStages;                        // [kAccBufs] accumulator ready (MMA commit)
+  uint64_t* acce = accf + kAccBufs;                        // [kAccBufs] accumulator read (4 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + kAccBufs);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __shared__ oscar_seq_state s_st;
+  __shared__ int s_loads, s_mmas;                          // jobs issued by the producer / MMA issuer
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int S = p.sink, W = p.recent, Hkv = p.num_kv_heads;
+  const int S = p.sink, W = p.recent;
 
   // rotation images are constant: stage them before waiting for earlier kernels
   {
@@ -263,19 +310,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(Pre
     for (int i = tid; i < kPfSmemImages / 16; i += kPfThreads) cp16(img + 16 * i, src + 16 * i);
     cp_commit_pf();
   }
+  if (tid == 256) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
+  }
   pdl_trigger();
   pdl_wait();
 
-  __shared__ oscar_seq_state s_st;
   if (tid == 0) s_st = p.state[b];
-  if (warp == 0) {
+  if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
   }
   if (tid == 0) {
-    mbar_init(smem_u32(&mbar[0]), 1);
-    mbar_init(smem_u32(&mbar[1]), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < kAccBufs; ++i) {
+      mbar_init(smem_u32(&accf[i]), 1);
+      mbar_init(smem_u32(&acce[i]), 4);
+    }
+    *abort_flag = 0;
+    s_loads = 0;
+    s_mmas = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   cp_wait_all_pf();
@@ -297,110 +356,153 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(Pre
   const int ntiles = d1 > d0 ? (int)((d1 - P0 + kTileM - 1) / kTileM) : 0;
   const int nmine = ntiles > c ? (ntiles - c + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   const int njobs = 2 * nmine;
+  auto tile_start = [&](int j) { return P0 + (int64_t)(c + (j >> 1) * (int)gridDim.x) * kTileM; };
 
-  const size_t tok_stride = (size_t)Hkv * kHeadDim;    // elements between tokens of the input
-  const __nv_bfloat16* xbase_k = p.k + ((size_t)b * p.n_new * Hkv + h) * kHeadDim;
-  const __nv_bfloat16* xbase_v = p.v + ((size_t)b * p.n_new * Hkv + h) * kHeadDim;
-
-  // stage the token rows of job j into tile buffer j & 1 (128-byte swizzle, K-major)
-  auto load_job = [&](int j) {
-    const int tile = c + (j >> 1) * (int)gridDim.x;
-    const __nv_bfloat16* xb = (j & 1) ? xbase_v : xbase_k;
-    uint8_t* buf = xbuf + (size_t)(j & 1) * kImageBytes;
-    for (int i = tid; i < kTileM * 16; i += kPfThreads) {
-      const int r = i >> 4, chunk = i & 15;
-      const int64_t pos = P0 + (int64_t)tile * kTileM + r;
-      if (pos < d0 || pos >= d1) continue;
-      const __nv_bfloat16* src = xb + (size_t)(pos - L) * tok_stride + 8 * chunk;
-      const int atom = chunk >> 3, cc = chunk & 7;
-      cp16(buf + atom * kAtomBytes + r * 128 + ((cc ^ (r & 7)) << 4), src);
+  if (warp == 8) {
+    // ---- TMA producer --------------------------------------------------------
+    if (lane == 0) {
+      uint64_t policy;
+      asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(policy));
+      for (int j = 0; j < njobs; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages && !mbar_wait(smem_u32(&empty[s]), (uint32_t)((j / kStages - 1) & 1), abort_flag)) {
+          *abort_flag = 1;
+          break;
+        }
+        const CUtensorMap* map = (j & 1) ? &p.tmap_v : &p.tmap_k;
+        const int tok = (int)(tile_start(j) - L);   // row of the tile's first position in the input
+        const uint32_t dst = smem_u32(slot + (size_t)s * kImageBytes);
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_expect_tx(fb, (uint32_t)kImageBytes);
+        tma_load_box(dst, map, 0, h, tok, b, fb, policy);
+        tma_load_box(dst + kAtomBytes, map, 64, h, tok, b, fb, policy);
+        s_loads = j + 1;
+      }
     }
-    cp_commit_pf();
-  };
-
-  bool alive = true;
-  if (njobs > 0) load_job(0);
-
-  auto epilogue = [&](int j) {
-    if (warp < 4) {
-      if (j & 1)
-        pf_epilogue<0, 1>(p, j, c, warp, lane, h, b, P0, d0, d1, tmem, kpart, vpart);
-      else
-        pf_epilogue<0, 0>(p, j, c, warp, lane, h, b, P0, d0, d1, tmem, kpart, vpart);
-    } else {
-      if (j & 1)
-        pf_epilogue<1, 1>(p, j, c, warp, lane, h, b, P0, d0, d1, tmem, kpart, vpart);
-      else
-        pf_epilogue<1, 0>(p, j, c, warp, lane, h, b, P0, d0, d1, tmem, kpart, vpart);
+  } else if (warp == 9) {
+    // ---- MMA issuer ----------------------------------------------------------
+    if (lane == 0) {
+      for (int j = 0; j < njobs; ++j) {
+        const int s = j % kStages, a = j % kAccBufs;
+        if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((j / kStages) & 1), abort_flag) ||
+            (j >= kAccBufs &&
+             !mbar_wait(smem_u32(&acce[a]), (uint32_t)((j / kAccBufs - 1) & 1), abort_flag))) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const int kind = j & 1;
+        const uint32_t a_base = smem_u32(slot + (size_t)s * kImageBytes);
+        const uint32_t hi_base = smem_u32(img + (size_t)(2 * kind) * kImageBytes);
+        const uint32_t lo_base = smem_u32(img + (size_t)(2 * kind + 1) * kImageBytes);
+        const uint32_t d_tmem = tmem + (uint32_t)(a * kHeadDim);
+#pragma unroll
+        for (int term = 0; term < 2; ++term) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (uint32_t)((kk >> 2) * kAtomBytes + (kk & 3) * 32);
+            umma_bf16(d_tmem, sw128_desc(a_base + off), sw128_desc((term ? lo_base : hi_base) + off),
+                      (term | kk) ? 1u : 0u);
+          }
+        }
+        umma_commit(smem_u32(&empty[s]));
+        umma_commit(smem_u32(&accf[a]));
+        s_mmas = j + 1;
+      }
     }
-  };
-
-  for (int j = 0; j < njobs && alive; ++j) {
-    // (a) the MMAs of job j - 1 are done: its tile buffer and accumulator are readable
-    if (j >= 1) {
-      const bool done = mbar_wait(smem_u32(&mbar[(j - 1) & 1]), ((j - 1) >> 1) & 1);
-      alive = __syncthreads_and(done) != 0;  // one decision for the whole CTA
-      if (!alive) {
-        if (tid == 0) atomicOr(p.err_flags, OSCAR_FLAG_TIMEOUT);
+  } else {
+    // ---- epilogue: warps 0-3 take the K jobs, warps 4-7 the V jobs ---------------
+    const int kind = warp >> 2;
+    const int row = 32 * (warp & 3) + lane;
+    for (int j = kind; j < njobs; j += 2) {
+      const int a = j % kAccBufs;
+      const bool ready = mbar_wait(smem_u32(&accf[a]), (uint32_t)((j / kAccBufs) & 1), abort_flag);
+      if (!__all_sync(0xffffffffu, ready)) {
+        if (lane == 0) *abort_flag = 1;
         break;
       }
-    }
-    // (b) prefetch job j + 1 into the buffer job j - 1 used
-    if (j + 1 < njobs) {
-      load_job(j + 1);
-      cp_wait_one_pf();
-    } else {
-      cp_wait_all_pf();
-    }
-    // (c) job j's tile is in shared memory
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // (d) issue job j
-    if (tid == 0) {
-      const int kind = j & 1;
-      const uint32_t a_base = smem_u32(xbuf + (size_t)(j & 1) * kImageBytes);
-      const uint32_t hi_base = smem_u32(img + (size_t)(2 * kind) * kImageBytes);
-      const uint32_t lo_base = smem_u32(img + (size_t)(2 * kind + 1) * kImageBytes);
-      const uint32_t d_tmem = tmem + (uint32_t)((j & 1) * kHeadDim);
-#pragma unroll
-      for (int term = 0; term < 2; ++term) {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (uint32_t)((kk >> 2) * kAtomBytes + (kk & 3) * 32);
-          umma_bf16(d_tmem, sw128_desc(a_base + off), sw128_desc((term ? lo_base : hi_base) + off),
-                    (term | kk) ? 1u : 0u);
-        }
-      }
-      umma_commit(smem_u32(&mbar[j & 1]));
-    }
-    // (e) quantise job j - 1 while job j runs
-    if (j >= 1) {
       tc_fence_after();
-      epilogue(j - 1);
+      uint32_t r[4][32];
+      const uint32_t taddr = tmem + (uint32_t)(a * kHeadDim) + ((uint32_t)(32 * (warp & 3)) << 16);
+      tmem_ld32(taddr, r[0]);
+      tmem_ld32(taddr + 32, r[1]);
+      tmem_ld32(taddr + 64, r[2]);
+      tmem_ld32(taddr + 96, r[3]);
+      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+      tmem_regs_ready(r[0]);
+      tmem_regs_ready(r[1]);
+      tmem_regs_ready(r[2]);
+      tmem_regs_ready(r[3]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acce[a]));   // the accumulator may be overwritten
+      const int64_t pos = tile_start(j) + row;
+      const bool valid = pos >= d0 && pos < d1;
+      if (kind == 0)
+        pf_token<0>(p, r, pos, valid, h, b);
+      else
+        pf_token<1>(p, r, pos, valid, h, b);
     }
   }
-  if (alive && njobs > 0) {
-    const int j = njobs - 1;
-    const bool done = mbar_wait(smem_u32(&mbar[j & 1]), (j >> 1) & 1);
-    if (__syncthreads_and(done)) {
-      tc_fence_after();
-      epilogue(j);
-    } else if (tid == 0) {
-      atomicOr(p.err_flags, OSCAR_FLAG_TIMEOUT);
-    }
-  }
-  cp_wait_all_pf();
+
+  // ---- teardown ------------------------------------------------------------------
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (*abort_flag) {
+    if (tid == 0) atomicOr(p.err_flags, OSCAR_FLAG_TIMEOUT);
+    if (tid == 256) {
+      // tiles still landing in shared memory
+      for (int j = s_mmas; j < s_loads; ++j) mbar_drain(smem_u32(&full[j % kStages]), (uint32_t)((j / kStages) & 1));
+    }
+    if (tid == 288 && s_mmas > 0) {
+      // MMAs still writing tensor memory (a commit tracks every earlier MMA)
+      const int j = s_mmas - 1;
+      mbar_drain(smem_u32(&accf[j % kAccBufs]), (uint32_t)((j / kAccBufs) & 1));
+    }
+    __syncthreads();
+  }
+  if (warp == 9) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
   }
 }
 
-cudaError_t launch_prefill_append(const PrefillParams& p, int ctas_per_head, cudaStream_t s) {
+// ---- host side -------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// k or v [batch][n_new][Hkv][128] bf16 as a 4-D map (channel, head, token, request)
+// with 64 x 1 x 128 x 1 boxes: each box is one 16 KiB swizzled operand atom
+bool encode_map(CUtensorMap* map, const void* base, int hkv, int n_new, int batch) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)n_new, (cuuint64_t)batch};
+  const cuuint64_t row = (cuuint64_t)kHeadDim * 2;
+  const cuuint64_t strides[3] = {row, row * hkv, row * hkv * (cuuint64_t)n_new};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kTileM, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_supported(const void* k, const void* v) {
+  return ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) == 0;
+}
+
+cudaError_t launch_prefill_append(const PrefillParams& p_in, int ctas_per_head, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(oscar_prefill_append_kernel,
@@ -408,6 +510,10 @@ cudaError_t launch_prefill_append(const PrefillParams& p, int ctas_per_head, cud
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  PrefillParams p = p_in;
+  if (!encode_map(&p.tmap_k, p.k, p.num_kv_heads, p.n_new, p.batch) ||
+      !encode_map(&p.tmap_v, p.v, p.num_kv_heads, p.n_new, p.batch))
+    return cudaErrorInvalidValue;
   cudaError_t e = launch_pdl(oscar_prefill_append_kernel, dim3(ctas_per_head, p.num_kv_heads, p.batch),
                              dim3(kPfThreads), kPfSmem, s, p);
   if (e != cudaSuccess) return e;

@@ -71,3 +71,20 @@ def test_prefill_fold_rv():
     layer.append(0, k, v, trace)
     check_int2(layer, 0, trace)
     check_decode(layer, 1)
+
+
+@pytest.mark.parametrize("frac", [0.15, 0.02])
+def test_prefill_heavy_clipping(frac):
+    """Clip values far below the calibrated ones: most groups have clipped
+    extremes (and some are clipped whole), so codes of values beyond the clip
+    must come out as the codes of the clip itself."""
+    layer = Layer(8, 2, 4, 64, 1, 2048, seed=11 + int(frac * 100))
+    for key in ("clip_K32", "clip_V32", "clip_K", "clip_V"):
+        layer.cal[key] = layer.cal[key] * frac
+    layer.ctx.load_rotations(layer.cal["R_K32"], layer.r_v32, layer.cal["clip_K32"], layer.cal["clip_V32"])
+    k, v = layer.draw(1700)
+    trace = layer.new_trace(2048)
+    layer.append(0, k, v, trace)
+    check_int2(layer, 0, trace)
+    check_decode(layer, 1)
+    assert layer.ctx.error_flags() == 0
