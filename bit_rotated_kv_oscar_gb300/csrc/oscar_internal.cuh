@@ -54,6 +54,7 @@ struct AppendParams {
   // last `recent` new tokens (virtual index v < sink -> token v, else token
   // n_new - recent + (v - sink)) and skips tokens that go straight to INT2
   int32_t tail_only;
+  int32_t tokens_per_cta;   // set by launch_quant_append
 };
 
 // tokens that go straight from the input to INT2 during a long append

@@ -14,19 +14,22 @@
 // (one per SM) owns a strided set of tiles of one (request, KV head) and walks
 // them as jobs (tile, K), (tile, V), ...
 //
-// Warp roles (320 threads), all hand-offs on mbarriers, no CTA-wide barrier in
+// Warp roles (576 threads), all hand-offs on mbarriers, no CTA-wide barrier in
 // the steady state:
-//   warp 8 (one lane)  TMA producer: each job's 128 x 128 bf16 token tile, as two
+//   warp 16 (one lane) TMA producer: each job's 128 x 128 bf16 token tile, as two
 //                      64-channel boxes with a 128-byte swizzle, into a 3-stage
 //                      ring of 32 KiB shared-memory slots;
-//   warp 9 (one lane)  MMA issuer: 16 tcgen05.mma (M 128, N 128, K 16; R_hi then
+//   warp 17 (one lane) MMA issuer: 16 tcgen05.mma (M 128, N 128, K 16; R_hi then
 //                      R_lo) per job into one of four 128-column accumulators
 //                      (512 TMEM columns), committed to the slot's "empty" and
 //                      the accumulator's "full" barrier;
-//   warps 0-3 / 4-7    K / V epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31,
-//                      one token per thread and all 128 columns, frees the
-//                      accumulator, then quantises and packs whole page-block
-//                      words, so no partial words are combined across warps.
+//   warps 0-15         epilogue, one warpgroup per accumulator (jobs j = g mod 4
+//                      for warpgroup g, so warpgroups 0 / 2 see K, 1 / 3 see V):
+//                      warp w reads TMEM lanes 32 (w % 4) .. +31, one token per
+//                      thread and all 128 columns, frees the accumulator, then
+//                      quantises and packs whole page-block words, so no partial
+//                      words are combined across warps. K and V run the same
+//                      instructions up to the final stores.
 // The four rotation images (R_K hi/lo, R_V hi/lo; bf16, K-major, 128-byte
 // swizzle) stay in shared memory for the whole kernel. Every mbarrier wait is
 // bounded: on expiry the kernel raises OSCAR_FLAG_TIMEOUT, the other roles stop
@@ -41,7 +44,9 @@
 
 namespace oscar {
 
-constexpr int kPfThreads = 320;
+constexpr int kPfThreads = 576;
+constexpr int kProducerTid = 512;                        // lane 0 of warp 16
+constexpr int kMmaTid = 544;                             // lane 0 of warp 17
 constexpr int kTileM = 128;
 constexpr int kImageBytes = kHeadDim * kHeadDim * 2;     // one bf16 128 x 128 operand: 32 KiB
 constexpr int kAtomBytes = kTileM * 128;                 // 64 bf16 columns of 128 rows: 16 KiB
@@ -174,25 +179,17 @@ __device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
 // [code(min_c), code(max_c)], the codes of the group's clipped extremes; that
 // is the only clamp applied per element.
 //
-// Packing: the bits of kMagic + code are kMagicBits + code, and each code goes to
-// a fixed 2-bit field of a word (shift s), so a word is accumulated as
-// sum (bits << s) and corrected once by the constant sum (kMagicBits << s).
-// For K every 32-bit word holds 16 codes (shifts 0, 2, ..., 30); for V every
-// 16-bit half-word holds 8 codes (shifts 0, 2, ..., 14) and the constant has no
-// bits below 16.
+// Packing: the bits of kMagic + code are kMagicBits + code. Every code of a token
+// goes to a 2-bit field of one of 16 half-words: channel ch = 16 si + rr to
+// half-word 2 (rr % 8) + rr / 8 at bit 2 si (the V layout); a K word (b2, x) is the
+// pair of half-words 4 b2 + x (low) and 4 b2 + 2 + x (high). A half-word is
+// accumulated in 32 bits as sum (bits << 2 si); kMagicBits has no bits below 16,
+// so the low 16 bits are exactly the packed codes.
 constexpr float kMagic = 12582912.f;        // 1.5 * 2^23
-constexpr uint32_t kMagicBits = 0x4B400000u;
 
-__host__ __device__ constexpr uint32_t k_word_bias() {
-  uint32_t c = 0;
-  for (int s = 0; s < 32; s += 2) c += kMagicBits << s;
-  return c;
-}
-constexpr uint32_t kKWordBias = k_word_bias();
-
-template <int KIND, int GQ, int NW>
+template <int GQ>
 __device__ __forceinline__ void group_quantise(const uint32_t (&r)[32], float clip, __half& s16, __half& z16,
-                                               uint32_t (&acc)[NW]) {
+                                               uint32_t (&acc)[16]) {
   float mn = __uint_as_float(r[0]), mx = mn;
 #pragma unroll
   for (int i = 1; i < 32; ++i) {
@@ -211,64 +208,52 @@ __device__ __forceinline__ void group_quantise(const uint32_t (&r)[32], float cl
   for (int i = 0; i < 32; ++i) {
     float m = __fadd_rn(__fmul_rn(__fsub_rn(__uint_as_float(r[i]), zf), rsf), kMagic);
     m = fminf(fmaxf(m, lo), hi);
-    const uint32_t bits = __float_as_uint(m);
     constexpr int kCh0 = 32 * GQ;
     const int ch = kCh0 + i;                            // compile-time
     const int si = ch >> 4, rr = ch & 15;
-    if (KIND == 0)
-      acc[2 * ((rr & 7) >> 1) + (rr >> 3)] += bits << (16 * (rr & 1) + 2 * si);
-    else
-      acc[2 * (rr & 7) + (rr >> 3)] += bits << (2 * si);
+    acc[2 * (rr & 7) + (rr >> 3)] += __float_as_uint(m) << (2 * si);
   }
 }
 
+__device__ __forceinline__ uint32_t low_halves(uint32_t lo, uint32_t hi) {
+  return __byte_perm(lo, hi, 0x5410);
+}
+
 // ---- epilogue: one token of one kind per thread ----------------------------------
-template <int KIND>
-__device__ __forceinline__ void pf_token(const PrefillParams& p, uint32_t (&r)[4][32], int64_t pos, bool valid,
-                                         int h, int b) {
-  const int Hkv = p.num_kv_heads;
-  const float clip = (KIND ? p.clip_V : p.clip_K)[h];
-  uint8_t* blk = nullptr;
-  if (valid) {
-    const int64_t pidx = pos / kPage;
-    const int32_t id = pidx < p.pt_stride ? p.page_table[(int64_t)b * p.pt_stride + pidx] : -1;
-    if (id >= 0 && id < p.num_pages)
-      blk = p.pool + ((int64_t)id * Hkv + h) * kBlockBytes;
-    else
-      atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
-  }
+__device__ __forceinline__ uint8_t* token_block(const PrefillParams& p, int64_t pos, bool valid, int h, int b) {
+  if (!valid) return nullptr;
+  const int64_t pidx = pos / kPage;
+  const int32_t id = pidx < p.pt_stride ? p.page_table[(int64_t)b * p.pt_stride + pidx] : -1;
+  if (id >= 0 && id < p.num_pages) return p.pool + ((int64_t)id * p.num_kv_heads + h) * kBlockBytes;
+  atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
+  return nullptr;
+}
+
+__device__ __forceinline__ void trace_group(const PrefillParams& p, const uint32_t (&r)[32], int64_t pos, bool valid,
+                                            int h, int b, int kind, int gq) {
   if (valid && p.trace && pos < p.trace_positions) {
-    float* tr = p.trace + ((((size_t)b * p.trace_positions + pos) * Hkv + h) * 2 + KIND) * kHeadDim;
+    float* tr = p.trace + ((((size_t)b * p.trace_positions + pos) * p.num_kv_heads + h) * 2 + kind) * kHeadDim;
 #pragma unroll
-    for (int g = 0; g < kGroups; ++g)
-#pragma unroll
-      for (int i = 0; i < 32; ++i) tr[32 * g + i] = __uint_as_float(r[g][i]);
+    for (int i = 0; i < 32; ++i) tr[32 * gq + i] = __uint_as_float(r[i]);
   }
-  constexpr int NW = KIND == 0 ? 8 : 16;
-  uint32_t acc[NW];
-#pragma unroll
-  for (int i = 0; i < NW; ++i) acc[i] = 0u;
-  __half s16[kGroups], z16[kGroups];
-  group_quantise<KIND, 0>(r[0], clip, s16[0], z16[0], acc);
-  group_quantise<KIND, 1>(r[1], clip, s16[1], z16[1], acc);
-  group_quantise<KIND, 2>(r[2], clip, s16[2], z16[2], acc);
-  group_quantise<KIND, 3>(r[3], clip, s16[3], z16[3], acc);
-  if (!blk) return;
+}
+
+__device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos, const uint32_t (&acc)[16],
+                                            const uint32_t (&sz)[kGroups]) {
   const int t = (int)(pos % kPage);
   const int a = t & 7, bb = (t & 7) >> 1, pair = t >> 3, th = t & 1, tt = t >> 3;
-  if (KIND == 0) {
+  if (kind == 0) {
     // codes: words (b2, x) at 16 (4 a + b2) + 4 (2 tt + x)
 #pragma unroll
     for (int b2 = 0; b2 < 4; ++b2)
       *reinterpret_cast<uint2*>(blk + 16 * (4 * a + b2) + 8 * tt) =
-          make_uint2(acc[2 * b2] - kKWordBias, acc[2 * b2 + 1] - kKWordBias);
+          make_uint2(low_halves(acc[4 * b2], acc[4 * b2 + 2]), low_halves(acc[4 * b2 + 1], acc[4 * b2 + 3]));
 #pragma unroll
     for (int g = 0; g < kGroups; ++g)
-      *reinterpret_cast<__half*>(blk + 1024 + 32 * bb + 8 * g + 4 * pair + 2 * th) = s16[g];
+      *reinterpret_cast<uint16_t*>(blk + 1024 + 32 * bb + 8 * g + 4 * pair + 2 * th) = (uint16_t)sz[g];
     // zeros of the four groups are contiguous: 1152 + 8 t + 2 g
-    const uint32_t z01 = (uint32_t)__half_as_ushort(z16[0]) | ((uint32_t)__half_as_ushort(z16[1]) << 16);
-    const uint32_t z23 = (uint32_t)__half_as_ushort(z16[2]) | ((uint32_t)__half_as_ushort(z16[3]) << 16);
-    *reinterpret_cast<uint2*>(blk + 1152 + 8 * t) = make_uint2(z01, z23);
+    *reinterpret_cast<uint2*>(blk + 1152 + 8 * t) =
+        make_uint2(__byte_perm(sz[0], sz[1], 0x7632), __byte_perm(sz[2], sz[3], 0x7632));
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -278,8 +263,8 @@ __device__ __forceinline__ void pf_token(const PrefillParams& p, uint32_t (&r)[4
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
       uint8_t* m = blk + 1280 + 16 * (4 * g + bb) + 4 * (2 * pair) + 2 * th;
-      *reinterpret_cast<__half*>(m) = s16[g];
-      *reinterpret_cast<__half*>(m + 4) = z16[g];
+      *reinterpret_cast<uint16_t*>(m) = (uint16_t)sz[g];
+      *reinterpret_cast<uint16_t*>(m + 4) = (uint16_t)(sz[g] >> 16);
     }
   }
 }
@@ -310,7 +295,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
     for (int i = tid; i < kPfSmemImages / 16; i += kPfThreads) cp16(img + 16 * i, src + 16 * i);
     cp_commit_pf();
   }
-  if (tid == 256) {
+  if (tid == kProducerTid) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
   }
@@ -318,7 +303,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
   pdl_wait();
 
   if (tid == 0) s_st = p.state[b];
-  if (warp == 9) {
+  if (warp == kMmaTid / 32) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
@@ -358,7 +343,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
   const int njobs = 2 * nmine;
   auto tile_start = [&](int j) { return P0 + (int64_t)(c + (j >> 1) * (int)gridDim.x) * kTileM; };
 
-  if (warp == 8) {
+  if (warp == kProducerTid / 32) {
     // ---- TMA producer --------------------------------------------------------
     if (lane == 0) {
       uint64_t policy;
@@ -379,7 +364,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
         s_loads = j + 1;
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == kMmaTid / 32) {
     // ---- MMA issuer ----------------------------------------------------------
     if (lane == 0) {
       for (int j = 0; j < njobs; ++j) {
@@ -411,37 +396,46 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
       }
     }
   } else {
-    // ---- epilogue: warps 0-3 take the K jobs, warps 4-7 the V jobs ---------------
-    const int kind = warp >> 2;
+    // ---- epilogue: warpgroup g takes the jobs j = g (mod 4), accumulator g -------
+    const int g = warp >> 2, kind = g & 1;
     const int row = 32 * (warp & 3) + lane;
-    for (int j = kind; j < njobs; j += 2) {
-      const int a = j % kAccBufs;
-      const bool ready = mbar_wait(smem_u32(&accf[a]), (uint32_t)((j / kAccBufs) & 1), abort_flag);
+    const float clip = (kind ? p.clip_V : p.clip_K)[h];
+    const uint32_t taddr = tmem + (uint32_t)(g * kHeadDim) + ((uint32_t)(32 * (warp & 3)) << 16);
+    for (int j = g; j < njobs; j += kAccBufs) {
+      const bool ready = mbar_wait(smem_u32(&accf[g]), (uint32_t)((j / kAccBufs) & 1), abort_flag);
       if (!__all_sync(0xffffffffu, ready)) {
         if (lane == 0) *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      uint32_t r[4][32];
-      const uint32_t taddr = tmem + (uint32_t)(a * kHeadDim) + ((uint32_t)(32 * (warp & 3)) << 16);
-      tmem_ld32(taddr, r[0]);
-      tmem_ld32(taddr + 32, r[1]);
-      tmem_ld32(taddr + 64, r[2]);
-      tmem_ld32(taddr + 96, r[3]);
-      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-      tmem_regs_ready(r[0]);
-      tmem_regs_ready(r[1]);
-      tmem_regs_ready(r[2]);
-      tmem_regs_ready(r[3]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acce[a]));   // the accumulator may be overwritten
       const int64_t pos = tile_start(j) + row;
       const bool valid = pos >= d0 && pos < d1;
-      if (kind == 0)
-        pf_token<0>(p, r, pos, valid, h, b);
-      else
-        pf_token<1>(p, r, pos, valid, h, b);
+      uint32_t acc[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] = 0u;
+      uint32_t sz[kGroups];   // scale (low half) and zero (high half) of each group
+      uint32_t r[32];
+#pragma unroll
+      for (int gq = 0; gq < kGroups; ++gq) {
+        tmem_ld32(taddr + 32 * gq, r);
+        asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+        tmem_regs_ready(r);
+        if (gq == kGroups - 1) {
+          // every column is in registers: the accumulator may be overwritten
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&acce[g]));
+        }
+        trace_group(p, r, pos, valid, h, b, kind, gq);
+        __half s16, z16;
+        if (gq == 0) group_quantise<0>(r, clip, s16, z16, acc);
+        if (gq == 1) group_quantise<1>(r, clip, s16, z16, acc);
+        if (gq == 2) group_quantise<2>(r, clip, s16, z16, acc);
+        if (gq == 3) group_quantise<3>(r, clip, s16, z16, acc);
+        sz[gq] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+      }
+      uint8_t* blk = token_block(p, pos, valid, h, b);
+      if (blk) store_token(blk, kind, pos, acc, sz);
     }
   }
 
@@ -451,18 +445,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
   __syncthreads();
   if (*abort_flag) {
     if (tid == 0) atomicOr(p.err_flags, OSCAR_FLAG_TIMEOUT);
-    if (tid == 256) {
+    if (tid == kProducerTid) {
       // tiles still landing in shared memory
       for (int j = s_mmas; j < s_loads; ++j) mbar_drain(smem_u32(&full[j % kStages]), (uint32_t)((j / kStages) & 1));
     }
-    if (tid == 288 && s_mmas > 0) {
+    if (tid == kMmaTid && s_mmas > 0) {
       // MMAs still writing tensor memory (a commit tracks every earlier MMA)
       const int j = s_mmas - 1;
       mbar_drain(smem_u32(&accf[j % kAccBufs]), (uint32_t)((j / kAccBufs) & 1));
     }
     __syncthreads();
   }
-  if (warp == 9) {
+  if (warp == kMmaTid / 32) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
   }

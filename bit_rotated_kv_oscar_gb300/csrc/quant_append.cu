@@ -1,10 +1,10 @@
 // Write path of the OSCAR INT2 cache: rotate, clip, group-quantise, pack.
 //
-// One CTA of 512 threads handles one new token of one request and one KV head
-// (K and V together). Depending on the token's position it either copies the
-// token into the BF16 sink, quantises it straight into its INT2 page, or
-// places it in the BF16 recent ring after quantising the ring entry it
-// evicts. Sources: "Juntos, AI Open-Sources OSCAR ..." (7minutos.es), section
+// One CTA of 512 threads handles a run of consecutive new tokens of one request
+// and one KV head (K and V together), one token after another. Depending on a
+// token's position it either copies the token into the BF16 sink, quantises it
+// straight into its INT2 page, or places it in the BF16 recent ring after
+// quantising the ring entry it evicts. Sources: "Juntos, AI Open-Sources OSCAR ..." (7minutos.es), section
 // "El sistema de servicio" (write path: rotate, clip to the calibrated
 // threshold, asymmetric per-token INT2 groups; sink and recent tokens in BF16);
 // "OSCAR: Offline Spectral Covariance-Aware Rotation ..." (gist.science, it),
@@ -40,7 +40,7 @@ __device__ __forceinline__ uint8_t* block_of(const AppendParams& p, int32_t id, 
   return p.pool + ((int64_t)id * p.num_kv_heads + h) * kBlockBytes;
 }
 
-constexpr int kTokensPerCta = 16;
+constexpr int kMaxTokensPerCta = 16;
 constexpr int kAppendSmem = 2 * kHeadDim * kHeadDim * 4;  // R_K[h] and R_V[h]
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -52,8 +52,8 @@ oscar_quant_append_kernel(AppendParams p) {
   // token indices of this CTA: all new tokens, or with tail_only only the first
   // `sink` and the last `recent` of them (virtual indices, see AppendParams)
   const int nvirt = p.tail_only ? p.sink + p.recent : p.n_new;
-  const int j0 = blockIdx.x * kTokensPerCta;
-  const int j1 = min(j0 + kTokensPerCta, nvirt);
+  const int j0 = blockIdx.x * p.tokens_per_cta;
+  const int j1 = min(j0 + p.tokens_per_cta, nvirt);
   const int S = p.sink, W = p.recent;
   const int Hkv = p.num_kv_heads;
 
@@ -264,10 +264,24 @@ cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int nvirt = p.tail_only ? p.sink + p.recent : p.n_new;
-  dim3 grid((unsigned)((nvirt + kTokensPerCta - 1) / kTokensPerCta), (unsigned)p.num_kv_heads,
-            (unsigned)p.batch);
-  cudaError_t e = launch_pdl(oscar_quant_append_kernel, grid, dim3(kThreads), kAppendSmem, s, p);
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
+      num_sms = 1;
+  }
+  // tokens are walked one after another inside a CTA: spread them over one wave
+  // of CTAs (one per SM), at most kMaxTokensPerCta each
+  AppendParams q = p;
+  const int64_t nvirt = p.tail_only ? p.sink + p.recent : p.n_new;
+  const int64_t units = (int64_t)p.num_kv_heads * p.batch;
+  int64_t tpc = (nvirt * units + num_sms - 1) / num_sms;
+  if (tpc < 1) tpc = 1;
+  if (tpc > kMaxTokensPerCta) tpc = kMaxTokensPerCta;
+  q.tokens_per_cta = (int32_t)tpc;
+  dim3 grid((unsigned)((nvirt + tpc - 1) / tpc), (unsigned)p.num_kv_heads, (unsigned)p.batch);
+  cudaError_t e = launch_pdl(oscar_quant_append_kernel, grid, dim3(kThreads), kAppendSmem, s, q);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
