@@ -55,13 +55,22 @@ __device__ __forceinline__ uint32_t slot_bits(uint32_t w) {
   }
 }
 
+// d += a b (no side effects: not volatile, so the compiler may interleave
+// independent products with the arithmetic around them)
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// d = a b (a zero accumulator without zeroing registers first)
+__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
@@ -357,11 +366,11 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
     const uint32_t kzA1 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbA + 1216 + zo) : 0u;
     const uint32_t kzB0 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbB + 1152 + zo) : 0u;
     const uint32_t kzB1 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbB + 1216 + zo) : 0u;
-    float c[4][4] = {};
-    mma16816(c[0], zq.x, zq.y, 0u, 0u, kzA0, 0u);
-    mma16816(c[1], zq.x, zq.y, 0u, 0u, kzA1, 0u);
-    mma16816(c[2], zq.x, zq.y, 0u, 0u, kzB0, 0u);
-    mma16816(c[3], zq.x, zq.y, 0u, 0u, kzB1, 0u);
+    float c[4][4];
+    mma16816_z(c[0], zq.x, zq.y, 0u, 0u, kzA0, 0u);
+    mma16816_z(c[1], zq.x, zq.y, 0u, 0u, kzA1, 0u);
+    mma16816_z(c[2], zq.x, zq.y, 0u, 0u, kzB0, 0u);
+    mma16816_z(c[3], zq.x, zq.y, 0u, 0u, kzB1, 0u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       u[2 * i] = c[i][0] + c[i][2];
@@ -370,19 +379,19 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
   }
 #pragma unroll
   for (int gq = 0; gq < 4; ++gq) {
-    float a[4][4] = {};
-#define OSCAR_QK(KB)                                                                 \
-  {                                                                                  \
-    const uint4 q4 = qs[(KB) * 32 + lane];                                           \
-    mma16816(a[0], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwA.x), slot_bits<KB>(kwA.y)); \
-    mma16816(a[1], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwA.z), slot_bits<KB>(kwA.w)); \
-    mma16816(a[2], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwB.x), slot_bits<KB>(kwB.y)); \
-    mma16816(a[3], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwB.z), slot_bits<KB>(kwB.w)); \
+    float a[4][4];
+#define OSCAR_QK(KB, MMA)                                                         \
+  {                                                                               \
+    const uint4 q4 = qs[(KB) * 32 + lane];                                        \
+    MMA(a[0], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwA.x), slot_bits<KB>(kwA.y)); \
+    MMA(a[1], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwA.z), slot_bits<KB>(kwA.w)); \
+    MMA(a[2], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwB.x), slot_bits<KB>(kwB.y)); \
+    MMA(a[3], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwB.z), slot_bits<KB>(kwB.w)); \
   }
-    if (gq == 0) { OSCAR_QK(0) OSCAR_QK(1) }
-    if (gq == 1) { OSCAR_QK(2) OSCAR_QK(3) }
-    if (gq == 2) { OSCAR_QK(4) OSCAR_QK(5) }
-    if (gq == 3) { OSCAR_QK(6) OSCAR_QK(7) }
+    if (gq == 0) { OSCAR_QK(0, mma16816_z) OSCAR_QK(1, mma16816) }
+    if (gq == 1) { OSCAR_QK(2, mma16816_z) OSCAR_QK(3, mma16816) }
+    if (gq == 2) { OSCAR_QK(4, mma16816_z) OSCAR_QK(5, mma16816) }
+    if (gq == 3) { OSCAR_QK(6, mma16816_z) OSCAR_QK(7, mma16816) }
 #undef OSCAR_QK
     // K scales of my tokens for this group: (t0, t0+1) and (t0+8, t0+9)
     const uint2 kA = *reinterpret_cast<const uint2*>(sbA + 1024 + 32 * tig + 8 * gq);
@@ -472,8 +481,11 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   const size_t page_stride = (size_t)p.num_kv_heads * kBlockBytes;
   unsigned valid_bits = 0;  // bit (j & 3): page j of this warp has a valid id
 
+  // page ids of this warp's first 32 pages, one per lane, loaded once (pages
+  // beyond that, possible only with more than 256 pages per split, load on use)
+  const int id_pre = lane < nmine ? ptrow[kWarps * lane] : -1;
   auto issue = [&](int j) {
-    const int id = ptrow[kWarps * j];
+    const int id = j < 32 ? __shfl_sync(0xffffffffu, id_pre, j) : ptrow[kWarps * j];
     const bool good = id >= 0 && id < p.num_pages;
     const unsigned bit = 1u << (j & (kStages - 1));
     valid_bits = good ? (valid_bits | bit) : (valid_bits & ~bit);

@@ -54,7 +54,7 @@ constexpr int kStages = 3;                                // token-tile slots
 constexpr int kAccBufs = 4;                               // 128-column accumulators
 constexpr int kPfSmemImages = 4 * kImageBytes;            // R_K hi, R_K lo, R_V hi, R_V lo
 constexpr int kPfSmemStages = kStages * kImageBytes;
-constexpr int kPfSmemBars = 2 * (kStages + kAccBufs) * 8 + 16;
+constexpr int kPfSmemBars = (2 * (kStages + kAccBufs) + 1) * 8 + 16;
 constexpr int kPfSmem = 1024 + kPfSmemImages + kPfSmemStages + kPfSmemBars;
 constexpr uint32_t kTmemCols = kAccBufs * kHeadDim;       // 512
 constexpr long kSpinLimit = 1L << 20;
@@ -280,7 +280,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
   uint64_t* empty = full + kStages;                        // [kStages] tile consumed (MMA commit)
   uint64_t* accf = empty + kStages;                        // [kAccBufs] accumulator ready (MMA commit)
   uint64_t* acce = accf + kAccBufs;                        // [kAccBufs] accumulator read (4 warps)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + kAccBufs);
+  uint64_t* drainb = acce + kAccBufs;                      // teardown after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drainb + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   __shared__ oscar_seq_state s_st;
   __shared__ int s_loads, s_mmas;                          // jobs issued by the producer / MMA issuer
@@ -317,6 +318,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
       mbar_init(smem_u32(&accf[i]), 1);
       mbar_init(smem_u32(&acce[i]), 4);
     }
+    mbar_init(smem_u32(drainb), 1);
     *abort_flag = 0;
     s_loads = 0;
     s_mmas = 0;
@@ -449,10 +451,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
       // tiles still landing in shared memory
       for (int j = s_mmas; j < s_loads; ++j) mbar_drain(smem_u32(&full[j % kStages]), (uint32_t)((j / kStages) & 1));
     }
-    if (tid == kMmaTid && s_mmas > 0) {
-      // MMAs still writing tensor memory (a commit tracks every earlier MMA)
-      const int j = s_mmas - 1;
-      mbar_drain(smem_u32(&accf[j % kAccBufs]), (uint32_t)((j / kAccBufs) & 1));
+    if (tid == kMmaTid) {
+      // MMAs still writing tensor memory: a commit tracks every MMA issued before it
+      umma_commit(smem_u32(drainb));
+      mbar_drain(smem_u32(drainb), 0u);
     }
     __syncthreads();
   }
