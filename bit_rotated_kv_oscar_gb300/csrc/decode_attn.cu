@@ -36,8 +36,13 @@ namespace oscar {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;
-constexpr int kStageBytes = kWarps * kStages * kBlockBytes;   // 48 KB
+// pages in flight per warp (a power of two): the ring of cp.async page copies
+#ifndef OSCAR_DEC_STAGES
+#define OSCAR_DEC_STAGES 4
+#endif
+constexpr int kStages = OSCAR_DEC_STAGES;
+constexpr int kStageBytes = kWarps * kStages * kBlockBytes;   // 48 KB with 4 stages
+static_assert((kStages & (kStages - 1)) == 0 && kStages >= 2, "page ring depth must be a power of two");
 constexpr int kMaxWindow = 1024;                                // sink + recent limit
 constexpr int kWinChunk = kWindowChunk;                         // window tokens per CTA
 
@@ -200,15 +205,18 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
     }
   }
   __syncthreads();
-  // A fragments of m16n8k16: rows 0-7 = head hi parts, rows 8-15 = lo parts
+  // column fragments of m16n8k16 (k = channel, n = head): per slot kb and lane
+  // (gid, tig) four words, hi parts of head gid at channels 16 kb + 2 tig (+1) and
+  // + 8 (+9), then the lo parts at the same channels, so that each operand pair
+  // is one aligned half of the 16-byte record entry
   uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
 #pragma unroll
   for (int n = 0; n < 4; ++n) {
     const int widx = tid + kRotThreads * n;
     const int r = widx & 3, lane = (widx >> 2) & 31, kb = widx >> 7;
     const int gid = lane >> 2, tig = lane & 3;
-    const int col = kb * 16 + 2 * tig + (r >= 2 ? 8 : 0);
-    const __half* src = hs[r & 1][gid];
+    const int col = kb * 16 + 2 * tig + ((r & 1) ? 8 : 0);
+    const __half* src = hs[r >> 1][gid];
     const uint32_t lo = __half_as_ushort(src[col]);
     const uint32_t hi = __half_as_ushort(src[col + 1]);
     rec[widx] = lo | (hi << 16);
@@ -351,62 +359,79 @@ __device__ __forceinline__ float ex2(float x) {
 // than kLazyLog2 (log2 units), so probabilities relative to it stay <= 2^8.
 constexpr float kLazyLog2 = 8.f;
 
-// scores of two staged pages A, B for my tokens (t0, t0+1, t0+8, t0+9), head gid,
-// in units u: u = sum_gq s_k (q~ . code) + sum_gq z_k sum q~ (scaled by 2^(k-24)).
-// u[0..3] page A, u[4..7] page B. qs: the CTA's q~ fragments in shared memory.
+// Scores of two staged pages A, B with the codes as the row operand: lane (gid,
+// tig) gets tokens gid and gid + 8 of each page for heads 2 tig and 2 tig + 1,
+// u[4 page + 2 (token is gid + 8) + (head is 2 tig + 1)], in units u = sum_gq s_k
+// (q~ . code) + sum_gq z_k sum q~ (scaled by 2^(k-24)). The code fragment of slot
+// KB for tokens (gid, gid + 8) is (kw.x, kw.z, kw.y, kw.w) masked to the slot;
+// q~ hi and lo are two column operands accumulating into the same group result,
+// so hi + lo needs no extra add. zqb: the zero-point column operand (group sums
+// of q~, hi in k rows 0-3, lo in rows 4-7).
 __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* sbB, const uint4* qs,
-                                            uint2 zq, int lane, float (&u)[8]) {
+                                            uint32_t zqb, int lane, float (&u)[8]) {
   const int gid = lane >> 2, tig = lane & 3;
   const uint4 kwA = *reinterpret_cast<const uint4*>(sbA + lane * 16);
   const uint4 kwB = *reinterpret_cast<const uint4*>(sbB + lane * 16);
   {
-    // K zeros of tokens gid and gid + 8, groups (2 tig, 2 tig + 1), as mma B operands
-    const int zo = 8 * gid + 4 * tig;
-    const uint32_t kzA0 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbA + 1152 + zo) : 0u;
-    const uint32_t kzA1 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbA + 1216 + zo) : 0u;
-    const uint32_t kzB0 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbB + 1152 + zo) : 0u;
-    const uint32_t kzB1 = tig < 2 ? *reinterpret_cast<const uint32_t*>(sbB + 1216 + zo) : 0u;
-    float c[4][4];
-    mma16816_z(c[0], zq.x, zq.y, 0u, 0u, kzA0, 0u);
-    mma16816_z(c[1], zq.x, zq.y, 0u, 0u, kzA1, 0u);
-    mma16816_z(c[2], zq.x, zq.y, 0u, 0u, kzB0, 0u);
-    mma16816_z(c[3], zq.x, zq.y, 0u, 0u, kzB1, 0u);
+    // K zeros of tokens gid and gid + 8, groups 2 (tig & 1) and 2 (tig & 1) + 1 (the
+    // lo copy of the group sums sits in k rows 4-7, read by tig 2 and 3)
+    const int zo = 1152 + 8 * gid + 4 * (tig & 1);
+    float zA[4], zB[4];
+    mma16816_z(zA, *reinterpret_cast<const uint32_t*>(sbA + zo), *reinterpret_cast<const uint32_t*>(sbA + zo + 64),
+               0u, 0u, zqb, 0u);
+    mma16816_z(zB, *reinterpret_cast<const uint32_t*>(sbB + zo), *reinterpret_cast<const uint32_t*>(sbB + zo + 64),
+               0u, 0u, zqb, 0u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      u[2 * i] = c[i][0] + c[i][2];
-      u[2 * i + 1] = c[i][1] + c[i][3];
+      u[i] = zA[i];
+      u[4 + i] = zB[i];
     }
   }
+  // K scales of tokens gid (pair 0) and gid + 8 (pair 1): halves at
+  // 1024 + 32 (gid / 2) + 8 gq + 2 (gid % 2) and 4 bytes further
+  const int so = 1024 + 32 * (gid >> 1);
+  const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
 #pragma unroll
   for (int gq = 0; gq < 4; ++gq) {
-    float a[4][4];
-#define OSCAR_QK(KB, MMA)                                                         \
-  {                                                                               \
-    const uint4 q4 = qs[(KB) * 32 + lane];                                        \
-    MMA(a[0], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwA.x), slot_bits<KB>(kwA.y)); \
-    MMA(a[1], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwA.z), slot_bits<KB>(kwA.w)); \
-    MMA(a[2], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwB.x), slot_bits<KB>(kwB.y)); \
-    MMA(a[3], q4.x, q4.y, q4.z, q4.w, slot_bits<KB>(kwB.z), slot_bits<KB>(kwB.w)); \
+    float a[4], c[4];
+#define OSCAR_QK(KB, MMA)                                                                          \
+  {                                                                                                \
+    const uint4 q4 = qs[(KB) * 32 + lane];                                                         \
+    const uint32_t xa = slot_bits<KB>(kwA.x), ya = slot_bits<KB>(kwA.y);                           \
+    const uint32_t za = slot_bits<KB>(kwA.z), wa = slot_bits<KB>(kwA.w);                           \
+    const uint32_t xb = slot_bits<KB>(kwB.x), yb = slot_bits<KB>(kwB.y);                           \
+    const uint32_t zb = slot_bits<KB>(kwB.z), wb = slot_bits<KB>(kwB.w);                           \
+    MMA(a, xa, za, ya, wa, q4.x, q4.y);                                                            \
+    mma16816(a, xa, za, ya, wa, q4.z, q4.w);                                                       \
+    MMA(c, xb, zb, yb, wb, q4.x, q4.y);                                                            \
+    mma16816(c, xb, zb, yb, wb, q4.z, q4.w);                                                       \
   }
     if (gq == 0) { OSCAR_QK(0, mma16816_z) OSCAR_QK(1, mma16816) }
     if (gq == 1) { OSCAR_QK(2, mma16816_z) OSCAR_QK(3, mma16816) }
     if (gq == 2) { OSCAR_QK(4, mma16816_z) OSCAR_QK(5, mma16816) }
     if (gq == 3) { OSCAR_QK(6, mma16816_z) OSCAR_QK(7, mma16816) }
 #undef OSCAR_QK
-    // K scales of my tokens for this group: (t0, t0+1) and (t0+8, t0+9)
-    const uint2 kA = *reinterpret_cast<const uint2*>(sbA + 1024 + 32 * tig + 8 * gq);
-    const uint2 kB = *reinterpret_cast<const uint2*>(sbB + 1024 + 32 * tig + 8 * gq);
-    const float2 sA01 = h2_bits_to_f2(kA.x), sA23 = h2_bits_to_f2(kA.y);
-    const float2 sB01 = h2_bits_to_f2(kB.x), sB23 = h2_bits_to_f2(kB.y);
-    u[0] = fmaf(sA01.x, a[0][0] + a[0][2], u[0]);
-    u[1] = fmaf(sA01.y, a[0][1] + a[0][3], u[1]);
-    u[2] = fmaf(sA23.x, a[1][0] + a[1][2], u[2]);
-    u[3] = fmaf(sA23.y, a[1][1] + a[1][3], u[3]);
-    u[4] = fmaf(sB01.x, a[2][0] + a[2][2], u[4]);
-    u[5] = fmaf(sB01.y, a[2][1] + a[2][3], u[5]);
-    u[6] = fmaf(sB23.x, a[3][0] + a[3][2], u[6]);
-    u[7] = fmaf(sB23.y, a[3][1] + a[3][3], u[7]);
+    const uint2 kA = *reinterpret_cast<const uint2*>(sbA + so + 8 * gq);
+    const uint2 kB = *reinterpret_cast<const uint2*>(sbB + so + 8 * gq);
+    const float2 sA = h2_bits_to_f2(__byte_perm(kA.x, kA.y, sel));   // (token gid, token gid + 8)
+    const float2 sB = h2_bits_to_f2(__byte_perm(kB.x, kB.y, sel));
+    u[0] = fmaf(sA.x, a[0], u[0]);
+    u[1] = fmaf(sA.x, a[1], u[1]);
+    u[2] = fmaf(sA.y, a[2], u[2]);
+    u[3] = fmaf(sA.y, a[3], u[3]);
+    u[4] = fmaf(sB.x, c[0], u[4]);
+    u[5] = fmaf(sB.x, c[1], u[5]);
+    u[6] = fmaf(sB.y, c[2], u[6]);
+    u[7] = fmaf(sB.y, c[3], u[7]);
   }
+}
+
+// transpose an 8 x 8 matrix of 16-bit values held one row pair per lane (lane
+// (gid, tig) holds row gid, columns 2 tig and 2 tig + 1)
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
+  uint32_t d;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
 
 // acc[cb] += codes^T (p * s_v) and oz += z_v^T p for one staged page; P01 / P23
@@ -466,7 +491,16 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   // query operand fragments (see oscar_rotate_q_kernel)
   const uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
   qs[tid] = reinterpret_cast<const uint4*>(rec)[tid];
-  const uint2 zq = reinterpret_cast<const uint2*>(rec + 1024)[lane];
+  // zero-point column operand: k rows 2 tig, 2 tig + 1 of head gid = group sums of
+  // q~ (hi for tig 0 / 1, lo for tig 2 / 3), taken from the record's row layout
+  uint32_t zqb;
+  {
+    const uint2 zq = reinterpret_cast<const uint2*>(rec + 1024)[lane];
+    const int src = (lane & ~3) | (tig & 1);
+    const uint32_t zx = __shfl_sync(0xffffffffu, zq.x, src);
+    const uint32_t zy = __shfl_sync(0xffffffffu, zq.y, src);
+    zqb = tig < 2 ? zx : zy;
+  }
   const float uscale = __uint_as_float(rec[1088]);
   const float tau_u = kLazyLog2 / uscale;
   // probabilities enter the value product as fp16 p * pscale with p <= 2^8 (lazy
@@ -509,13 +543,14 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
   // running (lazy) max in score units u (log2 units = u * uscale), running sum and
   // accumulators in units of pscale
-  float m_run = -INFINITY, l_run = 0.f;
+  // per lane: heads 2 tig (index 0) and 2 tig + 1 (index 1)
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float acc[8][4];
   float oz[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int cb = 0; cb < 8; ++cb) acc[cb][0] = acc[cb][1] = acc[cb][2] = acc[cb][3] = 0.f;
 
-  const int t0 = 2 * tig;  // my tokens: t0, t0+1, t0+8, t0+9
+  const int t0 = 2 * tig;  // tokens of my probability operand: t0, t0+1, t0+8, t0+9
 
   // pages are consumed two at a time (one softmax update per pair)
   for (int j = 0; j < nmine; j += 2) {
@@ -531,9 +566,23 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     const bool full = okA && okB && posA >= lo && posA + kPage <= hi && posB >= lo && posB + kPage <= hi;
 
     float u[8];
-    pair_scores(sbA, sbB, qs, zq, lane, u);
+    pair_scores(sbA, sbB, qs, zqb, lane, u);
     uint32_t mA01 = 0xffffffffu, mA23 = 0xffffffffu, mB01 = 0xffffffffu, mB23 = 0xffffffffu;
     if (!full) {
+      // scores: tokens gid, gid + 8 of each page
+      const bool sA0 = okA && posA + gid >= lo && posA + gid < hi;
+      const bool sA1 = okA && posA + gid + 8 >= lo && posA + gid + 8 < hi;
+      const bool sB0 = okB && posB + gid >= lo && posB + gid < hi;
+      const bool sB1 = okB && posB + gid + 8 >= lo && posB + gid + 8 < hi;
+      u[0] = sA0 ? u[0] : -INFINITY;
+      u[1] = sA0 ? u[1] : -INFINITY;
+      u[2] = sA1 ? u[2] : -INFINITY;
+      u[3] = sA1 ? u[3] : -INFINITY;
+      u[4] = sB0 ? u[4] : -INFINITY;
+      u[5] = sB0 ? u[5] : -INFINITY;
+      u[6] = sB1 ? u[6] : -INFINITY;
+      u[7] = sB1 ? u[7] : -INFINITY;
+      // value metadata of tokens t0, t0+1, t0+8, t0+9 (stale bytes in masked slots)
       bool v[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -541,47 +590,53 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
         v[i] = okA && posA + off >= lo && posA + off < hi;
         v[4 + i] = okB && posB + off >= lo && posB + off < hi;
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) u[i] = v[i] ? u[i] : -INFINITY;
       mA01 = (v[0] ? 0x0000ffffu : 0u) | (v[1] ? 0xffff0000u : 0u);
       mA23 = (v[2] ? 0x0000ffffu : 0u) | (v[3] ? 0xffff0000u : 0u);
       mB01 = (v[4] ? 0x0000ffffu : 0u) | (v[5] ? 0xffff0000u : 0u);
       mB23 = (v[6] ? 0x0000ffffu : 0u) | (v[7] ? 0xffff0000u : 0u);
     }
 
-    // ---- online softmax over the pair, per head gid (lazy maximum) -------------
-    float mx = fmaxf(fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3])), fmaxf(fmaxf(u[4], u[5]), fmaxf(u[6], u[7])));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    // (mx and m_run are both -inf only while nothing valid was seen: warp-uniform)
-    if (!(mx == -INFINITY && m_run == -INFINITY)) {
-    const bool bump = mx > m_run + tau_u;
-    if (__any_sync(0xffffffffu, bump)) {
-      const float m_new = bump ? mx : m_run;
-      const float alpha = bump ? ex2((m_run - m_new) * uscale) : 1.f;
-      m_run = m_new;
-      l_run *= alpha;
-      const float ae = __shfl_sync(0xffffffffu, alpha, 8 * tig);
-      const float ao = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+    // ---- online softmax over the pair, per head (lazy maximum) ------------------
+    float mx0 = fmaxf(fmaxf(u[0], u[2]), fmaxf(u[4], u[6]));
+    float mx1 = fmaxf(fmaxf(u[1], u[3]), fmaxf(u[5], u[7]));
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    // (every head sees the same tokens, so "nothing valid seen yet" is warp-uniform)
+    if (!(mx0 == -INFINITY && m0 == -INFINITY)) {
+    const bool bump0 = mx0 > m0 + tau_u, bump1 = mx1 > m1 + tau_u;
+    if (__any_sync(0xffffffffu, bump0 || bump1)) {
+      const float a0 = bump0 ? ex2((m0 - mx0) * uscale) : 1.f;
+      const float a1 = bump1 ? ex2((m1 - mx1) * uscale) : 1.f;
+      m0 = bump0 ? mx0 : m0;
+      m1 = bump1 ? mx1 : m1;
+      l0 *= a0;
+      l1 *= a1;
 #pragma unroll
       for (int cb = 0; cb < 8; ++cb) {
-        acc[cb][0] *= ae;
-        acc[cb][1] *= ao;
-        acc[cb][2] *= ae;
-        acc[cb][3] *= ao;
+        acc[cb][0] *= a0;
+        acc[cb][1] *= a1;
+        acc[cb][2] *= a0;
+        acc[cb][3] *= a1;
       }
-      oz[0] *= ae;
-      oz[1] *= ao;
-      oz[2] *= ae;
-      oz[3] *= ao;
+      oz[0] *= a0;
+      oz[1] *= a1;
+      oz[2] *= a0;
+      oz[3] *= a1;
     }
-    const float nb = fmaf(-m_run, uscale, lg_ps);
+    const float nb0 = fmaf(-m0, uscale, lg_ps), nb1 = fmaf(-m1, uscale, lg_ps);
     float pr[8];  // p * pscale, p <= 2^8
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], uscale, nb));
-    l_run += ((pr[0] + pr[1]) + (pr[2] + pr[3])) + ((pr[4] + pr[5]) + (pr[6] + pr[7]));
-    const uint32_t PA01 = f2_to_h2_bits(pr[0], pr[1]), PA23 = f2_to_h2_bits(pr[2], pr[3]);
-    const uint32_t PB01 = f2_to_h2_bits(pr[4], pr[5]), PB23 = f2_to_h2_bits(pr[6], pr[7]);
+    for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], uscale, (i & 1) ? nb1 : nb0));
+    l0 += (pr[0] + pr[2]) + (pr[4] + pr[6]);
+    l1 += (pr[1] + pr[3]) + (pr[5] + pr[7]);
+    // token-major probabilities -> the (token, head) column operand of P.V
+    const uint32_t PA01 = transpose8x8(f2_to_h2_bits(pr[0], pr[1]));
+    const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
+    const uint32_t PB01 = transpose8x8(f2_to_h2_bits(pr[4], pr[5]));
+    const uint32_t PB23 = transpose8x8(f2_to_h2_bits(pr[6], pr[7]));
     if (full) {
       page_values<false>(sbA, lane, PA01, PA23, 0u, 0u, acc, oz);
       page_values<false>(sbB, lane, PB01, PB23, 0u, 0u, acc, oz);
@@ -599,15 +654,20 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   cp_wait<0>();
 
   // ---- per-warp partial -> shared memory, then CTA merge --------------------
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
   const float inv_ps = 1.f / pscale;
   __syncthreads();  // staging buffers are reused below
   float* wpart = reinterpret_cast<float*>(smem);              // [8 warps][8 heads][128]
   float* wml = wpart + kWarps * kMaxGqa * kHeadDim;           // [8 warps][8 heads][2]
-  if (tig == 0) {
-    wml[(warp * kMaxGqa + gid) * 2] = m_run * uscale;           // log2 units
-    wml[(warp * kMaxGqa + gid) * 2 + 1] = l_run * inv_ps;
+  if (gid == 0) {
+    wml[(warp * kMaxGqa + 2 * tig) * 2] = m0 * uscale;          // log2 units
+    wml[(warp * kMaxGqa + 2 * tig) * 2 + 1] = l0 * inv_ps;
+    wml[(warp * kMaxGqa + 2 * tig + 1) * 2] = m1 * uscale;
+    wml[(warp * kMaxGqa + 2 * tig + 1) * 2 + 1] = l1 * inv_ps;
   }
 #pragma unroll
   for (int cb = 0; cb < 8; ++cb) {

@@ -25,8 +25,8 @@ constexpr int kGroups = kHeadDim / kGroup;   // 4 quantisation groups per token
 constexpr int kBlockBytes = OSCAR_PAGE_BLOCK_BYTES;
 constexpr int kMaxGqa = 8;
 // per-(request, KV head) record written by the query-rotation kernel:
-// [0, 1024) fp16x2 mma A fragments of q~ (hi/lo), [1024, 1088) A fragments of the
-// per-group sums of q~ (hi/lo), [1088] the score scale, rest zero
+// [0, 1024) fp16x2 mma column fragments of q~ (hi, lo), [1024, 1088) fragments of
+// the per-group sums of q~ (hi/lo), [1088] the score scale, rest zero
 constexpr int kQrecWords = 1104;
 constexpr int kPartFloats = kHeadDim + 4;    // o[128], m, l, 2 pad (rows stay 16-byte aligned)
 constexpr int kWindowChunk = 64;             // BF16 window tokens per decode CTA
