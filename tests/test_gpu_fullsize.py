@@ -1,0 +1,246 @@
+"""Full-size parity: every workload at its own sizes, driven the way the
+benchmark drives it (16384-token population chunks, one 131072-token append,
+the full decode batch with the automatic split count), and checked on samples
+the oracle computes one by one:
+  * the codes, scales and zeros of sampled pages bit-exact against the oracle
+    quantising the GPU's rotated values, and those rotated values within 1e-5
+    of the float64 rotation;
+  * decode outputs of sampled (request, KV head) pairs within rel-L2 2e-3 and
+    max-abs 1e-2 of the float64 oracle over the oracle's own cache of that
+    head, with rounding ties of its float64 rotation resolved to the GPU's
+    (valid) choice.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_rotated_kv_oscar_gb300 import abi, build
+from synth import WORKLOADS, draw_kv, draw_queries, draw_ragged_lengths
+from tests.gpu_harness import D, MAX_ABS, REL_L2, ROT_REL, Layer, rel_l2, resolve_group_ties
+from tests.test_gpu_parity import check_int2, check_window
+
+pytestmark = pytest.mark.gpu
+
+CHUNK = 16384   # population chunk of the benchmark
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "the gpu-marked tests need a CUDA device"
+    build.build()
+    abi.lib()
+
+
+def spec_layer(spec, max_batch, max_tokens):
+    return Layer(spec.num_q_heads, spec.num_kv_heads, spec.sink, spec.recent, max_batch, max_tokens,
+                 seed=spec.seed, n_cal=spec.calib_tokens, shuffled=spec.shuffled_pages,
+                 spikes=spec.token_spikes)
+
+
+def populate(layer, b, n, stream0, trace=None, chunk=CHUNK):
+    """Append n fresh tokens to request b in chunks of `chunk`."""
+    pos = 0
+    while pos < n:
+        m = min(chunk, n - pos)
+        k, v = draw_kv(layer.seed, stream0 + pos // chunk, m, layer.hkv, D, layer.spikes)
+        layer.append(b, k, v, trace)
+        pos += m
+
+
+def sample_pages(rng, layer, b, count):
+    """Page-aligned position ranges inside request b's INT2 region."""
+    S, E = layer.sink, min(layer.e[b], layer.len[b])
+    first, last = S // 16, (E - 1) // 16
+    pages = rng.choice(np.arange(first, last + 1), size=min(count, last - first + 1), replace=False)
+    return [(max(16 * int(p), S), min(16 * int(p) + 16, E)) for p in sorted(pages)]
+
+
+def check_sampled_int2(layer, b, trace, rng, count=8):
+    for lo, hi in sample_pages(rng, layer, b, count):
+        check_int2(layer, b, trace, lo, hi)
+
+
+def oracle_head(layer, b, h):
+    """The oracle's cache of KV head h of request b, its float64-rotation ties
+    resolved to the GPU's choice after checking the choice is a valid one."""
+    cal, S = layer.cal, layer.sink
+    L, E = layer.len[b], layer.e[b]
+    cache = oracle.OracleCache(cal["R_K32"][h:h + 1], layer.r_v32[h:h + 1], cal["clip_K32"][h:h + 1],
+                               cal["clip_V32"][h:h + 1], S)
+    cache.build(layer.k_host[b][:, h:h + 1], layer.v_host[b][:, h:h + 1], L, E)
+    hi = min(E, L)
+    if hi <= S:
+        return cache
+    pt = layer.cache.page_table_host[b]
+    n0, n1 = S // 16, (hi - 1) // 16 + 1
+    blocks = layer.blocks_of_pages(pt[n0:n1])[:, h:h + 1]
+    dec = []
+    for x in oracle.decode_page_block(blocks):
+        x = np.moveaxis(x, 2, 1)
+        x = x.reshape((-1,) + x.shape[2:])
+        dec.append(x[S - n0 * 16:hi - n0 * 16])
+    for kind in range(2):
+        x = (cache.k if kind == 0 else cache.v)[S:hi]
+        r = cache.r_k if kind == 0 else cache.r_v
+        clip = (cache.clip_k if kind == 0 else cache.clip_v).reshape(1, -1, 1).astype(np.float64)
+        x64 = (x[:, 0] @ r[0])[:, None]
+        eps = ROT_REL * np.abs(x64).max(-1, keepdims=True)
+        codes, s16, z16 = resolve_group_ties(x64, clip, eps, dec[kind], dec[2 + 2 * kind], dec[3 + 2 * kind])
+        if kind == 0:
+            cache.k_codes, cache.k_scale, cache.k_zero = codes, s16, z16
+        else:
+            cache.v_codes, cache.v_scale, cache.v_zero = codes, s16, z16
+    return cache
+
+
+def decode_rows(layer, q, row0):
+    """decode_attn for requests row0 .. row0 + len(q) - 1 (q float32 [B, hq, D])."""
+    bsz = q.shape[0]
+    qd = q.to(torch.bfloat16).to(layer.device).contiguous()
+    o = torch.full((bsz, layer.hq, D), float("nan"), device=layer.device)
+    layer.ctx.decode_attn(qd, layer.cache.page_table[row0:], layer.cache.state[row0:], o, bsz)
+    torch.cuda.synchronize()
+    return o.cpu().numpy()
+
+
+def check_sampled_decode(layer, q, o, pairs, row0=0, caches=None):
+    g = layer.hq // layer.hkv
+    worst = (0.0, 0.0)
+    for i, h in pairs:
+        b = row0 + i
+        cache = caches[h] if caches is not None else oracle_head(layer, b, h)
+        ref = oracle.decode_attention(q[i, h * g:(h + 1) * g].numpy().astype(np.float64), cache)
+        got = o[i, h * g:(h + 1) * g]
+        assert np.isfinite(got).all()
+        r, m = rel_l2(got, ref), float(np.abs(got - ref).max())
+        worst = (max(worst[0], r), max(worst[1], m))
+        assert r <= REL_L2 and m <= MAX_ABS, (b, h, r, m)
+    return worst
+
+
+def clone_request(layer, src, dst):
+    """Request dst gets a copy of request src's pages, window rows and state
+    (distinct pages, same contents), as the benchmark fills its batch."""
+    L, E, S, W, hkv = layer.len[src], layer.e[src], layer.sink, layer.recent, layer.hkv
+    layer.cache.reserve(dst, L)
+    pool = layer.cache.pool.view(-1, hkv, abi.PAGE_BLOCK_BYTES)
+    npg = (L + 15) // 16
+    src_ids = torch.as_tensor(layer.cache.page_table_host[src, :npg].astype(np.int64), device=pool.device)
+    dst_ids = torch.as_tensor(layer.cache.page_table_host[dst, :npg].astype(np.int64), device=pool.device)
+    pool[dst_ids] = pool[src_ids]
+    win = layer.cache.window.view(layer.cfg.max_batch, hkv, 2, S + W, D)
+    win[dst].copy_(win[src])
+    layer.cache.state[dst] = torch.tensor([L, E, dst, 0], dtype=torch.int32, device=pool.device)
+    layer.k_host[dst], layer.v_host[dst] = layer.k_host[src], layer.v_host[src]
+    layer.len[dst], layer.e[dst] = L, E
+    torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# Qwen3-8B layer, batch 1 x 32768 tokens, then decode steps with appends
+# ---------------------------------------------------------------------------
+
+def test_fullsize_qwen3_8b_bs1_32k():
+    spec = WORKLOADS["qwen3_8b_bs1_32k"]
+    n, steps = spec.context, 3
+    layer = spec_layer(spec, 1, n + steps + 16)
+    trace = layer.new_trace(n + steps)
+    populate(layer, 0, n, 10_000, trace)
+    rng = np.random.default_rng(1)
+    check_sampled_int2(layer, 0, trace, rng)
+    check_window(layer, 0)
+    for step in range(steps):
+        k, v = draw_kv(layer.seed, 100 + step, 1, layer.hkv, D, layer.spikes)
+        layer.append(0, k.view(1, layer.hkv, D), v.view(1, layer.hkv, D), trace)
+        q = draw_queries(layer.seed, 100 + step, 1, layer.hq, layer.hkv, D)
+        o = decode_rows(layer, q, 0)
+        check_sampled_decode(layer, q, o, [(0, h) for h in range(layer.hkv)])
+    check_int2(layer, 0, trace, layer.e[0] - 16, layer.e[0])
+    assert layer.ctx.error_flags() == 0
+
+
+# ---------------------------------------------------------------------------
+# Qwen3-8B layer, batch 16 with ragged lengths in 8k-32k and token spikes
+# ---------------------------------------------------------------------------
+
+def test_fullsize_qwen3_8b_bs16_ragged():
+    spec = WORKLOADS["qwen3_8b_bs16_ragged"]
+    lengths = draw_ragged_lengths(spec.seed, spec.batch, spec.context_min, spec.context)
+    layer = spec_layer(spec, spec.batch, int(lengths.max()) + 16)
+    trace = layer.new_trace(int(lengths.max()))
+    rng = np.random.default_rng(2)
+    for b in range(spec.batch):
+        trace.fill_(float("nan"))
+        populate(layer, b, int(lengths[b]), 20_000 + 100 * b, trace)
+        if b in (0, 7, 15):
+            check_sampled_int2(layer, b, trace, rng, count=4)
+            check_window(layer, b)
+    q = draw_queries(layer.seed, 3, spec.batch, layer.hq, layer.hkv, D)
+    o = decode_rows(layer, q, 0)
+    assert np.isfinite(o).all()
+    check_sampled_decode(layer, q, o, [(0, 0), (3, 7), (7, 3), (11, 5), (15, 1)])
+    assert layer.ctx.error_flags() == 0
+
+
+# ---------------------------------------------------------------------------
+# Qwen3-32B layer, batch 28 x 100000 tokens (copies of one populated request)
+# ---------------------------------------------------------------------------
+
+def test_fullsize_qwen3_32b_bs28_100k():
+    spec = WORKLOADS["qwen3_32b_bs28_100k"]
+    n, B = spec.context, spec.batch
+    layer = spec_layer(spec, B, n + 16)
+    trace = layer.new_trace(n)
+    populate(layer, 0, n, 10_000, trace)
+    rng = np.random.default_rng(3)
+    check_sampled_int2(layer, 0, trace, rng)
+    del trace
+    for b in range(1, B):
+        clone_request(layer, 0, b)
+    q = draw_queries(layer.seed, 3, B, layer.hq, layer.hkv, D)
+    o = decode_rows(layer, q, 0)
+    assert np.isfinite(o).all()
+    heads = (0, 5)
+    caches = {h: oracle_head(layer, 0, h) for h in heads}
+    check_sampled_decode(layer, q, o, [(b, h) for b in (0, 13, 27) for h in heads], caches=caches)
+    assert layer.ctx.error_flags() == 0
+
+
+# ---------------------------------------------------------------------------
+# 131072-token prefill, 16 forks at 65536 tokens with 4096-token suffixes
+# ---------------------------------------------------------------------------
+
+def test_fullsize_prefill_128k_prefix16():
+    spec = WORKLOADS["prefill_128k_prefix16"]
+    n, fork, suf, nreq = spec.context, spec.prefix_shared, spec.suffix, spec.batch
+    layer = spec_layer(spec, nreq + 1, n + 16)
+    trace = layer.new_trace(n)
+    k, v = draw_kv(layer.seed, 1, n, layer.hkv, D, layer.spikes)
+    layer.append(0, k, v, trace)                 # one long append: the tensor-core path
+    rng = np.random.default_rng(4)
+    check_sampled_int2(layer, 0, trace, rng, count=12)
+    check_window(layer, 0)
+    del trace
+    for r in range(1, nreq + 1):
+        layer.cache.fork(0, r, fork)
+        layer.cache.reserve(r, fork + suf, upload=False)
+    layer.cache.upload()
+    ks, vs = draw_kv(layer.seed, 2, nreq * suf, layer.hkv, D, layer.spikes)
+    ks, vs = ks.view(nreq, suf, layer.hkv, D), vs.view(nreq, suf, layer.hkv, D)
+    layer.ctx.quant_append(layer.cache.page_table[1:], layer.cache.state[1:],
+                           ks.to(torch.bfloat16).to(layer.device).contiguous(),
+                           vs.to(torch.bfloat16).to(layer.device).contiguous(), nreq, suf)
+    for r in range(1, nreq + 1):
+        layer.k_host[r] = np.concatenate([layer.k_host[0][:fork], ks[r - 1].numpy()])
+        layer.v_host[r] = np.concatenate([layer.v_host[0][:fork], vs[r - 1].numpy()])
+        layer.len[r], layer.e[r] = oracle.next_state(fork, fork, suf, layer.recent, layer.sink)
+    assert tuple(layer.device_state()[1][:2]) == (layer.len[1], layer.e[1])
+    check_window(layer, 1)
+    check_window(layer, nreq)
+    q = draw_queries(layer.seed, 3, nreq, layer.hq, layer.hkv, D)
+    o = decode_rows(layer, q, 1)
+    assert np.isfinite(o).all()
+    check_sampled_decode(layer, q, o, [(0, 0), (5, 6), (15, 3)], row0=1)
+    assert layer.ctx.error_flags() == 0
