@@ -114,6 +114,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings, returned on every rank (the
+    replicas run concurrently, so the job takes as long as its slowest rank)."""
+    if not dist:
+        return [float(v) for v in values]
+    dev = device if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def source_hash():
     h = hashlib.sha256()
     for name in ("decode_attn.cu", "oscar_internal.cuh"):
@@ -322,10 +333,7 @@ def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True
     app_ms = max(total_ms / args.steps - dec_ms, 0.0)
     warm_done = i
     i += args.steps
-    if dist:
-        t = torch.tensor([total_ms, app_ms, dec_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, app_ms, dec_ms = (float(x) for x in t.tolist())
+    total_ms, app_ms, dec_ms = max_over_ranks([total_ms, app_ms, dec_ms], dist, device)
     us_step = total_ms * 1000.0 / args.steps
     mid = warm_done + args.steps // 2
     dbytes = wl.decode_bytes(mid // len(wl.layers))
@@ -377,10 +385,7 @@ def run_e2e(wl, args, device, i0, dist):
     end.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks([ms], dist, device)[0]
     return {"value": ms * 1000.0 / args.steps, "unit": "us/step", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
 
@@ -460,10 +465,7 @@ def run_prefill(args, device, rank, dist):
     E = L - W
     logical = float(nreq * (hkv * (96 * (E - S) + 512 * (S + W)) + 4 * ((E + 15) // 16)) + nreq * hq * D * 6)
     unique = float(hkv * 96 * (fork - S) + nreq * hkv * (96 * (E - fork) + 512 * (S + W)) + nreq * hq * D * 6)
-    if dist:
-        t = torch.tensor([pre_us, dec_us], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        pre_us, dec_us = (float(x) for x in t.tolist())
+    pre_us, dec_us = max_over_ranks([pre_us, dec_us], dist, device)
     return {"prefill_tokens": n, "prefill_us": pre_us, "prefill_bytes": pre_bytes,
             "prefix_decode_us": dec_us, "prefix_logical_bytes": logical, "prefix_unique_bytes": unique}
 
