@@ -125,22 +125,26 @@ def max_over_ranks(values, dist, device):
     return [float(x) for x in t.tolist()]
 
 
-def source_hash():
+KERNEL_SOURCES = {"decode": ("decode_attn.cu", "oscar_internal.cuh"),
+                  "prefill": ("prefill_append.cu", "oscar_internal.cuh")}
+
+
+def source_hash(kind="decode"):
     h = hashlib.sha256()
-    for name in ("decode_attn.cu", "oscar_internal.cuh"):
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "bit_rotated_kv_oscar_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per decode launch from a committed ncu summary, if it was taken
-    on the current decode kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+def profiled_traffic(workload, kind="decode"):
+    """DRAM bytes per launch of the kernel from a committed ncu summary, if it was
+    taken on the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "%s_traffic.json" % kind)
     try:
         with open(path) as f:
             t = json.load(f)
-        if t.get("source_hash") != source_hash():
+        if t.get("source_hash") != source_hash(kind):
             return None
         return t.get("bytes_per_launch", {}).get(workload)
     except Exception:
@@ -263,6 +267,13 @@ class Workload:
         j = i % self.n_inputs
         ctx.decode_attn(self.q[j], cache.page_table, cache.state, self.o, self.B, stream)
 
+    def decode_timed(self, i, stream, ev_before, ev_after):
+        """decode_attn with the split-K attention kernel bracketed by two events."""
+        ctx, cache = self.layers[i % len(self.layers)]
+        j = i % self.n_inputs
+        ctx.decode_attn_timed(self.q[j], cache.page_table, cache.state, self.o, self.B, ev_before, ev_after,
+                              stream)
+
     def step(self, i, stream, ev=None):
         ctx, cache = self.layers[i % len(self.layers)]
         j = i % self.n_inputs
@@ -333,12 +344,21 @@ def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True
     app_ms = max(total_ms / args.steps - dec_ms, 0.0)
     warm_done = i
     i += args.steps
-    total_ms, app_ms, dec_ms = max_over_ranks([total_ms, app_ms, dec_ms], dist, device)
+    # the split-K attention kernel alone: eager decode calls, each bracketing that
+    # launch with its own event pair (layers cycled as in the timed graphs)
+    n_k = min(args.steps, 64)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
+    for k in range(n_k):
+        wl.decode_timed(i + k, stream, *kev[k])
+    torch.cuda.synchronize()
+    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / n_k
+    total_ms, app_ms, dec_ms, kern_ms = max_over_ranks([total_ms, app_ms, dec_ms, kern_ms], dist, device)
     us_step = total_ms * 1000.0 / args.steps
     mid = warm_done + args.steps // 2
     dbytes = wl.decode_bytes(mid // len(wl.layers))
     res = {
-        "workload": name, "us_per_step": us_step, "decode_us": dec_ms * 1000.0,
+        "workload": name, "us_per_step": us_step, "decode_us": dec_ms * 1000.0, "kernel_us": kern_ms * 1000.0,
+        "kernel_bytes": dbytes - wl.B * wl.spec.num_q_heads * D * 6,
         "append_us": app_ms * 1000.0, "decode_bytes": dbytes, "append_bytes": wl.append_bytes(),
         "layers_cycled": len(wl.layers), "per_layer_bytes": wl.per_layer_bytes, "clocks": clocks,
         "batch": wl.B, "lengths": [int(x) for x in wl.lengths[:4]],
@@ -417,20 +437,28 @@ def run_prefill(args, device, rank, dist):
             for t in draw_kv(seed, 1, n, hkv, D, device=device))
     stream = torch.cuda.current_stream(device)
     fresh = torch.tensor([0, S, 0, 0], dtype=torch.int32, device=device)
-    times = []
-    for it in range(max(3, args.warmup) + args.steps):
+    times, ktimes = [], []
+    for it in range(max(3, args.warmup) + 2 * args.steps):
         cache.state[0].copy_(fresh)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         # keep the device busy while the host encodes and launches, so the events
         # bracket device time only
         torch.cuda._sleep(200000)
-        e0.record(stream)
-        ctx.quant_append(cache.page_table, cache.state, k, v, 1, n, stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if it >= max(3, args.warmup):
-            times.append(e0.elapsed_time(e1))
+        if it < max(3, args.warmup) + args.steps:
+            # the whole call (tensor-core kernel + per-token tail kernel)
+            e0.record(stream)
+            ctx.quant_append(cache.page_table, cache.state, k, v, 1, n, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if it >= max(3, args.warmup):
+                times.append(e0.elapsed_time(e1))
+        else:
+            # the tensor-core kernel alone
+            ctx.quant_append_timed(cache.page_table, cache.state, k, v, 1, n, e0, e1, stream)
+            torch.cuda.synchronize()
+            ktimes.append(e0.elapsed_time(e1))
     pre_us = float(np.mean(times)) * 1000.0
+    pre_kernel_us = float(np.mean(ktimes)) * 1000.0
     n_int2 = max(n - W, S) - S
     pre_bytes = float(n * hkv * 2 * D * 2 + n_int2 * hkv * 96 + (S + W) * hkv * 2 * D * 2)
     # 16 forks at 65536 tokens with private suffixes
@@ -465,8 +493,12 @@ def run_prefill(args, device, rank, dist):
     E = L - W
     logical = float(nreq * (hkv * (96 * (E - S) + 512 * (S + W)) + 4 * ((E + 15) // 16)) + nreq * hq * D * 6)
     unique = float(hkv * 96 * (fork - S) + nreq * hkv * (96 * (E - fork) + 512 * (S + W)) + nreq * hq * D * 6)
-    pre_us, dec_us = max_over_ranks([pre_us, dec_us], dist, device)
+    pre_us, pre_kernel_us, dec_us = max_over_ranks([pre_us, pre_kernel_us, dec_us], dist, device)
+    # the tensor-core kernel's share of the bytes: the K / V of the tokens going
+    # straight to INT2 and their codes + metadata
+    pre_kernel_bytes = float(n_int2 * hkv * (2 * D * 2 + 96))
     return {"prefill_tokens": n, "prefill_us": pre_us, "prefill_bytes": pre_bytes,
+            "prefill_kernel_us": pre_kernel_us, "prefill_kernel_bytes": pre_kernel_bytes,
             "prefix_decode_us": dec_us, "prefix_logical_bytes": logical, "prefix_unique_bytes": unique}
 
 
@@ -607,12 +639,15 @@ def main():
                          (WORKLOADS[args.workload].num_kv_heads, WORKLOADS[args.workload].batch)}
 
     def roof(r):
-        achieved = r["decode_bytes"] / (r["decode_us"] * 1e-6) / 1e9
+        # the dominant kernel: split-K attention over the paged cache; algorithmic
+        # bytes = INT2 codes + metadata (96 B per token and KV head), the BF16 window
+        # (512 B per token and KV head) and the page table (4 B per page)
+        achieved = r["kernel_bytes"] / (r["kernel_us"] * 1e-6) / 1e9
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic(r["workload"]),
                 "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                "kernel": "decode_attn call (rotate_q + decode + merge launches)",
-                "algorithmic_bytes_per_launch": r["decode_bytes"]}
+                "kernel": "oscar_decode_kernel", "launch_us": round(r["kernel_us"], 3),
+                "algorithmic_bytes_per_launch": r["kernel_bytes"]}
 
     if rank == 0:
         spec = WORKLOADS[args.workload]
@@ -644,13 +679,17 @@ def main():
             })
         if pre is not None:
             ach = pre["prefill_bytes"] / (pre["prefill_us"] * 1e-6) / 1e9
+            kach = pre["prefill_kernel_bytes"] / (pre["prefill_kernel_us"] * 1e-6) / 1e9
             out["prefill"] = {
                 "workload": "prefill_128k_prefix16", "tokens": pre["prefill_tokens"],
                 "quant_append_us": round(pre["prefill_us"], 2),
-                "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                             "frac": round(ach / peak, 4), "traffic": None,
-                             "kernel": "quant_append call (tensor-core prefill + tail launches)",
-                             "algorithmic_bytes_per_launch": pre["prefill_bytes"]},
+                "quant_append_gbs": round(ach, 1), "quant_append_frac": round(ach / peak, 4),
+                "roofline": {"bound": "hbm", "achieved": round(kach, 1), "peak": peak, "unit": "GB/s",
+                             "frac": round(kach / peak, 4),
+                             "traffic": profiled_traffic("prefill_128k_prefix16", "prefill"),
+                             "kernel": "oscar_prefill_append_kernel",
+                             "launch_us": round(pre["prefill_kernel_us"], 2),
+                             "algorithmic_bytes_per_launch": pre["prefill_kernel_bytes"]},
                 "prefix16_decode_us": round(pre["prefix_decode_us"], 2),
                 "prefix16_logical_gbs": round(pre["prefix_logical_bytes"] / (pre["prefix_decode_us"] * 1e-6) / 1e9, 1),
                 "prefix16_unique_bytes": pre["prefix_unique_bytes"],

@@ -72,6 +72,9 @@ _SIGS = {
     "oscar_quant_append_traced": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32,
                                                  _P, ctypes.c_int32, _P]),
     "oscar_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P]),
+    "oscar_decode_attn_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P]),
+    "oscar_quant_append_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32, _P,
+                                                _P, _P]),
     "oscar_decode_splits": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "oscar_error_flags": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32]),
     "oscar_last_error": (ctypes.c_char_p, [_P]),
@@ -138,6 +141,15 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _event(ev):
+    """Raw cudaEvent_t of a torch.cuda.Event (recorded once so that it exists)."""
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        ev.record()
+    return ctypes.c_void_p(ev.cuda_event)
+
+
 def _stream(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -196,6 +208,20 @@ class Context:
         _check(lib().oscar_quant_append_traced(self.handle, _ptr(page_table), _ptr(state), _ptr(k),
                                                _ptr(v), batch, n_new, _ptr(trace), trace_positions,
                                                _stream(stream)), self.handle)
+
+    def decode_attn_timed(self, q, page_table, state, o, batch, ev_before, ev_after, stream=None):
+        """decode_attn that records torch.cuda.Event ev_before / ev_after around its
+        split-K attention kernel (for measurement)."""
+        _check(lib().oscar_decode_attn_timed(self.handle, _ptr(q), _ptr(page_table), _ptr(state), _ptr(o),
+                                             batch, _stream(stream), _event(ev_before), _event(ev_after)),
+               self.handle)
+
+    def quant_append_timed(self, page_table, state, k, v, batch, n_new, ev_before, ev_after, stream=None):
+        """quant_append that records torch.cuda.Event ev_before / ev_after around its
+        main kernel (the tensor-core kernel of a long append)."""
+        _check(lib().oscar_quant_append_timed(self.handle, _ptr(page_table), _ptr(state), _ptr(k), _ptr(v),
+                                              batch, n_new, _stream(stream), _event(ev_before),
+                                              _event(ev_after)), self.handle)
 
     def decode_attn(self, q, page_table, state, o, batch, stream=None):
         _check(lib().oscar_decode_attn(self.handle, _ptr(q), _ptr(page_table), _ptr(state), _ptr(o),

@@ -823,7 +823,8 @@ int decode_smem_bytes() {
   return m;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cudaEvent_t ev_before,
+                          cudaEvent_t ev_after) {
   static bool attr_set = false;
   const int smem = decode_smem_bytes();
   if (!attr_set) {
@@ -838,9 +839,11 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s) {
   if (p.win_slots + p.splits > kMaxSlots) return cudaErrorInvalidValue;
   cudaError_t e = launch_pdl(oscar_rotate_q_kernel, dim3(p.num_kv_heads, batch), dim3(kRotThreads), kRotSmem,
                              s, p);
+  if (e == cudaSuccess && ev_before) e = cudaEventRecord(ev_before, s);
   if (e == cudaSuccess)
     e = launch_pdl(oscar_decode_kernel, dim3(p.win_slots + p.splits, p.num_kv_heads, batch), dim3(kThreads),
                    smem, s, p);
+  if (e == cudaSuccess && ev_after) e = cudaEventRecord(ev_after, s);
   if (e == cudaSuccess)
     e = launch_pdl(oscar_merge_kernel, dim3(p.num_kv_heads, batch, (p.gqa + 1) / 2), dim3(kMergeThreads),
                    kMergeSmem, s, p);

@@ -299,7 +299,8 @@ int oscar_load_rotations(oscar_ctx* ctx, const float* R_K, const float* R_V, con
 
 static int append_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
                        const void* k, const void* v, int32_t batch, int32_t n_new, float* trace,
-                       int32_t trace_positions, void* stream) {
+                       int32_t trace_positions, void* stream, cudaEvent_t ev_before = nullptr,
+                       cudaEvent_t ev_after = nullptr) {
   if (!ctx) return OSCAR_ERR_INVALID_ARG;
   if (!ctx->loaded) return fail(ctx, OSCAR_ERR_NOT_LOADED, "quant_append: rotations not loaded");
   if (!ctx->pool) return fail(ctx, OSCAR_ERR_NOT_BOUND, "quant_append: no cache bound");
@@ -365,11 +366,12 @@ static int append_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_stat
     int cph = ctx->num_sms / (ctx->cfg.num_kv_heads * batch);
     if (cph < 1) cph = 1;
     if (cph > tiles) cph = tiles;
-    cudaError_t e = launch_prefill_append(pp, cph, st);
+    cudaError_t e = launch_prefill_append(pp, cph, st, ev_before, ev_after);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "quant_append (tensor-core part) launch");
     p.tail_only = 1;
+    ev_before = ev_after = nullptr;
   }
-  cudaError_t e = launch_quant_append(p, st);
+  cudaError_t e = launch_quant_append(p, st, ev_before, ev_after);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "quant_append launch");
   return OSCAR_OK;
 }
@@ -386,14 +388,21 @@ int oscar_quant_append_traced(oscar_ctx* ctx, const int32_t* page_table, oscar_s
   return append_impl(ctx, page_table, state, k, v, batch, n_new, trace, trace_positions, stream);
 }
 
+int oscar_quant_append_timed(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
+                             const void* k, const void* v, int32_t batch, int32_t n_new, void* stream,
+                             void* ev_before, void* ev_after) {
+  return append_impl(ctx, page_table, state, k, v, batch, n_new, nullptr, 0, stream,
+                     static_cast<cudaEvent_t>(ev_before), static_cast<cudaEvent_t>(ev_after));
+}
+
 int oscar_decode_splits(const oscar_ctx* ctx, int32_t batch, int32_t* splits) {
   if (!ctx || !splits || batch < 1) return OSCAR_ERR_INVALID_ARG;
   *splits = auto_splits(ctx, batch);
   return OSCAR_OK;
 }
 
-int oscar_decode_attn(oscar_ctx* ctx, const void* q, const int32_t* page_table,
-                      const oscar_seq_state* state, float* o, int32_t batch, void* stream) {
+static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table, const oscar_seq_state* state,
+                       float* o, int32_t batch, void* stream, cudaEvent_t ev_before, cudaEvent_t ev_after) {
   if (!ctx) return OSCAR_ERR_INVALID_ARG;
   if (!ctx->loaded) return fail(ctx, OSCAR_ERR_NOT_LOADED, "decode_attn: rotations not loaded");
   if (!ctx->pool) return fail(ctx, OSCAR_ERR_NOT_BOUND, "decode_attn: no cache bound");
@@ -425,9 +434,21 @@ int oscar_decode_attn(oscar_ctx* ctx, const void* q, const int32_t* page_table,
   p.max_batch = ctx->cfg.max_batch;
   p.scale_log2 = ctx->cfg.softmax_scale * 1.4426950408889634f;
   p.err_flags = ctx->flags;
-  cudaError_t e = launch_decode(p, batch, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_decode(p, batch, static_cast<cudaStream_t>(stream), ev_before, ev_after);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "decode_attn launch");
   return OSCAR_OK;
+}
+
+int oscar_decode_attn(oscar_ctx* ctx, const void* q, const int32_t* page_table,
+                      const oscar_seq_state* state, float* o, int32_t batch, void* stream) {
+  return decode_impl(ctx, q, page_table, state, o, batch, stream, nullptr, nullptr);
+}
+
+int oscar_decode_attn_timed(oscar_ctx* ctx, const void* q, const int32_t* page_table,
+                            const oscar_seq_state* state, float* o, int32_t batch, void* stream,
+                            void* ev_before, void* ev_after) {
+  return decode_impl(ctx, q, page_table, state, o, batch, stream, static_cast<cudaEvent_t>(ev_before),
+                     static_cast<cudaEvent_t>(ev_after));
 }
 
 int oscar_error_flags(oscar_ctx* ctx, uint32_t* flags, int32_t clear) {

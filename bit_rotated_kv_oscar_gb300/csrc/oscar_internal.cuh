@@ -121,11 +121,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // launchers (return cudaGetLastError())
-cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s);
-cudaError_t launch_prefill_append(const PrefillParams& p, int ctas_per_head, cudaStream_t s);
+// ev_before / ev_after (may be null): recorded on s around the main launch
+cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s, cudaEvent_t ev_before = nullptr,
+                                cudaEvent_t ev_after = nullptr);
+cudaError_t launch_prefill_append(const PrefillParams& p, int ctas_per_head, cudaStream_t s,
+                                  cudaEvent_t ev_before = nullptr, cudaEvent_t ev_after = nullptr);
 bool prefill_supported(const void* k, const void* v);   // TMA needs 16-byte aligned inputs
 int prefill_image_bytes();
-cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cudaEvent_t ev_before = nullptr,
+                          cudaEvent_t ev_after = nullptr);
 int decode_smem_bytes();
 
 }  // namespace oscar

@@ -498,7 +498,8 @@ bool prefill_supported(const void* k, const void* v) {
   return ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) == 0;
 }
 
-cudaError_t launch_prefill_append(const PrefillParams& p_in, int ctas_per_head, cudaStream_t s) {
+cudaError_t launch_prefill_append(const PrefillParams& p_in, int ctas_per_head, cudaStream_t s,
+                                  cudaEvent_t ev_before, cudaEvent_t ev_after) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(oscar_prefill_append_kernel,
@@ -510,9 +511,11 @@ cudaError_t launch_prefill_append(const PrefillParams& p_in, int ctas_per_head, 
   if (!encode_map(&p.tmap_k, p.k, p.num_kv_heads, p.n_new, p.batch) ||
       !encode_map(&p.tmap_v, p.v, p.num_kv_heads, p.n_new, p.batch))
     return cudaErrorInvalidValue;
+  if (ev_before && cudaEventRecord(ev_before, s) != cudaSuccess) return cudaGetLastError();
   cudaError_t e = launch_pdl(oscar_prefill_append_kernel, dim3(ctas_per_head, p.num_kv_heads, p.batch),
                              dim3(kPfThreads), kPfSmem, s, p);
   if (e != cudaSuccess) return e;
+  if (ev_after && (e = cudaEventRecord(ev_after, s)) != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -256,7 +256,8 @@ oscar_quant_append_kernel(AppendParams p) {
   }
 }
 
-cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s) {
+cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s, cudaEvent_t ev_before,
+                                cudaEvent_t ev_after) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(oscar_quant_append_kernel,
@@ -281,8 +282,10 @@ cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s) {
   if (tpc > kMaxTokensPerCta) tpc = kMaxTokensPerCta;
   q.tokens_per_cta = (int32_t)tpc;
   dim3 grid((unsigned)((nvirt + tpc - 1) / tpc), (unsigned)p.num_kv_heads, (unsigned)p.batch);
+  if (ev_before && cudaEventRecord(ev_before, s) != cudaSuccess) return cudaGetLastError();
   cudaError_t e = launch_pdl(oscar_quant_append_kernel, grid, dim3(kThreads), kAppendSmem, s, q);
   if (e != cudaSuccess) return e;
+  if (ev_after && (e = cudaEventRecord(ev_after, s)) != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

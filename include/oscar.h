@@ -208,6 +208,23 @@ int oscar_error_flags(oscar_ctx* ctx, uint32_t* flags, int32_t clear);
 /* Message of the last failure on ctx ("" if none; a static text for NULL). */
 const char* oscar_last_error(const oscar_ctx* ctx);
 
+/* Measurement variants (no counterpart on the method's pages: a profiling aid of
+ * this library). They do exactly what oscar_decode_attn / oscar_quant_append do
+ * and in addition record two caller-created CUDA events (cudaEvent_t, passed as
+ * void*, either may be NULL) on `stream`: ev_before just before and ev_after just
+ * after the launch of the main kernel - the split-K attention kernel of the
+ * decode call; the tensor-core kernel of a long append (an append short enough
+ * to take only the per-token kernel records the events around that kernel). The
+ * records order that launch after its predecessor and before its successor, so
+ * the programmatic overlap between neighbouring launches is lost while timing.
+ * Statuses and errors as for the untimed calls. */
+int oscar_decode_attn_timed(oscar_ctx* ctx, const void* q, const int32_t* page_table,
+                            const oscar_seq_state* state, float* o, int32_t batch, void* stream,
+                            void* ev_before, void* ev_after);
+int oscar_quant_append_timed(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
+                             const void* k, const void* v, int32_t batch, int32_t n_new, void* stream,
+                             void* ev_before, void* ev_after);
+
 /* Size of the fixed device array behind oscar_decode_attn_noalloc. */
 #define OSCAR_NOALLOC_SCRATCH_BYTES (32u << 20)
 
