@@ -597,17 +597,18 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     }
 
     // ---- online softmax over the pair, per head (lazy maximum) ------------------
+    // The running maximum only has to bound every score seen to within kLazyLog2:
+    // a warp vote on this lane's own scores decides whether it must move, and only
+    // then is the maximum over the head's 16 lanes taken.
     float mx0 = fmaxf(fmaxf(u[0], u[2]), fmaxf(u[4], u[6]));
     float mx1 = fmaxf(fmaxf(u[1], u[3]), fmaxf(u[5], u[7]));
+    if (__any_sync(0xffffffffu, mx0 > m0 + tau_u || mx1 > m1 + tau_u)) {
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    // (every head sees the same tokens, so "nothing valid seen yet" is warp-uniform)
-    if (!(mx0 == -INFINITY && m0 == -INFINITY)) {
-    const bool bump0 = mx0 > m0 + tau_u, bump1 = mx1 > m1 + tau_u;
-    if (__any_sync(0xffffffffu, bump0 || bump1)) {
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const bool bump0 = mx0 > m0 + tau_u, bump1 = mx1 > m1 + tau_u;
       const float a0 = bump0 ? ex2((m0 - mx0) * uscale) : 1.f;
       const float a1 = bump1 ? ex2((m1 - mx1) * uscale) : 1.f;
       m0 = bump0 ? mx0 : m0;
@@ -626,6 +627,9 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
       oz[2] *= a0;
       oz[3] *= a1;
     }
+    // every head sees the same tokens: the maximum stays -inf (warp-uniformly)
+    // until a valid token has been seen, and pairs before that add nothing
+    if (m0 != -INFINITY) {
     const float nb0 = fmaf(-m0, uscale, lg_ps), nb1 = fmaf(-m1, uscale, lg_ps);
     float pr[8];  // p * pscale, p <= 2^8
 #pragma unroll
