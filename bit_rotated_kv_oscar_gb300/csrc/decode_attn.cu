@@ -436,7 +436,10 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
 
 // acc[cb] += codes^T (p * s_v) and oz += z_v^T p for one staged page; P01 / P23
 // hold fp16 p * pscale of my tokens; with MASKED, m01 / m23 zero the metadata of
-// masked token slots (whose bytes may be stale)
+// masked token slots (whose bytes may be stale). Row 4 of the zero-point row
+// operand is all ones, so row 4 of oz sums the same fp16 probabilities the
+// values are weighted with: the softmax denominator, consistent with the
+// numerator to the last bit of p.
 template <bool MASKED>
 __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_t P01, uint32_t P23,
                                             uint32_t m01, uint32_t m23, float (&acc)[8][4],
@@ -459,8 +462,9 @@ __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_
 #undef OSCAR_PV
   }
   const uint8_t* mz = sb + 1280 + 16 * (4 * (gid & 3) + tig);
-  uint32_t za0 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 4) : 0u;
-  uint32_t za2 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 12) : 0u;
+  constexpr uint32_t kOnes = 0x3c003c00u;  // fp16 (1, 1)
+  uint32_t za0 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 4) : (gid == 4 ? kOnes : 0u);
+  uint32_t za2 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 12) : (gid == 4 ? kOnes : 0u);
   if (MASKED) {
     za0 &= m01;
     za2 &= m23;
@@ -543,8 +547,9 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
   // running (lazy) max in score units u (log2 units = u * uscale), running sum and
   // accumulators in units of pscale
-  // per lane: heads 2 tig (index 0) and 2 tig + 1 (index 1)
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // per lane: running maxima of heads 2 tig (index 0) and 2 tig + 1 (index 1); the
+  // running sums are row 4 of oz (see page_values)
+  float m0 = -INFINITY, m1 = -INFINITY;
   float acc[8][4];
   float oz[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -613,8 +618,6 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
       const float a1 = bump1 ? ex2((m1 - mx1) * uscale) : 1.f;
       m0 = bump0 ? mx0 : m0;
       m1 = bump1 ? mx1 : m1;
-      l0 *= a0;
-      l1 *= a1;
 #pragma unroll
       for (int cb = 0; cb < 8; ++cb) {
         acc[cb][0] *= a0;
@@ -634,8 +637,6 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     float pr[8];  // p * pscale, p <= 2^8
 #pragma unroll
     for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], uscale, (i & 1) ? nb1 : nb0));
-    l0 += (pr[0] + pr[2]) + (pr[4] + pr[6]);
-    l1 += (pr[1] + pr[3]) + (pr[5] + pr[7]);
     // token-major probabilities -> the (token, head) column operand of P.V
     const uint32_t PA01 = transpose8x8(f2_to_h2_bits(pr[0], pr[1]));
     const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
@@ -658,20 +659,16 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   cp_wait<0>();
 
   // ---- per-warp partial -> shared memory, then CTA merge --------------------
-#pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-  }
   const float inv_ps = 1.f / pscale;
   __syncthreads();  // staging buffers are reused below
   float* wpart = reinterpret_cast<float*>(smem);              // [8 warps][8 heads][128]
   float* wml = wpart + kWarps * kMaxGqa * kHeadDim;           // [8 warps][8 heads][2]
-  if (gid == 0) {
+  if (gid == 4) {
+    // oz row 4: the sums of the probabilities of heads 2 tig, 2 tig + 1
     wml[(warp * kMaxGqa + 2 * tig) * 2] = m0 * uscale;          // log2 units
-    wml[(warp * kMaxGqa + 2 * tig) * 2 + 1] = l0 * inv_ps;
+    wml[(warp * kMaxGqa + 2 * tig) * 2 + 1] = oz[0] * inv_ps;
     wml[(warp * kMaxGqa + 2 * tig + 1) * 2] = m1 * uscale;
-    wml[(warp * kMaxGqa + 2 * tig + 1) * 2 + 1] = l1 * inv_ps;
+    wml[(warp * kMaxGqa + 2 * tig + 1) * 2 + 1] = oz[1] * inv_ps;
   }
 #pragma unroll
   for (int cb = 0; cb < 8; ++cb) {
