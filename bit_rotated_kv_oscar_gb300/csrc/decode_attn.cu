@@ -136,8 +136,12 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
   __shared__ __half gsum[2][kMaxGqa][kGroups];
   __shared__ float wmax[4];
   stage_matrix(Rs, p.R_K + (size_t)h * kHeadDim * kHeadDim, tid, kRotThreads);  // constant data
-  pdl_trigger();
-  pdl_wait();  // q may come from the previous kernel; qrec is read by the previous decode
+  // No wait here: every kernel of this library lets its dependents start only
+  // after its own prerequisites completed, so by the time this kernel runs, q
+  // (written before the preceding kernel) is final and the previous decode no
+  // longer reads qrec. The preceding kernel itself (typically the append) may
+  // still run: the wait at the end makes this kernel finish after it, so the
+  // attention kernel's wait covers both.
   for (int i = tid; i < g * kHeadDim; i += kRotThreads)
     qs[i >> 7][i & 127] = __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g) * kHeadDim + i]);
   cp_wait<0>();
@@ -230,6 +234,8 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
           ((uint32_t)__half_as_ushort(gsum[r][gid][2 * tig + 1]) << 16);
     rec[1024 + tid] = w;
   }
+  pdl_wait();
+  pdl_trigger();
 }
 
 // --------------------------------------------------------------------------
@@ -713,8 +719,8 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
 __global__ void __launch_bounds__(kThreads, 2) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  pdl_trigger();
   pdl_wait();  // cache, state and q~ come from earlier kernels
+  pdl_trigger();
   const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   if (x < p.win_slots)
     window_attention(p, b, h, x, smem);
@@ -746,8 +752,8 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   const int nh = min(2, g - m0);
   if (!p.fold_rv) stage_matrix(RT, p.R_VT + (size_t)h * kHeadDim * kHeadDim, tid, kMergeThreads);
   else cp_commit();
-  pdl_trigger();
   pdl_wait();  // the partials come from the decode kernel
+  pdl_trigger();
   const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
   for (int i = tid; i < nslots * nh; i += kMergeThreads) {
     const int sidx = i / nh, hh = i % nh;

@@ -99,8 +99,10 @@ struct DecodeParams {
 
 // Programmatic dependent launch: kernels launched with launch_pdl may start
 // while the previous kernel on the stream is still running. Each of them stages
-// constant data first, lets its own dependents start (pdl_trigger) and calls
-// pdl_wait before it touches anything an earlier kernel writes or reads.
+// constant data first, calls pdl_wait before it touches anything an earlier
+// kernel writes or reads, and only then lets its own dependents start
+// (pdl_trigger): so when a kernel starts, everything before its predecessor has
+// completed. The query rotation relies on that to run beside the append.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::); }
 

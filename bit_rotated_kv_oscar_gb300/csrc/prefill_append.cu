@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_k)) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&p.tmap_v)) : "memory");
   }
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
 
   if (tid == 0) s_st = p.state[b];
   if (warp == kMmaTid / 32) {

@@ -75,8 +75,8 @@ oscar_quant_append_kernel(AppendParams p) {
     }
     asm volatile("cp.async.commit_group;\n" ::);
   }
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   if (tid == 0) {
     s_st = p.state[b];
     __threadfence();

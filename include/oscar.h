@@ -27,6 +27,12 @@
  *     Kernel work is asynchronous on that stream; errors found by the host are
  *     reported at once, errors found by the device are latched in a flag word
  *     read by oscar_error_flags().
+ *   - Kernels are launched with programmatic dependent launch and let the next
+ *     launch on the stream start only once their own inputs were complete. A
+ *     caller's kernel that runs right before a call of this library and itself
+ *     allows early dependent launch must likewise do so only after its own
+ *     prerequisites completed (the query rotation of oscar_decode_attn reads q
+ *     as soon as it starts).
  *   - Supported shapes: head_dim 128, page_size 16, group_size 32, and a query
  *     group (num_q_heads / num_kv_heads) of 1, 2, 4 or 8. Anything else is
  *     OSCAR_ERR_UNSUPPORTED.
