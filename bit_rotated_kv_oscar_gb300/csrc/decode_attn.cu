@@ -441,23 +441,21 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
 }
 
 // acc[cb] += codes^T (p * s_v) and oz += z_v^T p for one staged page; P01 / P23
-// hold fp16 p * pscale of my tokens; with MASKED, m01 / m23 zero the metadata of
-// masked token slots (whose bytes may be stale). Row 4 of the zero-point row
+// hold fp16 p * pscale of my tokens (0 for masked tokens, whose value metadata
+// the caller has zeroed). Row 4 of the zero-point row
 // operand is all ones, so row 4 of oz sums the same fp16 probabilities the
 // values are weighted with: the softmax denominator, consistent with the
 // numerator to the last bit of p.
-template <bool MASKED>
 __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_t P01, uint32_t P23,
-                                            uint32_t m01, uint32_t m23, float (&acc)[8][4],
-                                            float (&oz)[4]) {
+                                            float (&acc)[8][4], float (&oz)[4]) {
   const int gid = lane >> 2, tig = lane & 3;
   const uint4 vw = *reinterpret_cast<const uint4*>(sb + 512 + lane * 16);
 #pragma unroll
   for (int gq = 0; gq < 4; ++gq) {
     const uint2 mv = *reinterpret_cast<const uint2*>(sb + 1280 + 16 * (4 * gq + tig));
     const uint2 mv2 = *reinterpret_cast<const uint2*>(sb + 1280 + 16 * (4 * gq + tig) + 8);
-    const uint32_t B0 = hmul2_bits(P01, MASKED ? (mv.x & m01) : mv.x);
-    const uint32_t B1 = hmul2_bits(P23, MASKED ? (mv2.x & m23) : mv2.x);
+    const uint32_t B0 = hmul2_bits(P01, mv.x);
+    const uint32_t B1 = hmul2_bits(P23, mv2.x);
 #define OSCAR_PV(CB)                                                                          \
   mma16816(acc[CB], slot_bits<CB>(vw.x), slot_bits<CB>(vw.y), slot_bits<CB>(vw.z), slot_bits<CB>(vw.w), \
            B0, B1);
@@ -469,13 +467,37 @@ __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_
   }
   const uint8_t* mz = sb + 1280 + 16 * (4 * (gid & 3) + tig);
   constexpr uint32_t kOnes = 0x3c003c00u;  // fp16 (1, 1)
-  uint32_t za0 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 4) : (gid == 4 ? kOnes : 0u);
-  uint32_t za2 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 12) : (gid == 4 ? kOnes : 0u);
-  if (MASKED) {
-    za0 &= m01;
-    za2 &= m23;
-  }
+  const uint32_t za0 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 4) : (gid == 4 ? kOnes : 0u);
+  const uint32_t za2 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 12) : (gid == 4 ? kOnes : 0u);
   mma16816(oz, za0, 0u, za2, 0u, P01, P23);
+}
+
+// bits t of the tokens t in [0, 16) of a page at position pos that lie in [lo, hi)
+__device__ __forceinline__ uint32_t page_token_bits(bool ok, int pos, int lo, int hi) {
+  const int a = max(lo - pos, 0), e = min(hi - pos, kPage);
+  return (ok && e > a) ? (((1u << (e - a)) - 1u) << a) : 0u;
+}
+
+// zero the value scales and zeros of the tokens of two staged pages whose bit in
+// `valid` is clear (bit t: page A token t, bit 16 + t: page B token t); lane:
+// page lane / 16, 16-byte chunk c = 4 g + bb of the value metadata, whose 32-bit
+// word w holds tokens 8 (w / 2) + 2 bb and + 1 (scales for even w, zeros for odd)
+__device__ __forceinline__ void zero_masked_value_meta(uint8_t* sbA, uint8_t* sbB, uint32_t valid, int lane) {
+  const int c = lane & 15;
+  const uint32_t vpage = (lane >> 4) ? (valid >> 16) : (valid & 0xffffu);
+  uint4* chunk = reinterpret_cast<uint4*>(((lane >> 4) ? sbB : sbA) + 1280 + 16 * c);
+  uint32_t keep[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int tw = 8 * (w >> 1) + 2 * (c & 3);
+    keep[w] = (((vpage >> tw) & 1u) ? 0x0000ffffu : 0u) | (((vpage >> (tw + 1)) & 1u) ? 0xffff0000u : 0u);
+  }
+  uint4 x = *chunk;
+  x.x &= keep[0];
+  x.y &= keep[1];
+  x.z &= keep[2];
+  x.w &= keep[3];
+  *chunk = x;
 }
 
 __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, uint8_t* smem) {
@@ -561,8 +583,6 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 #pragma unroll
   for (int cb = 0; cb < 8; ++cb) acc[cb][0] = acc[cb][1] = acc[cb][2] = acc[cb][3] = 0.f;
 
-  const int t0 = 2 * tig;  // tokens of my probability operand: t0, t0+1, t0+8, t0+9
-
   // pages are consumed two at a time (one softmax update per pair)
   for (int j = 0; j < nmine; j += 2) {
     const bool two = j + 1 < nmine;
@@ -578,33 +598,24 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
     float u[8];
     pair_scores(sbA, sbB, qs, zqb, lane, u);
-    uint32_t mA01 = 0xffffffffu, mA23 = 0xffffffffu, mB01 = 0xffffffffu, mB23 = 0xffffffffu;
     if (!full) {
-      // scores: tokens gid, gid + 8 of each page
-      const bool sA0 = okA && posA + gid >= lo && posA + gid < hi;
-      const bool sA1 = okA && posA + gid + 8 >= lo && posA + gid + 8 < hi;
-      const bool sB0 = okB && posB + gid >= lo && posB + gid < hi;
-      const bool sB1 = okB && posB + gid + 8 >= lo && posB + gid + 8 < hi;
-      u[0] = sA0 ? u[0] : -INFINITY;
-      u[1] = sA0 ? u[1] : -INFINITY;
-      u[2] = sA1 ? u[2] : -INFINITY;
-      u[3] = sA1 ? u[3] : -INFINITY;
-      u[4] = sB0 ? u[4] : -INFINITY;
-      u[5] = sB0 ? u[5] : -INFINITY;
-      u[6] = sB1 ? u[6] : -INFINITY;
-      u[7] = sB1 ? u[7] : -INFINITY;
-      // value metadata of tokens t0, t0+1, t0+8, t0+9 (stale bytes in masked slots)
-      bool v[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int off = t0 + (i & 1) + 8 * (i >> 1);
-        v[i] = okA && posA + off >= lo && posA + off < hi;
-        v[4 + i] = okB && posB + off >= lo && posB + off < hi;
-      }
-      mA01 = (v[0] ? 0x0000ffffu : 0u) | (v[1] ? 0xffff0000u : 0u);
-      mA23 = (v[2] ? 0x0000ffffu : 0u) | (v[3] ? 0xffff0000u : 0u);
-      mB01 = (v[4] ? 0x0000ffffu : 0u) | (v[5] ? 0xffff0000u : 0u);
-      mB23 = (v[6] ? 0x0000ffffu : 0u) | (v[7] ? 0xffff0000u : 0u);
+      // tokens outside [lo, hi), on a page with a bad id or on a missing second
+      // page: scores -inf, and their value scales and zeros set to 0 in shared
+      // memory (the bytes there may be stale), so the value product is the same
+      // code for every pair
+      const uint32_t valid = page_token_bits(okA, posA, lo, hi) | (page_token_bits(okB, posB, lo, hi) << 16);
+      const bool a0v = (valid >> gid) & 1u, a1v = (valid >> (gid + 8)) & 1u;
+      const bool b0v = (valid >> (gid + 16)) & 1u, b1v = (valid >> (gid + 24)) & 1u;
+      u[0] = a0v ? u[0] : -INFINITY;
+      u[1] = a0v ? u[1] : -INFINITY;
+      u[2] = a1v ? u[2] : -INFINITY;
+      u[3] = a1v ? u[3] : -INFINITY;
+      u[4] = b0v ? u[4] : -INFINITY;
+      u[5] = b0v ? u[5] : -INFINITY;
+      u[6] = b1v ? u[6] : -INFINITY;
+      u[7] = b1v ? u[7] : -INFINITY;
+      zero_masked_value_meta(const_cast<uint8_t*>(sbA), const_cast<uint8_t*>(sbB), valid, lane);
+      __syncwarp();
     }
 
     // ---- online softmax over the pair, per head (lazy maximum) ------------------
@@ -648,13 +659,8 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
     const uint32_t PB01 = transpose8x8(f2_to_h2_bits(pr[4], pr[5]));
     const uint32_t PB23 = transpose8x8(f2_to_h2_bits(pr[6], pr[7]));
-    if (full) {
-      page_values<false>(sbA, lane, PA01, PA23, 0u, 0u, acc, oz);
-      page_values<false>(sbB, lane, PB01, PB23, 0u, 0u, acc, oz);
-    } else {
-      page_values<true>(sbA, lane, PA01, PA23, mA01, mA23, acc, oz);
-      page_values<true>(sbB, lane, PB01, PB23, mB01, mB23, acc, oz);
-    }
+    page_values(sbA, lane, PA01, PA23, acc, oz);
+    page_values(sbB, lane, PB01, PB23, acc, oz);
     }
     __syncwarp();
     if (j + kStages < nmine) issue(j + kStages);
