@@ -30,6 +30,8 @@
 // out of the per-channel-block accumulator (values).
 #include <math.h>
 
+#include <type_traits>
+
 #include "oscar_internal.cuh"
 
 namespace oscar {
@@ -51,14 +53,16 @@ __host__ __device__ constexpr float slot_factor(int i) {
   return i <= 4 ? (float)(1 << (2 * i)) : (float)(1 << (2 * (i - 5)));
 }
 
+// w: a code word, wh = w >> 10 (computed once per word, shared by slots 5..7)
 template <int I>
-__device__ __forceinline__ uint32_t slot_bits(uint32_t w) {
+__device__ __forceinline__ uint32_t slot_bits(uint32_t w, uint32_t wh) {
   if constexpr (I <= 4) {
     return w & (0x00030003u << (2 * I));
   } else {
-    return (w >> 10) & (0x00030003u << (2 * (I - 5)));
+    return wh & (0x00030003u << (2 * (I - 5)));
   }
 }
+__device__ __forceinline__ uint4 shr10(uint4 w) { return make_uint4(w.x >> 10, w.y >> 10, w.z >> 10, w.w >> 10); }
 
 // d += a b (no side effects: not volatile, so the compiler may interleave
 // independent products with the arithmetic around them)
@@ -378,6 +382,7 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
   const int gid = lane >> 2, tig = lane & 3;
   const uint4 kwA = *reinterpret_cast<const uint4*>(sbA + lane * 16);
   const uint4 kwB = *reinterpret_cast<const uint4*>(sbB + lane * 16);
+  const uint4 kwAh = shr10(kwA), kwBh = shr10(kwB);
   {
     // K zeros of tokens gid and gid + 8, groups 2 (tig & 1) and 2 (tig & 1) + 1 (the
     // lo copy of the group sums sits in k rows 4-7, read by tig 2 and 3)
@@ -403,10 +408,10 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
 #define OSCAR_QK(KB, MMA)                                                                          \
   {                                                                                                \
     const uint4 q4 = qs[(KB) * 32 + lane];                                                         \
-    const uint32_t xa = slot_bits<KB>(kwA.x), ya = slot_bits<KB>(kwA.y);                           \
-    const uint32_t za = slot_bits<KB>(kwA.z), wa = slot_bits<KB>(kwA.w);                           \
-    const uint32_t xb = slot_bits<KB>(kwB.x), yb = slot_bits<KB>(kwB.y);                           \
-    const uint32_t zb = slot_bits<KB>(kwB.z), wb = slot_bits<KB>(kwB.w);                           \
+    const uint32_t xa = slot_bits<KB>(kwA.x, kwAh.x), ya = slot_bits<KB>(kwA.y, kwAh.y);           \
+    const uint32_t za = slot_bits<KB>(kwA.z, kwAh.z), wa = slot_bits<KB>(kwA.w, kwAh.w);           \
+    const uint32_t xb = slot_bits<KB>(kwB.x, kwBh.x), yb = slot_bits<KB>(kwB.y, kwBh.y);           \
+    const uint32_t zb = slot_bits<KB>(kwB.z, kwBh.z), wb = slot_bits<KB>(kwB.w, kwBh.w);           \
     MMA(a, xa, za, ya, wa, q4.x, q4.y);                                                            \
     mma16816(a, xa, za, ya, wa, q4.z, q4.w);                                                       \
     MMA(c, xb, zb, yb, wb, q4.x, q4.y);                                                            \
@@ -450,6 +455,7 @@ __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_
                                             float (&acc)[8][4], float (&oz)[4]) {
   const int gid = lane >> 2, tig = lane & 3;
   const uint4 vw = *reinterpret_cast<const uint4*>(sb + 512 + lane * 16);
+  const uint4 vwh = shr10(vw);
 #pragma unroll
   for (int gq = 0; gq < 4; ++gq) {
     const uint2 mv = *reinterpret_cast<const uint2*>(sb + 1280 + 16 * (4 * gq + tig));
@@ -457,7 +463,8 @@ __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_
     const uint32_t B0 = hmul2_bits(P01, mv.x);
     const uint32_t B1 = hmul2_bits(P23, mv2.x);
 #define OSCAR_PV(CB)                                                                          \
-  mma16816(acc[CB], slot_bits<CB>(vw.x), slot_bits<CB>(vw.y), slot_bits<CB>(vw.z), slot_bits<CB>(vw.w), \
+  mma16816(acc[CB], slot_bits<CB>(vw.x, vwh.x), slot_bits<CB>(vw.y, vwh.y), slot_bits<CB>(vw.z, vwh.z),   \
+           slot_bits<CB>(vw.w, vwh.w),                                                                    \
            B0, B1);
     if (gq == 0) { OSCAR_PV(0) OSCAR_PV(1) }
     if (gq == 1) { OSCAR_PV(2) OSCAR_PV(3) }
@@ -550,25 +557,27 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   // page ids of this warp's first 32 pages, one per lane, loaded once (pages
   // beyond that, possible only with more than 256 pages per split, load on use)
   const int id_pre = lane < nmine ? ptrow[kWarps * lane] : -1;
-  auto issue = [&](int j) {
+  // stage page j into ring slot sl (= j % kStages); a page whose id is outside the
+  // pool is not copied, is masked out of the attention and reported after the loop
+  bool bad_id = false;
+  auto issue = [&](int j, int sl) {
     const int id = j < 32 ? __shfl_sync(0xffffffffu, id_pre, j) : ptrow[kWarps * j];
     const bool good = id >= 0 && id < p.num_pages;
-    const unsigned bit = 1u << (j & (kStages - 1));
+    const unsigned bit = 1u << sl;
     valid_bits = good ? (valid_bits | bit) : (valid_bits & ~bit);
+    bad_id |= !good;
     if (good) {
       const uint8_t* src = pool_h + (size_t)id * page_stride;
-      uint8_t* dst = sbuf + (j & (kStages - 1)) * kBlockBytes + lane * 16;
+      uint8_t* dst = sbuf + sl * kBlockBytes + lane * 16;
       cp_async16(dst, src);
       cp_async16(dst + 512, src + 512);
       cp_async16(dst + 1024, src + 1024);
-    } else if (lane == 0) {
-      atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
     }
   };
 
 #pragma unroll
   for (int s = 0; s < kStages; ++s) {
-    if (s < nmine) issue(s);
+    if (s < nmine) issue(s, s);
     cp_commit();
   }
   __syncthreads();  // q~ fragments visible to every warp
@@ -583,15 +592,21 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 #pragma unroll
   for (int cb = 0; cb < 8; ++cb) acc[cb][0] = acc[cb][1] = acc[cb][2] = acc[cb][3] = 0.f;
 
-  // pages are consumed two at a time (one softmax update per pair)
-  for (int j = 0; j < nmine; j += 2) {
+  // Pages are consumed two at a time (one softmax update per pair), pair j in ring
+  // slots SA, SA + 1 with SA = j % kStages; the loop below is unrolled over the two
+  // slot pairs so that every ring address and valid bit is a constant.
+  static_assert(kStages == 4, "the page loop is unrolled over two slot pairs");
+  auto consume_pair = [&](int j, auto sa_const) {
+    constexpr int SA = decltype(sa_const)::value;
     const bool two = j + 1 < nmine;
-    if (two) cp_wait<kStages - 2>(); else cp_wait<kStages - 1>();
+    // the copy groups of pages j and j + 1 (empty when a page does not exist) are
+    // the oldest two of the kStages in flight
+    cp_wait<kStages - 2>();
     __syncwarp();
-    const uint8_t* sbA = sbuf + (j & (kStages - 1)) * kBlockBytes;
-    const uint8_t* sbB = sbuf + ((j + 1) & (kStages - 1)) * kBlockBytes;
-    const bool okA = (valid_bits >> (j & (kStages - 1))) & 1u;
-    const bool okB = two && ((valid_bits >> ((j + 1) & (kStages - 1))) & 1u);
+    uint8_t* sbA = sbuf + SA * kBlockBytes;
+    uint8_t* sbB = sbA + kBlockBytes;
+    const bool okA = (valid_bits >> SA) & 1u;
+    const bool okB = two && ((valid_bits >> (SA + 1)) & 1u);
     const int posA = (pbeg + warp + kWarps * j) * kPage;
     const int posB = posA + kWarps * kPage;
     const bool full = okA && okB && posA >= lo && posA + kPage <= hi && posB >= lo && posB + kPage <= hi;
@@ -614,7 +629,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
       u[5] = b0v ? u[5] : -INFINITY;
       u[6] = b1v ? u[6] : -INFINITY;
       u[7] = b1v ? u[7] : -INFINITY;
-      zero_masked_value_meta(const_cast<uint8_t*>(sbA), const_cast<uint8_t*>(sbB), valid, lane);
+      zero_masked_value_meta(sbA, sbB, valid, lane);
       __syncwarp();
     }
 
@@ -663,12 +678,17 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     page_values(sbB, lane, PB01, PB23, acc, oz);
     }
     __syncwarp();
-    if (j + kStages < nmine) issue(j + kStages);
+    if (j + kStages < nmine) issue(j + kStages, SA);
     cp_commit();
-    if (j + 1 + kStages < nmine) issue(j + 1 + kStages);
+    if (j + 1 + kStages < nmine) issue(j + 1 + kStages, SA + 1);
     cp_commit();
+  };
+  for (int j = 0; j < nmine; j += 4) {
+    consume_pair(j, std::integral_constant<int, 0>{});
+    if (j + 2 < nmine) consume_pair(j + 2, std::integral_constant<int, 2>{});
   }
   cp_wait<0>();
+  if (__any_sync(0xffffffffu, bad_id) && lane == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
 
   // ---- per-warp partial -> shared memory, then CTA merge --------------------
   const float inv_ps = 1.f / pscale;
