@@ -554,20 +554,34 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   const size_t page_stride = (size_t)p.num_kv_heads * kBlockBytes;
   unsigned valid_bits = 0;  // bit (j & 3): page j of this warp has a valid id
 
-  // page ids of this warp's first 32 pages, one per lane, loaded once (pages
-  // beyond that, possible only with more than 256 pages per split, load on use)
-  const int id_pre = lane < nmine ? ptrow[kWarps * lane] : -1;
-  // stage page j into ring slot sl (= j % kStages); a page whose id is outside the
-  // pool is not copied, is masked out of the attention and reported after the loop
-  bool bad_id = false;
+  // page ids of this warp's first 64 pages, two per lane, loaded once together with
+  // their validity (a ballot); pages beyond that, possible only with more than 512
+  // pages per split, load on use. A page whose id is outside the pool is not
+  // copied, is masked out of the attention and reported after the loop.
+  const int id0 = lane < nmine ? ptrow[kWarps * lane] : 0;
+  const int id1 = lane + 32 < nmine ? ptrow[kWarps * (lane + 32)] : 0;
+  const uint32_t good0 = __ballot_sync(0xffffffffu, id0 >= 0 && id0 < p.num_pages);
+  const uint32_t good1 = __ballot_sync(0xffffffffu, id1 >= 0 && id1 < p.num_pages);
+  bool bad_id = good0 != 0xffffffffu || good1 != 0xffffffffu;
+  const uint32_t stride = (uint32_t)page_stride;   // heads x 1536 bytes, far below 2^32
+  // stage page j into ring slot sl (= j % kStages)
   auto issue = [&](int j, int sl) {
-    const int id = j < 32 ? __shfl_sync(0xffffffffu, id_pre, j) : ptrow[kWarps * j];
-    const bool good = id >= 0 && id < p.num_pages;
-    const unsigned bit = 1u << sl;
-    valid_bits = good ? (valid_bits | bit) : (valid_bits & ~bit);
-    bad_id |= !good;
+    int id;
+    bool good;
+    if (j < 32) {
+      id = __shfl_sync(0xffffffffu, id0, j);
+      good = (good0 >> j) & 1u;
+    } else if (j < 64) {
+      id = __shfl_sync(0xffffffffu, id1, j - 32);
+      good = (good1 >> (j - 32)) & 1u;
+    } else {
+      id = ptrow[kWarps * j];
+      good = id >= 0 && id < p.num_pages;
+      bad_id |= !good;
+    }
+    valid_bits = (valid_bits & ~(1u << sl)) | ((uint32_t)good << sl);
     if (good) {
-      const uint8_t* src = pool_h + (size_t)id * page_stride;
+      const uint8_t* src = pool_h + (uint64_t)(uint32_t)id * stride;
       uint8_t* dst = sbuf + sl * kBlockBytes + lane * 16;
       cp_async16(dst, src);
       cp_async16(dst + 512, src + 512);
