@@ -30,6 +30,11 @@ constexpr int kMaxGqa = 8;
 constexpr int kQrecWords = 1104;
 constexpr int kPartFloats = kHeadDim + 4;    // o[128], m, l, 2 pad (rows stay 16-byte aligned)
 constexpr int kWindowChunk = 64;             // BF16 window tokens per decode CTA
+// INT2 pages one decode CTA streams at most when the split count is automatic
+#ifndef OSCAR_SPLIT_PAGES
+#define OSCAR_SPLIT_PAGES 512
+#endif
+constexpr int kSplitPages = OSCAR_SPLIT_PAGES;
 
 struct AppendParams {
   const int32_t* page_table;
