@@ -313,44 +313,33 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
     }
   }
   __syncthreads();
-  if (warp < g) {
+  for (int m = warp; m < g; m += kWarps) {
     float mx = -INFINITY;
-    for (int t = lane; t < n; t += 32) mx = fmaxf(mx, sc[warp * kWinChunk + t]);
+    for (int t = lane; t < n; t += 32) mx = fmaxf(mx, sc[m * kWinChunk + t]);
     mx = warp_maxf(mx);
     float l = 0.f;
     for (int t = lane; t < n; t += 32) {
-      const float e = exp2f(sc[warp * kWinChunk + t] - mx);
-      sc[warp * kWinChunk + t] = e;
+      const float e = exp2f(sc[m * kWinChunk + t] - mx);
+      sc[m * kWinChunk + t] = e;
       l += e;
     }
     l = warp_sum(l);
     if (lane == 0) {
-      stat[2 * warp] = mx;
-      stat[2 * warp + 1] = l;
+      stat[2 * m] = mx;
+      stat[2 * m + 1] = l;
     }
   }
   __syncthreads();
   // values: thread per (head, channel)
-  const int c = tid & (kHeadDim - 1), m0 = tid >> 7;
-  float acc[kMaxGqa / 2] = {0.f, 0.f, 0.f, 0.f};
-  for (int r = 0; r < n; ++r) {
-    const float v = __bfloat162float(vrows[r * kHeadDim + c]);
-#pragma unroll
-    for (int i = 0; i < kMaxGqa / 2; ++i) {
-      const int m = m0 + 2 * i;
-      if (m < g) acc[i] = fmaf(sc[m * kWinChunk + r], v, acc[i]);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kMaxGqa / 2; ++i) {
-    const int m = m0 + 2 * i;
-    if (m < g) {
-      float* dst = part + (size_t)m * kPartFloats;
-      dst[c] = acc[i];
-      if (c == 0) {
-        dst[kHeadDim] = stat[2 * m];
-        dst[kHeadDim + 1] = stat[2 * m + 1];
-      }
+  for (int i = tid; i < g * kHeadDim; i += kThreads) {
+    const int m = i >> 7, c = i & (kHeadDim - 1);
+    float acc = 0.f;
+    for (int r = 0; r < n; ++r) acc = fmaf(sc[m * kWinChunk + r], __bfloat162float(vrows[r * kHeadDim + c]), acc);
+    float* dst = part + (size_t)m * kPartFloats;
+    dst[c] = acc;
+    if (c == 0) {
+      dst[kHeadDim] = stat[2 * m];
+      dst[kHeadDim + 1] = stat[2 * m + 1];
     }
   }
 }
@@ -529,7 +518,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
   // query operand fragments (see oscar_rotate_q_kernel)
   const uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
-  qs[tid] = reinterpret_cast<const uint4*>(rec)[tid];
+  for (int i = tid; i < 8 * 32; i += kThreads) qs[i] = reinterpret_cast<const uint4*>(rec)[i];
   // zero-point column operand: k rows 2 tig, 2 tig + 1 of head gid = group sums of
   // q~ (hi for tig 0 / 1, lo for tig 2 / 3), taken from the record's row layout
   uint32_t zqb;
@@ -552,7 +541,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   const int32_t* ptrow = p.page_table + (size_t)b * p.pt_stride + pbeg + warp;
   const uint8_t* pool_h = p.pool + (size_t)h * kBlockBytes + lane * 16;
   const size_t page_stride = (size_t)p.num_kv_heads * kBlockBytes;
-  unsigned valid_bits = 0;  // bit (j & 3): page j of this warp has a valid id
+  unsigned valid_bits = 0;  // bit (j % kStages): page j of this warp has a valid id
 
   // page ids of this warp's first 64 pages, two per lane, loaded once together with
   // their validity (a ballot); pages beyond that, possible only with more than 512
