@@ -746,7 +746,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) oscar_decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_wait();  // cache, state and q~ come from earlier kernels
   pdl_trigger();

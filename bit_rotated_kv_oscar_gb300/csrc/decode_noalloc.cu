@@ -44,7 +44,7 @@ int noalloc_splits(const oscar_config* c, int num_sms, int batch) {
   const int64_t units = (int64_t)batch * c->num_kv_heads;
   const int64_t pages = c->max_pages_per_seq;
   const int64_t wins = units * ((c->sink + c->recent + kWindowChunk - 1) / kWindowChunk);
-  int64_t by_wave = (2 * (int64_t)num_sms - wins) / units;
+  int64_t by_wave = (kDecodeCtasPerSm * (int64_t)num_sms - wins) / units;
   int64_t by_pages = (pages + kSplitPages - 1) / kSplitPages;
   int64_t s = by_wave > by_pages ? by_wave : by_pages;
   const int64_t cap = (pages + 7) / 8;

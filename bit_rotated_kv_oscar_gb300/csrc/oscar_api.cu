@@ -95,10 +95,10 @@ int auto_splits(const oscar_ctx* ctx, int batch) {
   if (ctx->cfg.num_splits > 0) return ctx->cfg.num_splits;
   const int64_t units = (int64_t)batch * ctx->cfg.num_kv_heads;
   const int64_t pages = ctx->cfg.max_pages_per_seq;
-  // fill one wave of two CTAs per SM together with the BF16-window CTAs; at most
+  // fill one wave of decode CTAs together with the BF16-window CTAs; at most
   // kSplitPages pages per CTA
   const int64_t wins = units * win_slots(&ctx->cfg);
-  int64_t by_wave = (2 * (int64_t)ctx->num_sms - wins) / units;
+  int64_t by_wave = (kDecodeCtasPerSm * (int64_t)ctx->num_sms - wins) / units;
   int64_t by_pages = (pages + kSplitPages - 1) / kSplitPages;
   int64_t s = by_wave > by_pages ? by_wave : by_pages;
   const int64_t cap = (pages + 7) / 8;  // keep >= 8 pages per split

@@ -35,6 +35,8 @@ constexpr int kWindowChunk = 64;             // BF16 window tokens per decode CT
 #define OSCAR_SPLIT_PAGES 512
 #endif
 constexpr int kSplitPages = OSCAR_SPLIT_PAGES;
+// decode CTAs resident per SM (registers and shared memory are sized for it)
+constexpr int kDecodeCtasPerSm = 2;
 
 struct AppendParams {
   const int32_t* page_table;

@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "oscar_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace oscar {
 
@@ -57,55 +58,12 @@ constexpr int kPfSmemStages = kStages * kImageBytes;
 constexpr int kPfSmemBars = (2 * (kStages + kAccBufs) + 1) * 8 + 16;
 constexpr int kPfSmem = 1024 + kPfSmemImages + kPfSmemStages + kPfSmemBars;
 constexpr uint32_t kTmemCols = kAccBufs * kHeadDim;       // 512
-constexpr long kSpinLimit = 1L << 20;
-
 // ---- PTX wrappers ------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
 __device__ __forceinline__ void cp16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
 }
 __device__ __forceinline__ void cp_commit_pf() { asm volatile("cp.async.commit_group;\n" ::); }
 __device__ __forceinline__ void cp_wait_all_pf() { asm volatile("cp.async.wait_group 0;\n" ::); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-
-__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(addr), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t addr) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(addr) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t addr, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(addr), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-// bounded wait on an mbarrier phase; false when the limit expires or another
-// role has given up (abort set)
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, const volatile int* abort) {
-  for (long it = 0; it < kSpinLimit; ++it) {
-    if (mbar_test(addr, parity)) return true;
-    if ((it & 31) == 31 && *abort) return false;
-  }
-  return false;
-}
-// bounded wait used while tearing down after an abort
-__device__ __forceinline__ bool mbar_drain(uint32_t addr, uint32_t parity) {
-  for (long it = 0; it < kSpinLimit; ++it)
-    if (mbar_test(addr, parity)) return true;
-  return false;
-}
 
 // one 64-channel x 128-token box of a 4-D tensor map into shared memory,
 // completing on an mbarrier; the input is read once, so it is marked for early
@@ -119,18 +77,6 @@ __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* ma
       : "memory");
 }
 
-// shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);        // start address
-  d |= (uint64_t)1 << 16;                         // leading byte offset (unused with this swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset
-  d |= (uint64_t)1 << 46;                         // descriptor version
-  d |= (uint64_t)2 << 61;                         // 128-byte swizzle
-  return d;
-}
-
 // instruction descriptor: D f32, A and B bf16, both K-major, M = 128, N = 128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
                             ((uint32_t)(128 >> 4) << 24);
@@ -141,34 +87,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate));
 }
-__device__ __forceinline__ void umma_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
-               : "memory");
-}
-
-// 32 consecutive accumulator columns of the warp's 32 TMEM lanes (no wait)
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-// the registers of a tcgen05.ld are defined only after tcgen05.wait::ld; tying
-// them to an asm statement placed after the wait keeps every use behind it
-__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
-                 "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
-                 "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
-}
-
 // ---- quantiser -----------------------------------------------------------------
 // The code of a value is clamp(rint(fp32(fp32(xc - zf) * fp32(1 / sf))), 0, 3) on
 // the clipped value xc (rint: nearest, ties to even). Adding 1.5 * 2^23 rounds a
