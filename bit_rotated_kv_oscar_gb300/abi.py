@@ -25,7 +25,12 @@ STATUS = {
 FLAG_BAD_PAGE_ID = 1
 FLAG_BAD_STATE = 2
 FLAG_TIMEOUT = 4
-PAGE_BLOCK_BYTES = 1536
+PAGE_BLOCK_BYTES = 1536  # group size 32
+
+
+def page_block_bytes(group_size: int = 32) -> int:
+    """Bytes of one (page, KV head) block of the INT2 pool (include/oscar.h)."""
+    return 1024 + 128 * (128 // group_size)
 
 
 class OscarError(RuntimeError):

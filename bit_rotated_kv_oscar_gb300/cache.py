@@ -113,4 +113,5 @@ class PagedCache:
         """(INT2 bytes of the mapped pages, BF16 window bytes) for `batch` requests."""
         used = np.unique(self.page_table_host[:batch][self.page_table_host[:batch] >= 0]).size
         kv = self.cfg.num_kv_heads
-        return used * kv * abi.PAGE_BLOCK_BYTES, batch * kv * 2 * (self.cfg.sink + self.cfg.recent) * 128 * 2
+        return (used * kv * abi.page_block_bytes(self.cfg.group_size),
+                batch * kv * 2 * (self.cfg.sink + self.cfg.recent) * 128 * 2)

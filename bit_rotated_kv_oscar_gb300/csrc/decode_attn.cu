@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
   __shared__ float qs[kMaxGqa][kHeadDim];
   __shared__ float red[kMaxGqa][kHeadDim];
   __shared__ __half hs[2][kMaxGqa][kHeadDim];
-  __shared__ __half gsum[2][kMaxGqa][kGroups];
+  __shared__ float wsum[kMaxGqa][4];  // per head and warp: 2^(k-24) times the sum of its 32 channels of q~
   __shared__ float wmax[4];
   stage_matrix(Rs, p.R_K + (size_t)h * kHeadDim * kHeadDim, tid, kRotThreads);  // constant data
   // No wait here: every kernel of this library lets its dependents start only
@@ -195,17 +195,13 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
       hs[1][m][c] = __float2half_rn(a - __half2float(hi));
     }
     uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
-    // group sums of q~ per head, scaled like the mma results (2^(k-24) sum q~),
-    // split into fp16 hi + lo: the A operand of the zero-point mma
+    // sums of q~ per head and 32 channels, scaled like the mma results
+    // (2^(k-24) sum q~); the group sums below are the zero-point operand
     const float gscale = ldexpf(1.f, k - 24);
 #pragma unroll
     for (int m = 0; m < kMaxGqa; ++m) {
       const float sm = warp_sum(acc[m]) * gscale;
-      if ((c & 31) == 0) {
-        const __half hi = __float2half_rn(sm);
-        gsum[0][m][c >> 5] = hi;
-        gsum[1][m][c >> 5] = __float2half_rn(sm - __half2float(hi));
-      }
+      if ((c & 31) == 0) wsum[m][c >> 5] = sm;
     }
     if (c == 0) {
       rec[1088] = __float_as_uint(ldexpf(1.f, 24 - k));
@@ -229,13 +225,23 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
     const uint32_t hi = __half_as_ushort(src[col + 1]);
     rec[widx] = lo | (hi << 16);
   }
-  // zero-point A fragment: row gid = head gid (hi), row gid + 8 = lo; k = group
+  // zero-point column operand: per lane (gid, tig) a hi and a lo word, the fp16
+  // hi / lo parts of the group sums of q~ for head gid, groups 2 tig and 2 tig + 1
+  // (4 groups of 32 channels: tig < 2; 2 groups of 64: tig = 0)
   if (tid < 64) {
     const int lane = tid >> 1, r = tid & 1, gid = lane >> 2, tig = lane & 3;
+    const int ng = p.ngroups;
     uint32_t w = 0u;
-    if (tig < 2)
-      w = (uint32_t)__half_as_ushort(gsum[r][gid][2 * tig]) |
-          ((uint32_t)__half_as_ushort(gsum[r][gid][2 * tig + 1]) << 16);
+    if (2 * tig < ng) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int gq = 2 * tig + e;
+        const float sm = ng == kGroups ? wsum[gid][gq] : wsum[gid][2 * gq] + wsum[gid][2 * gq + 1];
+        const __half hi = __float2half_rn(sm);
+        const __half part = r ? __float2half_rn(sm - __half2float(hi)) : hi;
+        w |= (uint32_t)__half_as_ushort(part) << (16 * e);
+      }
+    }
     rec[1024 + tid] = w;
   }
   pdl_wait();
@@ -366,6 +372,8 @@ constexpr float kLazyLog2 = 8.f;
 // q~ hi and lo are two column operands accumulating into the same group result,
 // so hi + lo needs no extra add. zqb: the zero-point column operand (group sums
 // of q~, hi in k rows 0-3, lo in rows 4-7).
+// NG: quantisation groups per token (4 of 32 channels, or 2 of 64).
+template <int NG>
 __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* sbB, const uint4* qs,
                                             uint32_t zqb, int lane, float (&u)[8]) {
   const int gid = lane >> 2, tig = lane & 3;
@@ -373,14 +381,18 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
   const uint4 kwB = *reinterpret_cast<const uint4*>(sbB + lane * 16);
   const uint4 kwAh = shr10(kwA), kwBh = shr10(kwB);
   {
-    // K zeros of tokens gid and gid + 8, groups 2 (tig & 1) and 2 (tig & 1) + 1 (the
-    // lo copy of the group sums sits in k rows 4-7, read by tig 2 and 3)
-    const int zo = 1152 + 8 * gid + 4 * (tig & 1);
+    // K zeros of tokens gid and gid + 8: k rows 0 .. NG-1 of the zero-point
+    // product pair with the hi, rows NG .. 2NG-1 with the lo copy of the group
+    // sums (4 groups: groups 2 (tig & 1), +1 for every tig; 2 groups: groups 0, 1
+    // for tig 0 and 1, nothing for tig 2 and 3)
+    const int zo = kzero_off(NG, gid, NG == kGroups ? 2 * (tig & 1) : 0);
+    constexpr int zpair = kzero_off(NG, 8, 0) - kzero_off(NG, 0, 0);  // token gid + 8
+    const bool zon = NG == kGroups || tig < 2;
     float zA[4], zB[4];
-    mma16816_z(zA, *reinterpret_cast<const uint32_t*>(sbA + zo), *reinterpret_cast<const uint32_t*>(sbA + zo + 64),
-               0u, 0u, zqb, 0u);
-    mma16816_z(zB, *reinterpret_cast<const uint32_t*>(sbB + zo), *reinterpret_cast<const uint32_t*>(sbB + zo + 64),
-               0u, 0u, zqb, 0u);
+    mma16816_z(zA, zon ? *reinterpret_cast<const uint32_t*>(sbA + zo) : 0u,
+               zon ? *reinterpret_cast<const uint32_t*>(sbA + zo + zpair) : 0u, 0u, 0u, zqb, 0u);
+    mma16816_z(zB, zon ? *reinterpret_cast<const uint32_t*>(sbB + zo) : 0u,
+               zon ? *reinterpret_cast<const uint32_t*>(sbB + zo + zpair) : 0u, 0u, 0u, zqb, 0u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       u[i] = zA[i];
@@ -388,11 +400,11 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
     }
   }
   // K scales of tokens gid (pair 0) and gid + 8 (pair 1): halves at
-  // 1024 + 32 (gid / 2) + 8 gq + 2 (gid % 2) and 4 bytes further
-  const int so = 1024 + 32 * (gid >> 1);
+  // 1024 + 8 NG (gid / 2) + 8 gq + 2 (gid % 2) and 4 bytes further
+  const int so = kscale_off(NG, gid & ~1, 0);
   const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
 #pragma unroll
-  for (int gq = 0; gq < 4; ++gq) {
+  for (int gq = 0; gq < NG; ++gq) {
     float a[4], c[4];
 #define OSCAR_QK(KB, MMA)                                                                          \
   {                                                                                                \
@@ -406,10 +418,15 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
     MMA(c, xb, zb, yb, wb, q4.x, q4.y);                                                            \
     mma16816(c, xb, zb, yb, wb, q4.z, q4.w);                                                       \
   }
-    if (gq == 0) { OSCAR_QK(0, mma16816_z) OSCAR_QK(1, mma16816) }
-    if (gq == 1) { OSCAR_QK(2, mma16816_z) OSCAR_QK(3, mma16816) }
-    if (gq == 2) { OSCAR_QK(4, mma16816_z) OSCAR_QK(5, mma16816) }
-    if (gq == 3) { OSCAR_QK(6, mma16816_z) OSCAR_QK(7, mma16816) }
+    if constexpr (NG == kGroups) {
+      if (gq == 0) { OSCAR_QK(0, mma16816_z) OSCAR_QK(1, mma16816) }
+      if (gq == 1) { OSCAR_QK(2, mma16816_z) OSCAR_QK(3, mma16816) }
+      if (gq == 2) { OSCAR_QK(4, mma16816_z) OSCAR_QK(5, mma16816) }
+      if (gq == 3) { OSCAR_QK(6, mma16816_z) OSCAR_QK(7, mma16816) }
+    } else {
+      if (gq == 0) { OSCAR_QK(0, mma16816_z) OSCAR_QK(1, mma16816) OSCAR_QK(2, mma16816) OSCAR_QK(3, mma16816) }
+      if (gq == 1) { OSCAR_QK(4, mma16816_z) OSCAR_QK(5, mma16816) OSCAR_QK(6, mma16816) OSCAR_QK(7, mma16816) }
+    }
 #undef OSCAR_QK
     const uint2 kA = *reinterpret_cast<const uint2*>(sbA + so + 8 * gq);
     const uint2 kB = *reinterpret_cast<const uint2*>(sbB + so + 8 * gq);
@@ -436,35 +453,44 @@ __device__ __forceinline__ uint32_t transpose8x8(uint32_t a) {
 
 // acc[cb] += codes^T (p * s_v) and oz += z_v^T p for one staged page; P01 / P23
 // hold fp16 p * pscale of my tokens (0 for masked tokens, whose value metadata
-// the caller has zeroed). Row 4 of the zero-point row
+// the caller has zeroed). Rows gq < NG of oz are the value zero-point terms of
+// group gq; row 4 of the zero-point row
 // operand is all ones, so row 4 of oz sums the same fp16 probabilities the
 // values are weighted with: the softmax denominator, consistent with the
 // numerator to the last bit of p.
+template <int NG>
 __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_t P01, uint32_t P23,
                                             float (&acc)[8][4], float (&oz)[4]) {
   const int gid = lane >> 2, tig = lane & 3;
   const uint4 vw = *reinterpret_cast<const uint4*>(sb + 512 + lane * 16);
   const uint4 vwh = shr10(vw);
+  constexpr int vbase = vscale_off(NG, 0, 0);
 #pragma unroll
-  for (int gq = 0; gq < 4; ++gq) {
-    const uint2 mv = *reinterpret_cast<const uint2*>(sb + 1280 + 16 * (4 * gq + tig));
-    const uint2 mv2 = *reinterpret_cast<const uint2*>(sb + 1280 + 16 * (4 * gq + tig) + 8);
+  for (int gq = 0; gq < NG; ++gq) {
+    const uint2 mv = *reinterpret_cast<const uint2*>(sb + vbase + 16 * (4 * gq + tig));
+    const uint2 mv2 = *reinterpret_cast<const uint2*>(sb + vbase + 16 * (4 * gq + tig) + 8);
     const uint32_t B0 = hmul2_bits(P01, mv.x);
     const uint32_t B1 = hmul2_bits(P23, mv2.x);
 #define OSCAR_PV(CB)                                                                          \
   mma16816(acc[CB], slot_bits<CB>(vw.x, vwh.x), slot_bits<CB>(vw.y, vwh.y), slot_bits<CB>(vw.z, vwh.z),   \
            slot_bits<CB>(vw.w, vwh.w),                                                                    \
            B0, B1);
-    if (gq == 0) { OSCAR_PV(0) OSCAR_PV(1) }
-    if (gq == 1) { OSCAR_PV(2) OSCAR_PV(3) }
-    if (gq == 2) { OSCAR_PV(4) OSCAR_PV(5) }
-    if (gq == 3) { OSCAR_PV(6) OSCAR_PV(7) }
+    if constexpr (NG == kGroups) {
+      if (gq == 0) { OSCAR_PV(0) OSCAR_PV(1) }
+      if (gq == 1) { OSCAR_PV(2) OSCAR_PV(3) }
+      if (gq == 2) { OSCAR_PV(4) OSCAR_PV(5) }
+      if (gq == 3) { OSCAR_PV(6) OSCAR_PV(7) }
+    } else {
+      if (gq == 0) { OSCAR_PV(0) OSCAR_PV(1) OSCAR_PV(2) OSCAR_PV(3) }
+      if (gq == 1) { OSCAR_PV(4) OSCAR_PV(5) OSCAR_PV(6) OSCAR_PV(7) }
+    }
 #undef OSCAR_PV
   }
-  const uint8_t* mz = sb + 1280 + 16 * (4 * (gid & 3) + tig);
+  // rows 0 .. NG-1: the value zeros of the groups; row 4: ones
+  const uint8_t* mz = sb + vbase + 16 * (4 * (gid & (NG - 1)) + tig);
   constexpr uint32_t kOnes = 0x3c003c00u;  // fp16 (1, 1)
-  const uint32_t za0 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 4) : (gid == 4 ? kOnes : 0u);
-  const uint32_t za2 = gid < 4 ? *reinterpret_cast<const uint32_t*>(mz + 12) : (gid == 4 ? kOnes : 0u);
+  const uint32_t za0 = gid < NG ? *reinterpret_cast<const uint32_t*>(mz + 4) : (gid == 4 ? kOnes : 0u);
+  const uint32_t za2 = gid < NG ? *reinterpret_cast<const uint32_t*>(mz + 12) : (gid == 4 ? kOnes : 0u);
   mma16816(oz, za0, 0u, za2, 0u, P01, P23);
 }
 
@@ -478,10 +504,12 @@ __device__ __forceinline__ uint32_t page_token_bits(bool ok, int pos, int lo, in
 // `valid` is clear (bit t: page A token t, bit 16 + t: page B token t); lane:
 // page lane / 16, 16-byte chunk c = 4 g + bb of the value metadata, whose 32-bit
 // word w holds tokens 8 (w / 2) + 2 bb and + 1 (scales for even w, zeros for odd)
+template <int NG>
 __device__ __forceinline__ void zero_masked_value_meta(uint8_t* sbA, uint8_t* sbB, uint32_t valid, int lane) {
   const int c = lane & 15;
+  if (c >= 4 * NG) return;  // NG groups: 4 NG chunks
   const uint32_t vpage = (lane >> 4) ? (valid >> 16) : (valid & 0xffffu);
-  uint4* chunk = reinterpret_cast<uint4*>(((lane >> 4) ? sbB : sbA) + 1280 + 16 * c);
+  uint4* chunk = reinterpret_cast<uint4*>(((lane >> 4) ? sbB : sbA) + vscale_off(NG, 0, 0) + 16 * c);
   uint32_t keep[4];
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
@@ -496,6 +524,7 @@ __device__ __forceinline__ void zero_masked_value_meta(uint8_t* sbA, uint8_t* sb
   *chunk = x;
 }
 
+template <int NG>
 __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -524,10 +553,13 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   uint32_t zqb;
   {
     const uint2 zq = reinterpret_cast<const uint2*>(rec + 1024)[lane];
-    const int src = (lane & ~3) | (tig & 1);
+    const int src = NG == kGroups ? (lane & ~3) | (tig & 1) : lane & ~3;
     const uint32_t zx = __shfl_sync(0xffffffffu, zq.x, src);
     const uint32_t zy = __shfl_sync(0xffffffffu, zq.y, src);
-    zqb = tig < 2 ? zx : zy;
+    if constexpr (NG == kGroups)
+      zqb = tig < 2 ? zx : zy;
+    else
+      zqb = tig == 0 ? zx : (tig == 1 ? zy : 0u);
   }
   const float uscale = __uint_as_float(rec[1088]);
   const float tau_u = kLazyLog2 / uscale;
@@ -539,8 +571,9 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
 
   uint8_t* sbuf = smem + warp * kStages * kBlockBytes;
   const int32_t* ptrow = p.page_table + (size_t)b * p.pt_stride + pbeg + warp;
-  const uint8_t* pool_h = p.pool + (size_t)h * kBlockBytes + lane * 16;
-  const size_t page_stride = (size_t)p.num_kv_heads * kBlockBytes;
+  constexpr int kBB = block_bytes(NG);
+  const uint8_t* pool_h = p.pool + (size_t)h * kBB + lane * 16;
+  const size_t page_stride = (size_t)p.num_kv_heads * kBB;
   unsigned valid_bits = 0;  // bit (j % kStages): page j of this warp has a valid id
 
   // page ids of this warp's first 64 pages, two per lane, loaded once together with
@@ -574,7 +607,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
       uint8_t* dst = sbuf + sl * kBlockBytes + lane * 16;
       cp_async16(dst, src);
       cp_async16(dst + 512, src + 512);
-      cp_async16(dst + 1024, src + 1024);
+      if (NG == kGroups || lane < 16) cp_async16(dst + 1024, src + 1024);  // metadata: 128 NG bytes
     }
   };
 
@@ -615,7 +648,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     const bool full = okA && okB && posA >= lo && posA + kPage <= hi && posB >= lo && posB + kPage <= hi;
 
     float u[8];
-    pair_scores(sbA, sbB, qs, zqb, lane, u);
+    pair_scores<NG>(sbA, sbB, qs, zqb, lane, u);
     if (!full) {
       // tokens outside [lo, hi), on a page with a bad id or on a missing second
       // page: scores -inf, and their value scales and zeros set to 0 in shared
@@ -632,7 +665,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
       u[5] = b0v ? u[5] : -INFINITY;
       u[6] = b1v ? u[6] : -INFINITY;
       u[7] = b1v ? u[7] : -INFINITY;
-      zero_masked_value_meta(sbA, sbB, valid, lane);
+      zero_masked_value_meta<NG>(sbA, sbB, valid, lane);
       __syncwarp();
     }
 
@@ -677,8 +710,8 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
     const uint32_t PB01 = transpose8x8(f2_to_h2_bits(pr[4], pr[5]));
     const uint32_t PB23 = transpose8x8(f2_to_h2_bits(pr[6], pr[7]));
-    page_values(sbA, lane, PA01, PA23, acc, oz);
-    page_values(sbB, lane, PB01, PB23, acc, oz);
+    page_values<NG>(sbA, lane, PA01, PA23, acc, oz);
+    page_values<NG>(sbB, lane, PB01, PB23, acc, oz);
     }
     __syncwarp();
     if (j + kStages < nmine) issue(j + kStages, SA);
@@ -707,7 +740,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   }
 #pragma unroll
   for (int cb = 0; cb < 8; ++cb) {
-    const int gq = cb >> 1;
+    const int gq = cb / (8 / NG);
     const float ze = __shfl_sync(0xffffffffu, oz[0], 4 * gq + tig) * inv_ps;
     const float zo = __shfl_sync(0xffffffffu, oz[1], 4 * gq + tig) * inv_ps;
     const float sc = 16777216.f / slot_factor(cb) * inv_ps;
@@ -746,6 +779,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   }
 }
 
+template <int NG>
 __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_wait();  // cache, state and q~ come from earlier kernels
@@ -754,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
   if (x < p.win_slots)
     window_attention(p, b, h, x, smem);
   else
-    int2_attention(p, b, h, x - p.win_slots, smem);
+    int2_attention<NG>(p, b, h, x - p.win_slots, smem);
 }
 
 // --------------------------------------------------------------------------
@@ -864,7 +898,10 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
   static bool attr_set = false;
   const int smem = decode_smem_bytes();
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(oscar_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(oscar_decode_kernel<kGroups>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(oscar_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(oscar_rotate_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmem);
     if (e == cudaSuccess)
@@ -877,7 +914,8 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
                              s, p);
   if (e == cudaSuccess && ev_before) e = cudaEventRecord(ev_before, s);
   if (e == cudaSuccess)
-    e = launch_pdl(oscar_decode_kernel, dim3(p.win_slots + p.splits, p.num_kv_heads, batch), dim3(kThreads),
+    e = launch_pdl(p.ngroups == kGroups ? oscar_decode_kernel<kGroups> : oscar_decode_kernel<2>,
+                   dim3(p.win_slots + p.splits, p.num_kv_heads, batch), dim3(kThreads),
                    smem, s, p);
   if (e == cudaSuccess && ev_after) e = cudaEventRecord(ev_after, s);
   if (e == cudaSuccess)

@@ -152,6 +152,7 @@ extern "C" int oscar_decode_attn_noalloc(const oscar_config* cfg, const void* q,
   p.num_kv_heads = hkv;
   p.gqa = g;
   p.sink = cfg->sink;
+  p.ngroups = kHeadDim / cfg->group_size;
   p.recent = cfg->recent;
   p.splits = splits;
   p.fold_rv = cfg->fold_rv;

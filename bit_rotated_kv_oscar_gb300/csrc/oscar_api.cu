@@ -65,8 +65,8 @@ int check_config_msg(const oscar_config* c, std::string* msg) {
            "finite softmax_scale >= 0 required";
     return OSCAR_ERR_INVALID_ARG;
   }
-  if (c->head_dim != kHeadDim || c->page_size != kPage || c->group_size != kGroup) {
-    *msg = "only head_dim 128, page_size 16, group_size 32 are built";
+  if (c->head_dim != kHeadDim || c->page_size != kPage || (c->group_size != 32 && c->group_size != 64)) {
+    *msg = "only head_dim 128, page_size 16, group_size 32 or 64 are built";
     return OSCAR_ERR_UNSUPPORTED;
   }
   const int g = c->num_q_heads / c->num_kv_heads;
@@ -174,7 +174,7 @@ int oscar_cache_bytes(const oscar_config* cfg, int64_t num_pages, size_t* pool_b
   int st = check_config_msg(cfg, &msg);
   if (st) return st;
   if (num_pages < 0 || !pool_bytes || !window_bytes) return OSCAR_ERR_INVALID_ARG;
-  *pool_bytes = (size_t)num_pages * cfg->num_kv_heads * kBlockBytes;
+  *pool_bytes = (size_t)num_pages * cfg->num_kv_heads * block_bytes(kHeadDim / cfg->group_size);
   *window_bytes = (size_t)cfg->max_batch * cfg->num_kv_heads * 2 * (cfg->sink + cfg->recent) *
                   kHeadDim * sizeof(__nv_bfloat16);
   return OSCAR_OK;
@@ -329,6 +329,7 @@ static int append_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_stat
   p.clip_V = ctx->clip_V;
   p.num_kv_heads = ctx->cfg.num_kv_heads;
   p.sink = ctx->cfg.sink;
+  p.ngroups = kHeadDim / ctx->cfg.group_size;
   p.recent = ctx->cfg.recent;
   p.n_new = n_new;
   p.batch = batch;
@@ -355,6 +356,7 @@ static int append_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_stat
     pp.clip_V = ctx->clip_V;
     pp.num_kv_heads = ctx->cfg.num_kv_heads;
     pp.sink = ctx->cfg.sink;
+    pp.ngroups = kHeadDim / ctx->cfg.group_size;
     pp.recent = ctx->cfg.recent;
     pp.n_new = n_new;
     pp.batch = batch;
@@ -427,6 +429,7 @@ static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table,
   p.num_kv_heads = ctx->cfg.num_kv_heads;
   p.gqa = ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads;
   p.sink = ctx->cfg.sink;
+  p.ngroups = kHeadDim / ctx->cfg.group_size;
   p.recent = ctx->cfg.recent;
   p.splits = auto_splits(ctx, batch);
   p.win_slots = win_slots(&ctx->cfg);

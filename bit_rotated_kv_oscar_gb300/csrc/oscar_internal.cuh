@@ -20,9 +20,22 @@ __host__ __device__ __forceinline__ bool state_ok(const oscar_seq_state& st, int
 
 constexpr int kHeadDim = 128;
 constexpr int kPage = 16;
-constexpr int kGroup = 32;
-constexpr int kGroups = kHeadDim / kGroup;   // 4 quantisation groups per token
-constexpr int kBlockBytes = OSCAR_PAGE_BLOCK_BYTES;
+constexpr int kGroup = 32;                   // the default group size
+constexpr int kGroups = kHeadDim / kGroup;   // 4 quantisation groups per token (at most)
+constexpr int kBlockBytes = OSCAR_PAGE_BLOCK_BYTES;   // block of the default group size (the largest)
+
+// Page block of a group size with ng = 128 / group_size groups per token: codes
+// as for every group size, then the fp16 metadata (see include/oscar.h).
+__host__ __device__ constexpr int block_bytes(int ng) { return 1024 + 128 * ng; }
+__host__ __device__ constexpr int kscale_off(int ng, int t, int gq) {
+  return 1024 + 8 * ng * ((t & 7) >> 1) + 8 * gq + 4 * (t >> 3) + 2 * (t & 1);
+}
+__host__ __device__ constexpr int kzero_off(int ng, int t, int gq) { return 1024 + 32 * ng + 2 * ng * t + 2 * gq; }
+__host__ __device__ constexpr int vscale_off(int ng, int t, int gq) {
+  return 1024 + 64 * ng + 16 * (4 * gq + ((t & 7) >> 1)) + 8 * (t >> 3) + 2 * (t & 1);
+}
+static_assert(block_bytes(kGroups) == kBlockBytes, "the default block size");
+static_assert(block_bytes(2) == OSCAR_PAGE_BLOCK_BYTES_FOR(64), "the group-64 block size");
 constexpr int kMaxGqa = 8;
 // per-(request, KV head) record written by the query-rotation kernel:
 // [0, 1024) fp16x2 mma column fragments of q~ (hi, lo), [1024, 1088) fragments of
@@ -52,6 +65,7 @@ struct AppendParams {
   const float* clip_K;      // [Hkv]
   const float* clip_V;
   int32_t num_kv_heads, sink, recent, n_new, batch, max_batch;
+  int32_t ngroups;          // quantisation groups per token: 128 / group_size (4 or 2)
   int32_t fold_rv;          // 1: V arrives already rotated (R_V folded into the projection)
   float* trace;             // optional [B][trace_positions][Hkv][2][128]
   int32_t trace_positions;
@@ -79,6 +93,7 @@ struct PrefillParams {
   const float* clip_K;
   const float* clip_V;
   int32_t num_kv_heads, sink, recent, n_new, batch, max_batch;
+  int32_t ngroups;          // quantisation groups per token: 128 / group_size (4 or 2)
   float* trace;
   int32_t trace_positions;
   uint32_t* err_flags;
@@ -100,6 +115,7 @@ struct DecodeParams {
   const float* pv_scale;    // [Hkv] power of two applied to p * s_v before fp16 rounding
   int32_t num_q_heads, num_kv_heads, gqa, sink, recent, splits, fold_rv, max_batch;
   int32_t win_slots;        // CTAs over the BF16 window, 64 tokens each
+  int32_t ngroups;          // quantisation groups per token: 128 / group_size (4 or 2)
   float scale_log2;         // softmax_scale * log2(e)
   uint32_t* err_flags;
 };

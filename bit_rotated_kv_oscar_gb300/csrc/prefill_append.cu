@@ -105,28 +105,43 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 // so the low 16 bits are exactly the packed codes.
 constexpr float kMagic = 12582912.f;        // 1.5 * 2^23
 
-template <int GQ>
-__device__ __forceinline__ void group_quantise(const uint32_t (&r)[32], float clip, __half& s16, __half& z16,
-                                               uint32_t (&acc)[16]) {
-  float mn = __uint_as_float(r[0]), mx = mn;
+__device__ __forceinline__ void chunk_minmax(const uint32_t (&r)[32], float& mn, float& mx) {
 #pragma unroll
-  for (int i = 1; i < 32; ++i) {
+  for (int i = 0; i < 32; ++i) {
     mn = fminf(mn, __uint_as_float(r[i]));
     mx = fmaxf(mx, __uint_as_float(r[i]));
   }
+}
+
+// scale and zero of a group from the minimum and maximum of its rotated values
+// (clipping is monotonic, so the clipped extremes are the clipped minimum and
+// maximum), and the bounds the codes of the group's values are clamped to
+struct GroupQ {
+  __half s16, z16;
+  float zf, rsf, lo, hi;
+};
+__device__ __forceinline__ GroupQ group_params(float mn, float mx, float clip) {
+  GroupQ q;
   mn = fminf(fmaxf(mn, -clip), clip);
   mx = fminf(fmaxf(mx, -clip), clip);
-  s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-  z16 = __float2half_rn(mn);
-  const float sf = __half2float(s16), zf = __half2float(z16);
-  const float rsf = sf != 0.f ? __frcp_rn(sf) : 0.f;  // sf == 0: every code is 0
-  const float lo = fminf(fmaxf(__fadd_rn(__fmul_rn(__fsub_rn(mn, zf), rsf), kMagic), kMagic), kMagic + 3.f);
-  const float hi = fminf(fmaxf(__fadd_rn(__fmul_rn(__fsub_rn(mx, zf), rsf), kMagic), kMagic), kMagic + 3.f);
+  q.s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+  q.z16 = __float2half_rn(mn);
+  const float sf = __half2float(q.s16);
+  q.zf = __half2float(q.z16);
+  q.rsf = sf != 0.f ? __frcp_rn(sf) : 0.f;  // sf == 0: every code is 0
+  q.lo = fminf(fmaxf(__fadd_rn(__fmul_rn(__fsub_rn(mn, q.zf), q.rsf), kMagic), kMagic), kMagic + 3.f);
+  q.hi = fminf(fmaxf(__fadd_rn(__fmul_rn(__fsub_rn(mx, q.zf), q.rsf), kMagic), kMagic), kMagic + 3.f);
+  return q;
+}
+
+// codes of the 32 channels 32 CH .. 32 CH + 31 into the packed half-words
+template <int CH>
+__device__ __forceinline__ void chunk_codes(const uint32_t (&r)[32], const GroupQ& q, uint32_t (&acc)[16]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    float m = __fadd_rn(__fmul_rn(__fsub_rn(__uint_as_float(r[i]), zf), rsf), kMagic);
-    m = fminf(fmaxf(m, lo), hi);
-    constexpr int kCh0 = 32 * GQ;
+    float m = __fadd_rn(__fmul_rn(__fsub_rn(__uint_as_float(r[i]), q.zf), q.rsf), kMagic);
+    m = fminf(fmaxf(m, q.lo), q.hi);
+    constexpr int kCh0 = 32 * CH;
     const int ch = kCh0 + i;                            // compile-time
     const int si = ch >> 4, rr = ch & 15;
     acc[2 * (rr & 7) + (rr >> 3)] += __float_as_uint(m) << (2 * si);
@@ -142,7 +157,7 @@ __device__ __forceinline__ uint8_t* token_block(const PrefillParams& p, int64_t 
   if (!valid) return nullptr;
   const int64_t pidx = pos / kPage;
   const int32_t id = pidx < p.pt_stride ? p.page_table[(int64_t)b * p.pt_stride + pidx] : -1;
-  if (id >= 0 && id < p.num_pages) return p.pool + ((int64_t)id * p.num_kv_heads + h) * kBlockBytes;
+  if (id >= 0 && id < p.num_pages) return p.pool + ((int64_t)id * p.num_kv_heads + h) * block_bytes(p.ngroups);
   atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
   return nullptr;
 }
@@ -156,10 +171,11 @@ __device__ __forceinline__ void trace_group(const PrefillParams& p, const uint32
   }
 }
 
+// sz[g]: scale (low half) and zero (high half) of group g; ng groups per token
 __device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos, const uint32_t (&acc)[16],
-                                            const uint32_t (&sz)[kGroups]) {
+                                            const uint32_t (&sz)[kGroups], int ng) {
   const int t = (int)(pos % kPage);
-  const int a = t & 7, bb = (t & 7) >> 1, pair = t >> 3, th = t & 1, tt = t >> 3;
+  const int a = t & 7, bb = (t & 7) >> 1, th = t & 1, tt = t >> 3;
   if (kind == 0) {
     // codes: words (b2, x) at 16 (4 a + b2) + 4 (2 tt + x)
 #pragma unroll
@@ -168,10 +184,13 @@ __device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos,
           make_uint2(low_halves(acc[4 * b2], acc[4 * b2 + 2]), low_halves(acc[4 * b2 + 1], acc[4 * b2 + 3]));
 #pragma unroll
     for (int g = 0; g < kGroups; ++g)
-      *reinterpret_cast<uint16_t*>(blk + 1024 + 32 * bb + 8 * g + 4 * pair + 2 * th) = (uint16_t)sz[g];
-    // zeros of the four groups are contiguous: 1152 + 8 t + 2 g
-    *reinterpret_cast<uint2*>(blk + 1152 + 8 * t) =
-        make_uint2(__byte_perm(sz[0], sz[1], 0x7632), __byte_perm(sz[2], sz[3], 0x7632));
+      if (g < ng) *reinterpret_cast<uint16_t*>(blk + kscale_off(ng, t, g)) = (uint16_t)sz[g];
+    // the zeros of a token are contiguous
+    if (ng == kGroups)
+      *reinterpret_cast<uint2*>(blk + kzero_off(ng, t, 0)) =
+          make_uint2(__byte_perm(sz[0], sz[1], 0x7632), __byte_perm(sz[2], sz[3], 0x7632));
+    else
+      *reinterpret_cast<uint32_t*>(blk + kzero_off(ng, t, 0)) = __byte_perm(sz[0], sz[1], 0x7632);
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -180,13 +199,17 @@ __device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos,
     }
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
-      uint8_t* m = blk + 1280 + 16 * (4 * g + bb) + 4 * (2 * pair) + 2 * th;
-      *reinterpret_cast<uint16_t*>(m) = (uint16_t)sz[g];
-      *reinterpret_cast<uint16_t*>(m + 4) = (uint16_t)(sz[g] >> 16);
+      if (g < ng) {
+        uint8_t* m = blk + vscale_off(ng, t, g);
+        *reinterpret_cast<uint16_t*>(m) = (uint16_t)sz[g];
+        *reinterpret_cast<uint16_t*>(m + 4) = (uint16_t)(sz[g] >> 16);
+      }
     }
   }
 }
 
+// NG: quantisation groups per token (p.ngroups), 4 (groups of 32) or 2 (of 64)
+template <int NG>
 __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t dsm_raw[];
   // 1024-byte alignment for the swizzled operands
@@ -335,27 +358,58 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
       for (int i = 0; i < 16; ++i) acc[i] = 0u;
       uint32_t sz[kGroups];   // scale (low half) and zero (high half) of each group
       uint32_t r[32];
-#pragma unroll
-      for (int gq = 0; gq < kGroups; ++gq) {
-        tmem_ld32(taddr + 32 * gq, r);
+      auto load_chunk = [&](int ch) {
+        tmem_ld32(taddr + 32 * ch, r);
         asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
         tmem_regs_ready(r);
-        if (gq == kGroups - 1) {
-          // every column is in registers: the accumulator may be overwritten
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&acce[g]));
+      };
+      auto release = [&]() {
+        // every column this thread needs is in registers: the accumulator may be overwritten
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&acce[g]));
+      };
+      if constexpr (NG == kGroups) {
+        // groups of 32 channels: one TMEM chunk each
+#pragma unroll
+        for (int gq = 0; gq < kGroups; ++gq) {
+          load_chunk(gq);
+          if (gq == kGroups - 1) release();
+          trace_group(p, r, pos, valid, h, b, kind, gq);
+          float mn = __uint_as_float(r[0]), mx = mn;
+          chunk_minmax(r, mn, mx);
+          const GroupQ q = group_params(mn, mx, clip);
+          if (gq == 0) chunk_codes<0>(r, q, acc);
+          if (gq == 1) chunk_codes<1>(r, q, acc);
+          if (gq == 2) chunk_codes<2>(r, q, acc);
+          if (gq == 3) chunk_codes<3>(r, q, acc);
+          sz[gq] = (uint32_t)__half_as_ushort(q.s16) | ((uint32_t)__half_as_ushort(q.z16) << 16);
         }
-        trace_group(p, r, pos, valid, h, b, kind, gq);
-        __half s16, z16;
-        if (gq == 0) group_quantise<0>(r, clip, s16, z16, acc);
-        if (gq == 1) group_quantise<1>(r, clip, s16, z16, acc);
-        if (gq == 2) group_quantise<2>(r, clip, s16, z16, acc);
-        if (gq == 3) group_quantise<3>(r, clip, s16, z16, acc);
-        sz[gq] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+      } else {
+        // groups of 64 channels: the extremes of both chunks first, then the codes
+        // of the second chunk (in registers) and of the first (read again)
+#pragma unroll
+        for (int gq = 0; gq < 2; ++gq) {
+          load_chunk(2 * gq);
+          trace_group(p, r, pos, valid, h, b, kind, 2 * gq);
+          float mn = __uint_as_float(r[0]), mx = mn;
+          chunk_minmax(r, mn, mx);
+          load_chunk(2 * gq + 1);
+          trace_group(p, r, pos, valid, h, b, kind, 2 * gq + 1);
+          chunk_minmax(r, mn, mx);
+          const GroupQ q = group_params(mn, mx, clip);
+          if (gq == 0) chunk_codes<1>(r, q, acc);
+          if (gq == 1) chunk_codes<3>(r, q, acc);
+          load_chunk(2 * gq);
+          if (gq == 1) release();
+          if (gq == 0) chunk_codes<0>(r, q, acc);
+          if (gq == 1) chunk_codes<2>(r, q, acc);
+          sz[gq] = (uint32_t)__half_as_ushort(q.s16) | ((uint32_t)__half_as_ushort(q.z16) << 16);
+        }
+        sz[2] = sz[3] = 0u;
       }
       uint8_t* blk = token_block(p, pos, valid, h, b);
-      if (blk) store_token(blk, kind, pos, acc, sz);
+      if (blk) store_token(blk, kind, pos, acc, sz, NG);
     }
   }
 
@@ -420,18 +474,21 @@ cudaError_t launch_prefill_append(const PrefillParams& p_in, int ctas_per_head, 
                                   cudaEvent_t ev_before, cudaEvent_t ev_after) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(oscar_prefill_append_kernel,
+    cudaError_t e = cudaFuncSetAttribute(oscar_prefill_append_kernel<kGroups>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(oscar_prefill_append_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  if (p_in.ngroups != kGroups && p_in.ngroups != 2) return cudaErrorInvalidValue;
   PrefillParams p = p_in;
   if (!encode_map(&p.tmap_k, p.k, p.num_kv_heads, p.n_new, p.batch) ||
       !encode_map(&p.tmap_v, p.v, p.num_kv_heads, p.n_new, p.batch))
     return cudaErrorInvalidValue;
   if (ev_before && cudaEventRecord(ev_before, s) != cudaSuccess) return cudaGetLastError();
-  cudaError_t e = launch_pdl(oscar_prefill_append_kernel, dim3(ctas_per_head, p.num_kv_heads, p.batch),
-                             dim3(kPfThreads), kPfSmem, s, p);
+  cudaError_t e = launch_pdl(p.ngroups == kGroups ? oscar_prefill_append_kernel<kGroups> : oscar_prefill_append_kernel<2>,
+                             dim3(ctas_per_head, p.num_kv_heads, p.batch), dim3(kPfThreads), kPfSmem, s, p);
   if (e != cudaSuccess) return e;
   if (ev_after && (e = cudaEventRecord(ev_after, s)) != cudaSuccess) return e;
   return cudaGetLastError();

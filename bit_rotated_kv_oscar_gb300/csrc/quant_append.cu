@@ -37,7 +37,7 @@ __device__ __forceinline__ uint8_t* block_of(const AppendParams& p, int32_t id, 
     atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
     return nullptr;
   }
-  return p.pool + ((int64_t)id * p.num_kv_heads + h) * kBlockBytes;
+  return p.pool + ((int64_t)id * p.num_kv_heads + h) * block_bytes(p.ngroups);
 }
 
 constexpr int kMaxTokensPerCta = 16;
@@ -63,6 +63,7 @@ oscar_quant_append_kernel(AppendParams p) {
   __shared__ float red[2][2][kHeadDim];        // partial dot products
   __shared__ uint8_t codes[2][kHeadDim];
   __shared__ __half meta[2][kGroups][2];
+  __shared__ float wmm[2][4][2];  // per kind and warp: min, max of its 32 clipped channels
 
   // the rotations are constant: stage them before waiting for earlier kernels
   {
@@ -168,16 +169,35 @@ oscar_quant_append_kernel(AppendParams p) {
           red[kind][half][c] = acc;
         }
         __syncthreads();
-        if ((tid & 255) < kHeadDim) {
-          const int kind = tid >> 8, c = tid & 127;
+        // thread (kind, c) < 128 per kind: clip, then the group minimum and maximum
+        // (a group of 32 channels is one warp; a group of 64 two warps, combined
+        // through shared memory)
+        const bool qthread = (tid & 255) < kHeadDim;
+        const int kind = tid >> 8, c = tid & 127;
+        float x = 0.f, mn = 0.f, mx = 0.f;
+        if (qthread) {
           const float x_rot = red[kind][0][c] + red[kind][1][c];
           if (p.trace && qpos < p.trace_positions) {
             p.trace[((((size_t)b * p.trace_positions + qpos) * Hkv + h) * 2 + kind) * kHeadDim + c] = x_rot;
           }
           const float clip = (kind ? p.clip_V : p.clip_K)[h];
-          const float x = fminf(fmaxf(x_rot, -clip), clip);
-          // one warp = one group of 32 channels
-          const float mn = warp_min(x), mx = warp_max(x);
+          x = fminf(fmaxf(x_rot, -clip), clip);
+          mn = warp_min(x);
+          mx = warp_max(x);
+          if (p.ngroups != kGroups && (c & 31) == 0) {
+            wmm[kind][c >> 5][0] = mn;
+            wmm[kind][c >> 5][1] = mx;
+          }
+        }
+        if (p.ngroups != kGroups) {
+          __syncthreads();
+          if (qthread) {
+            const int w = (c >> 5) ^ 1;  // the other warp of a 64-channel group
+            mn = fminf(mn, wmm[kind][w][0]);
+            mx = fmaxf(mx, wmm[kind][w][1]);
+          }
+        }
+        if (qthread) {
           const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
           const __half z16 = __float2half_rn(mn);
           const float sf = __half2float(s16), zf = __half2float(z16);
@@ -188,9 +208,10 @@ oscar_quant_append_kernel(AppendParams p) {
             code = (int)u;
           }
           codes[kind][c] = (uint8_t)code;
-          if ((c & 31) == 0) {
-            meta[kind][c >> 5][0] = s16;
-            meta[kind][c >> 5][1] = z16;
+          const int gsz = kHeadDim / p.ngroups;
+          if ((c & (gsz - 1)) == 0) {
+            meta[kind][c / gsz][0] = s16;
+            meta[kind][c / gsz][1] = z16;
           }
         }
         __syncthreads();
@@ -220,15 +241,16 @@ oscar_quant_append_kernel(AppendParams p) {
                 (uint16_t)hw;
           } else if (tid >= 64 && tid < 72) {
             // scale / zero of each group, K and V
-            const int u = tid - 64, kind = u >> 2, gq = u & 3;
-            const int bb = (t & 7) >> 1, pair = t >> 3, half = t & 1;
-            if (kind == 0) {
-              *reinterpret_cast<__half*>(blk + 1024 + 32 * bb + 8 * gq + 4 * pair + 2 * half) = meta[0][gq][0];
-              *reinterpret_cast<__half*>(blk + 1152 + 4 * (2 * t + (gq >> 1)) + 2 * (gq & 1)) = meta[0][gq][1];
-            } else {
-              uint8_t* m = blk + 1280 + 16 * (4 * gq + bb) + 4 * (2 * pair) + 2 * half;
-              *reinterpret_cast<__half*>(m) = meta[1][gq][0];
-              *reinterpret_cast<__half*>(m + 4) = meta[1][gq][1];
+            const int u = tid - 64, kind2 = u >> 2, gq = u & 3, ng = p.ngroups;
+            if (gq < ng) {
+              if (kind2 == 0) {
+                *reinterpret_cast<__half*>(blk + kscale_off(ng, t, gq)) = meta[0][gq][0];
+                *reinterpret_cast<__half*>(blk + kzero_off(ng, t, gq)) = meta[0][gq][1];
+              } else {
+                uint8_t* m = blk + vscale_off(ng, t, gq);
+                *reinterpret_cast<__half*>(m) = meta[1][gq][0];
+                *reinterpret_cast<__half*>(m + 4) = meta[1][gq][1];
+              }
             }
           }
         }

@@ -33,28 +33,31 @@
  *     allows early dependent launch must likewise do so only after its own
  *     prerequisites completed (the query rotation of oscar_decode_attn reads q
  *     as soon as it starts).
- *   - Supported shapes: head_dim 128, page_size 16, group_size 32, and a query
- *     group (num_q_heads / num_kv_heads) of 1, 2, 4 or 8. Anything else is
- *     OSCAR_ERR_UNSUPPORTED.
+ *   - Supported shapes: head_dim 128, page_size 16, group_size 32 or 64 (the
+ *     same for K and V), and a query group (num_q_heads / num_kv_heads) of 1,
+ *     2, 4 or 8. Anything else is OSCAR_ERR_UNSUPPORTED.
  *
  * Storage formats (owned by the library, allocated by the caller)
  *
- *   INT2 pool: num_pages * num_kv_heads blocks of 1536 bytes; the block of page
- *   id p and KV head h starts at byte (p * num_kv_heads + h) * 1536. A page
- *   holds 16 consecutive positions, slot t = position % 16. Codes and
- *   metadata of one token are spread over the block so that each lane of a
- *   warp reads the exact operand fragment it feeds to the tensor cores:
+ *   INT2 pool: num_pages * num_kv_heads blocks of BB = 1024 + 128 * NG bytes,
+ *   NG = 128 / group_size groups per token (BB = 1536 for group_size 32, 1280
+ *   for 64; OSCAR_PAGE_BLOCK_BYTES_FOR(group_size)); the block of page id p and
+ *   KV head h starts at byte (p * num_kv_heads + h) * BB. A page holds 16
+ *   consecutive positions, slot t = position % 16. Codes and metadata of one
+ *   token are spread over the block so that each lane of a warp reads the
+ *   exact operand fragment it feeds to the tensor cores:
  *     K code of slot t, channel c (2 bits, bytes [0, 512)):
  *       i = c/16, r = c%16, x = r/8, b = (r%8)/2, hi = r%2, a = t%8, th = t/8;
  *       32-bit little-endian word at byte 16*(4a+b) + 4*(2*th+x), bit 16*hi+2*i.
  *     V code of slot t, channel c (bytes [512, 1024)):
  *       i = c/16, r = c%16, x = r/8, a = r%8, tt = t/8, b = (t%8)/2, hi = t%2;
  *       word at byte 512 + 16*(4a+b) + 4*(2*tt+x), bit 16*hi+2*i.
- *     fp16 scale and zero of group gq (channels 32gq..32gq+31) of slot t, with
- *       b = (t%8)/2, pair = t/8, half = t%2 (bytes [1024, 1536)):
- *       K scale at byte 1024 + 32*b + 8*gq + 4*pair + 2*half;
- *       K zero  at byte 1152 + 4*(2*t + gq/2) + 2*(gq%2);
- *       V scale at byte 1280 + 16*(4*gq + b) + 4*(2*pair) + 2*half, V zero 4 bytes later.
+ *     fp16 scale and zero of group gq (channels group_size*gq ..) of slot t,
+ *       with b = (t%8)/2, pair = t/8, half = t%2 (bytes [1024, BB)):
+ *       K scale at byte 1024 + 8*NG*b + 8*gq + 4*pair + 2*half;
+ *       K zero  at byte 1024 + 32*NG + 2*NG*t + 2*gq;
+ *       V scale at byte 1024 + 64*NG + 16*(4*gq + b) + 4*(2*pair) + 2*half,
+ *       V zero 4 bytes later.
  *   Slots of positions outside [sink, int2_end) are never read.
  *
  *   Window: bf16 [max_batch][num_kv_heads][2 (K, V)][sink + recent][128],
@@ -85,7 +88,8 @@ extern "C" {
 #endif
 
 #define OSCAR_ABI_VERSION 1
-#define OSCAR_PAGE_BLOCK_BYTES 1536
+#define OSCAR_PAGE_BLOCK_BYTES 1536 /* group_size 32 */
+#define OSCAR_PAGE_BLOCK_BYTES_FOR(group_size) (1024 + 128 * (128 / (group_size)))
 
 typedef enum oscar_status {
   OSCAR_OK = 0,
@@ -107,7 +111,7 @@ typedef struct oscar_config {
   int32_t num_kv_heads;
   int32_t head_dim;          /* 128 */
   int32_t page_size;         /* 16 */
-  int32_t group_size;        /* 32: channels per quantisation group */
+  int32_t group_size;        /* 32 or 64: channels per quantisation group (K and V) */
   int32_t sink;              /* S >= 0: leading tokens kept in BF16 */
   int32_t recent;            /* W >= 1: trailing tokens kept in BF16 */
   int32_t max_batch;         /* requests per call, >= 1 */

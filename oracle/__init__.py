@@ -51,6 +51,7 @@ from .oscar_oracle import (  # noqa: F401
 )
 from .layout_codec import (  # noqa: F401
     PAGE_BLOCK_BYTES,
+    page_block_bytes,
     encode_page_block,
     decode_page_block,
     k_code_location,

@@ -140,14 +140,18 @@ def clip_threshold(rotated_abs: np.ndarray, percentile: float = 99.9) -> float:
 
 
 def calibrate(q_cal: np.ndarray, k_cal: np.ndarray, v_cal: np.ndarray,
-              percentile: float = 99.9, scale: float | None = None) -> dict:
+              percentile: float = 99.9, scale: float | None = None,
+              clip_percentile_k: float | None = None, clip_percentile_v: float | None = None) -> dict:
     """Offline calibration for one layer.
 
     q_cal [N, Hq, d], k_cal / v_cal [N, Hkv, d] (float). Per KV head h:
     C_Q is averaged over the h's query heads, C_S likewise; R_K = U_Q H P,
     R_V = U_S H P. One clip value per layer for K and one for V (percentile of
     |x @ R| over all calibration tokens, channels and KV heads), broadcast to
-    every head. Returns float64 arrays plus float32 copies for the device.
+    every head. clip_percentile_k / _v override the percentile for K / V: the
+    pages print typical clips "cK = 0.96, cV = 0.92" ([ES] "El sistema de
+    servicio"), read here as the 96th / 92nd percentiles for that preset.
+    Returns float64 arrays plus float32 copies for the device.
     """
     q_cal = np.asarray(q_cal, dtype=np.float64)
     k_cal = np.asarray(k_cal, dtype=np.float64)
@@ -170,8 +174,8 @@ def calibrate(q_cal: np.ndarray, k_cal: np.ndarray, v_cal: np.ndarray,
         r_v[h] = composite_rotation(eig_desc(c_s[h])[1])
     k_rot = np.einsum("nhi,hij->nhj", k_cal, r_k)
     v_rot = np.einsum("nhi,hij->nhj", v_cal, r_v)
-    clip_k = clip_threshold(np.abs(k_rot), percentile)
-    clip_v = clip_threshold(np.abs(v_rot), percentile)
+    clip_k = clip_threshold(np.abs(k_rot), percentile if clip_percentile_k is None else clip_percentile_k)
+    clip_v = clip_threshold(np.abs(v_rot), percentile if clip_percentile_v is None else clip_percentile_v)
     return {
         "R_K": r_k, "R_V": r_v, "C_Q": c_q, "C_S": c_s,
         "clip_K": np.full(hkv, clip_k), "clip_V": np.full(hkv, clip_v),

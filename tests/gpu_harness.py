@@ -73,16 +73,18 @@ class Layer:
 
     def __init__(self, hq, hkv, sink, recent, max_batch, max_tokens, seed=0, n_cal=512,
                  shuffled=True, fold_rv=0, num_splits=0, extra_pages=0, spikes=False,
-                 device="cuda"):
+                 device="cuda", group=32, clip_percentiles=(99.9, 99.9)):
         self.hq, self.hkv, self.sink, self.recent = hq, hkv, sink, recent
+        self.group = group
         self.seed, self.spikes, self.device = seed, spikes, device
         q_cal = draw_queries(seed, 900, n_cal, hq, hkv, D).numpy()
         k_cal, v_cal = (t.numpy() for t in draw_kv(seed, 900, n_cal, hkv, D, spikes))
-        self.cal = oracle.calibrate(q_cal, k_cal, v_cal)
+        self.cal = oracle.calibrate(q_cal, k_cal, v_cal, clip_percentile_k=clip_percentiles[0],
+                                    clip_percentile_v=clip_percentiles[1])
         self.fold_rv = fold_rv
         max_pages = (max_tokens + 15) // 16
         self.cfg = abi.make_config(hq, hkv, sink, recent, max_batch, max_pages, fold_rv=fold_rv,
-                                   num_splits=num_splits)
+                                   num_splits=num_splits, group_size=group)
         self.ctx = abi.Context(self.cfg)
         r_v = np.broadcast_to(np.eye(D, dtype=np.float32), (hkv, D, D)) if fold_rv else self.cal["R_V32"]
         self.r_v32 = np.ascontiguousarray(r_v)
@@ -149,7 +151,8 @@ class Layer:
     def oracle_cache(self, b):
         r_k = self.cal["R_K32"]
         return oracle.OracleCache(r_k, self.r_v32, self.cal["clip_K32"], self.cal["clip_V32"],
-                                  self.sink).build(self.k_host[b], self.v_host[b], self.len[b], self.e[b])
+                                  self.sink, self.group).build(self.k_host[b], self.v_host[b], self.len[b],
+                                                               self.e[b])
 
     def oracle_decode(self, q, b, resolve_ties=True):
         cache = self.oracle_cache_resolved(b) if resolve_ties else self.oracle_cache(b)
@@ -173,7 +176,7 @@ class Layer:
             x64 = np.einsum("nhi,hij->nhj", x, r)
             eps = ROT_REL * np.abs(x64).max(-1, keepdims=True)                 # [n, hkv, 1]
             codes, s16, z16 = resolve_group_ties(x64, clip, eps, dec[kind], dec[2 + 2 * kind],
-                                                 dec[3 + 2 * kind])
+                                                 dec[3 + 2 * kind], group=self.group)
             if kind == 0:
                 cache.k_codes, cache.k_scale, cache.k_zero = codes, s16, z16
             else:
@@ -184,8 +187,8 @@ class Layer:
         return self.cache.state.cpu().numpy()
 
     def blocks_of_pages(self, page_ids):
-        """Pool blocks of the given page ids as numpy [n, hkv, 1536]."""
-        pool = self.cache.pool.view(-1, self.hkv, abi.PAGE_BLOCK_BYTES)
+        """Pool blocks of the given page ids as numpy [n, hkv, block bytes]."""
+        pool = self.cache.pool.view(-1, self.hkv, abi.page_block_bytes(self.group))
         idx = torch.as_tensor(np.asarray(page_ids, dtype=np.int64), device=pool.device)
         return pool[idx].cpu().numpy()
 
@@ -194,7 +197,7 @@ class Layer:
         each [hi - lo, hkv, ...], read through the oracle's restatement of the layout."""
         pt = self.cache.page_table_host[b]
         n0, n1 = lo // 16, (hi - 1) // 16 + 1
-        dec = oracle.decode_page_block(self.blocks_of_pages(pt[n0:n1]))
+        dec = oracle.decode_page_block(self.blocks_of_pages(pt[n0:n1]), group=self.group)
         res = []
         for x in dec:
             x = np.moveaxis(x, 2, 1)

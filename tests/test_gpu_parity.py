@@ -68,21 +68,21 @@ def check_int2(layer, b, trace, lo=None, hi=None):
         assert np.all(err <= ROT_REL * np.abs(ref).max(-1)), float((err / np.abs(ref).max(-1)).max())
         codes, s16, z16 = dec[kind], dec[2 + 2 * kind], dec[3 + 2 * kind]
         # (1) the oracle quantises the GPU's rotated float32 values: bit-exact
-        oc, os_, oz = oracle.quantize_groups(got.astype(F32), clip.astype(F32))
+        oc, os_, oz = oracle.quantize_groups(got.astype(F32), clip.astype(F32), layer.group)
         assert np.array_equal(codes, oc)
         assert np.array_equal(s16.view(np.uint16), os_.view(np.uint16))
         assert np.array_equal(z16.view(np.uint16), oz.view(np.uint16))
         # (2) the oracle quantises its own rotation: equal away from rounding ties
-        ic, is_, iz = oracle.quantize_groups(ref.astype(F32), clip.astype(F32))
+        ic, is_, iz = oracle.quantize_groups(ref.astype(F32), clip.astype(F32), layer.group)
         mism = ic != codes
         assert mism.mean() < 1e-3, mism.mean()
         if mism.any():
-            sf = np.repeat(is_.astype(np.float64), 32, axis=-1)
-            zf = np.repeat(iz.astype(np.float64), 32, axis=-1)
+            sf = np.repeat(is_.astype(np.float64), layer.group, axis=-1)
+            zf = np.repeat(iz.astype(np.float64), layer.group, axis=-1)
             xc = np.clip(ref.astype(F32), -clip, clip).astype(np.float64)
             u = (xc - zf) / np.where(sf == 0, 1, sf)
-            same_meta = (np.repeat(is_, 32, -1) == np.repeat(os_, 32, -1)) & \
-                        (np.repeat(iz, 32, -1) == np.repeat(oz, 32, -1))
+            same_meta = (np.repeat(is_, layer.group, -1) == np.repeat(os_, layer.group, -1)) & \
+                        (np.repeat(iz, layer.group, -1) == np.repeat(oz, layer.group, -1))
             tie = np.abs(u - np.floor(u) - 0.5) < 1e-3
             assert np.all(tie[mism & same_meta]), "code mismatch away from a rounding tie"
 
