@@ -174,12 +174,13 @@ class Workload:
         # offline calibration on 2048 synthetic calibration tokens
         q_cal = draw_queries(seed, 900, spec.calib_tokens, hq, hkv, D).numpy()
         k_cal, v_cal = (t.numpy() for t in draw_kv(seed, 900, spec.calib_tokens, hkv, D, spec.token_spikes))
-        cal = calibrate(q_cal, k_cal, v_cal)
-        self.cfg = abi.make_config(hq, hkv, S, W, B, max_pages)
+        cal = calibrate(q_cal, k_cal, v_cal, clip_percentile_k=spec.clip_percentile_k,
+                        clip_percentile_v=spec.clip_percentile_v)
+        self.cfg = abi.make_config(hq, hkv, S, W, B, max_pages, group_size=spec.group_size)
         num_pages = B * max_pages
         # cache bytes of one layer at the starting lengths
         int2_tok = np.maximum(self.lengths - W, S) - S
-        per_layer = int(hkv * 96 * int2_tok.sum())
+        per_layer = int(hkv * spec.int2_token_bytes * int2_tok.sum())
         l2 = torch.cuda.get_device_properties(device).L2_cache_size
         n_layers = 1 if per_layer > 4 * l2 else int(math.ceil(4 * l2 / max(per_layer, 1)))
         if min_layers:
@@ -224,13 +225,16 @@ class Workload:
                               v.to(torch.bfloat16).contiguous(), 1, n)
             pos += n
         torch.cuda.synchronize()
-        pool0 = c0.pool.view(-1, hkv, 1536)
+        from bit_rotated_kv_oscar_gb300 import abi
+
+        bb = abi.page_block_bytes(spec.group_size)
+        pool0 = c0.pool.view(-1, hkv, bb)
         win0 = c0.window.view(B, hkv, 2, spec.sink + spec.recent, D)
         st0 = c0.state[b0].clone()
         S, W = spec.sink, spec.recent
         src_pages = torch.as_tensor(c0.page_table_host[b0].astype(np.int64), device=self.device)
         for li, (ctx, cache) in enumerate(self.layers):
-            pool = cache.pool.view(-1, hkv, 1536)
+            pool = cache.pool.view(-1, hkv, bb)
             win = cache.window.view(B, hkv, 2, S + W, D)
             for b in range(B):
                 if li == 0 and b == b0:
@@ -252,15 +256,16 @@ class Workload:
         n_int2 = E - s.sink
         n_bf16 = np.minimum(L, s.sink) + (L - E)
         pages = (E + 15) // 16
-        b = s.num_kv_heads * (96 * n_int2 + 512 * n_bf16) + 4 * pages
+        b = s.num_kv_heads * (s.int2_token_bytes * n_int2 + 512 * n_bf16) + 4 * pages
         return float(b.sum() + self.B * s.num_q_heads * D * (2 + 4))
 
     def append_bytes(self):
         """Algorithmic HBM bytes of one single-token quant_append for the batch:
         read the new K/V (512 B per head), read the evicted ring token (512 B),
-        write its INT2 codes + metadata (96 B) and the new ring row (512 B)."""
+        write its INT2 codes + metadata (96 B for groups of 32) and the new ring
+        row (512 B)."""
         s = self.spec
-        return float(self.B * s.num_kv_heads * (512 + 512 + 96 + 512))
+        return float(self.B * s.num_kv_heads * (512 + 512 + s.int2_token_bytes + 512))
 
     def decode_only(self, i, stream):
         ctx, cache = self.layers[i % len(self.layers)]
@@ -460,7 +465,8 @@ def run_prefill(args, device, rank, dist):
     pre_us = float(np.mean(times)) * 1000.0
     pre_kernel_us = float(np.mean(ktimes)) * 1000.0
     n_int2 = max(n - W, S) - S
-    pre_bytes = float(n * hkv * 2 * D * 2 + n_int2 * hkv * 96 + (S + W) * hkv * 2 * D * 2)
+    tb = spec.int2_token_bytes
+    pre_bytes = float(n * hkv * 2 * D * 2 + n_int2 * hkv * tb + (S + W) * hkv * 2 * D * 2)
     # 16 forks at 65536 tokens with private suffixes
     for r in range(1, nreq + 1):
         cache.fork(0, r, fork)
@@ -491,12 +497,12 @@ def run_prefill(args, device, rank, dist):
     dec_us = e0.elapsed_time(e1) * 1000.0 / args.steps
     L = fork + suf
     E = L - W
-    logical = float(nreq * (hkv * (96 * (E - S) + 512 * (S + W)) + 4 * ((E + 15) // 16)) + nreq * hq * D * 6)
-    unique = float(hkv * 96 * (fork - S) + nreq * hkv * (96 * (E - fork) + 512 * (S + W)) + nreq * hq * D * 6)
+    logical = float(nreq * (hkv * (tb * (E - S) + 512 * (S + W)) + 4 * ((E + 15) // 16)) + nreq * hq * D * 6)
+    unique = float(hkv * tb * (fork - S) + nreq * hkv * (tb * (E - fork) + 512 * (S + W)) + nreq * hq * D * 6)
     pre_us, pre_kernel_us, dec_us = max_over_ranks([pre_us, pre_kernel_us, dec_us], dist, device)
     # the tensor-core kernel's share of the bytes: the K / V of the tokens going
     # straight to INT2 and their codes + metadata
-    pre_kernel_bytes = float(n_int2 * hkv * (2 * D * 2 + 96))
+    pre_kernel_bytes = float(n_int2 * hkv * (2 * D * 2 + tb))
     return {"prefill_tokens": n, "prefill_us": pre_us, "prefill_bytes": pre_bytes,
             "prefill_kernel_us": pre_kernel_us, "prefill_kernel_bytes": pre_kernel_bytes,
             "prefix_decode_us": dec_us, "prefix_logical_bytes": logical, "prefix_unique_bytes": unique}
@@ -509,12 +515,16 @@ def footprint(name):
     bf16 = s.batch * L * s.num_kv_heads * 2 * D * 2
     n_int2 = max(L - s.recent, s.sink) - s.sink
     pages = (L + 15) // 16
-    oscar = s.batch * (pages * s.num_kv_heads * 1536 + (s.sink + s.recent) * s.num_kv_heads * 2 * D * 2)
+    block = 1024 + 128 * (D // s.group_size)   # one (page, KV head) block, include/oscar.h
+    oscar = s.batch * (pages * s.num_kv_heads * block + (s.sink + s.recent) * s.num_kv_heads * 2 * D * 2)
     bits = {}
     for g in (32, 64, 128):
         bits["G%d_bits_per_int2_element" % g] = 2 + 32 / g
-    return {"workload": name, "bf16_bytes": bf16, "oscar_bytes": oscar, "ratio": round(bf16 / oscar, 3),
-            "int2_tokens_per_request": n_int2, **bits}
+    # stored bits per cached element (K and V, INT2 pages and the BF16 window)
+    stored = 8.0 * oscar / (s.batch * L * s.num_kv_heads * 2 * D)
+    return {"workload": name, "group": s.group_size, "sink": s.sink, "recent": s.recent,
+            "bf16_bytes": bf16, "oscar_bytes": oscar, "ratio": round(bf16 / oscar, 3),
+            "stored_bits_per_element": round(stored, 3), "int2_tokens_per_request": n_int2, **bits}
 
 
 # ---------------------------------------------------------------------------
@@ -583,7 +593,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="oscar", choices=["oscar", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_bs1_32k")
-    ap.add_argument("--extra", default="qwen3_32b_bs28_100k,qwen3_8b_bs16_ragged",
+    ap.add_argument("--extra", default="qwen3_32b_bs28_100k,qwen3_8b_bs16_ragged,qwen3_32b_bs28_100k_pages",
                     help="further decode workloads, comma separated ('' to skip)")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill / prefix-sharing measurement")
     ap.add_argument("--prefill-only", action="store_true",
@@ -640,7 +650,8 @@ def main():
 
     def roof(r):
         # the dominant kernel: split-K attention over the paged cache; algorithmic
-        # bytes = INT2 codes + metadata (96 B per token and KV head), the BF16 window
+        # bytes = INT2 codes + metadata (96 B per token and KV head for groups of 32,
+        # 80 B for groups of 64), the BF16 window
         # (512 B per token and KV head) and the page table (4 B per page)
         achieved = r["kernel_bytes"] / (r["kernel_us"] * 1e-6) / 1e9
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -671,8 +682,10 @@ def main():
             "extra": [],
         }
         for r in extras:
+            es = WORKLOADS[r["workload"]]
             out["extra"].append({
-                "workload": r["workload"], "us_per_step": round(r["us_per_step"], 3),
+                "workload": r["workload"], "group": es.group_size, "sink": es.sink, "recent": es.recent,
+                "us_per_step": round(r["us_per_step"], 3),
                 "decode_us": round(r["decode_us"], 3), "append_us": round(r["append_us"], 3),
                 "decode_gbs": round(r["decode_bytes"] / (r["decode_us"] * 1e-6) / 1e9, 1),
                 "roofline": roof(r), "clocks": r["clocks"], "layers_cycled": r["layers_cycled"],
@@ -695,7 +708,8 @@ def main():
                 "prefix16_unique_bytes": pre["prefix_unique_bytes"],
                 "prefix16_logical_bytes": pre["prefix_logical_bytes"],
             }
-        out["footprint"] = [footprint("qwen3_32b_bs28_100k"), footprint("qwen3_8b_bs1_32k")]
+        out["footprint"] = [footprint(n) for n in ("qwen3_32b_bs28_100k", "qwen3_8b_bs1_32k",
+                                                   "qwen3_32b_bs28_100k_pages", "qwen3_8b_bs1_32k_pages")]
         print(json.dumps(out))
     if dist:
         dist.destroy_process_group()

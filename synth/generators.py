@@ -51,6 +51,14 @@ class WorkloadSpec:
     decode_steps: int = 1
     prefix_shared: int = 0  # tokens of a shared prefix (prefix-sharing workload)
     suffix: int = 0         # private tokens per request after the shared prefix
+    clip_percentile_k: float = 99.9
+    clip_percentile_v: float = 99.9
+
+    @property
+    def int2_token_bytes(self) -> int:
+        """Bytes of one INT2 token of one KV head: K and V codes plus fp16
+        scale and zero per group."""
+        return 2 * (self.head_dim // 4) + 2 * (self.head_dim // self.group_size) * 4
 
     @property
     def gqa(self) -> int:
@@ -70,6 +78,14 @@ WORKLOADS = {
     # Qwen3-32B layer shape, 28 requests of 100000 tokens
     "qwen3_32b_bs28_100k": WorkloadSpec("qwen3_32b_bs28_100k", 64, 8, 128, 28, 100000, 100000,
                                         seed=3),
+    # the same two decode workloads with the pages' own constants: groups of 64
+    # channels, sink 64, recent window 256, clips at the 96th / 92nd percentile
+    "qwen3_8b_bs1_32k_pages": WorkloadSpec("qwen3_8b_bs1_32k_pages", 32, 8, 128, 1, 32768, 32768,
+                                           seed=1, decode_steps=100, group_size=64, sink=64, recent=256,
+                                           clip_percentile_k=96.0, clip_percentile_v=92.0),
+    "qwen3_32b_bs28_100k_pages": WorkloadSpec("qwen3_32b_bs28_100k_pages", 64, 8, 128, 28, 100000, 100000,
+                                              seed=3, group_size=64, sink=64, recent=256,
+                                              clip_percentile_k=96.0, clip_percentile_v=92.0),
     # 131072-token prefill, then 16 requests sharing its first 65536 tokens
     # through aliased pages, each with a private 4096-token suffix
     "prefill_128k_prefix16": WorkloadSpec("prefill_128k_prefix16", 32, 8, 128, 16, 131072, 131072,
