@@ -477,35 +477,44 @@ def run_prefill(args, device, rank, dist):
     ctx.quant_append(cache.page_table[1:], cache.state[1:], ks, vs, nreq, suf, stream)
     q = draw_queries(seed, 3, nreq, hq, hkv, D, device=device).to(torch.bfloat16).contiguous()
     o = torch.empty(nreq, hq, D, device=device)
-    for _ in range(max(3, args.warmup)):
-        ctx.decode_attn(q, cache.page_table[1:], cache.state[1:], o, nreq, stream)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(device)
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(g, stream=cap):
-            for _ in range(args.steps):
-                ctx.decode_attn(q, cache.page_table[1:], cache.state[1:], o, nreq, cap)
-    g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    dec_us = e0.elapsed_time(e1) * 1000.0 / args.steps
+    def graph_us(call):
+        """Mean duration of one call, timed over a CUDA graph of args.steps calls."""
+        for _ in range(max(3, args.warmup)):
+            call(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(args.steps):
+                    call(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000.0 / args.steps
+
+    # every fork reads the shared pages itself, then the shared range once per pack
+    dec_us = graph_us(lambda st: ctx.decode_attn(q, cache.page_table[1:], cache.state[1:], o, nreq, st))
+    shared_us = graph_us(lambda st: ctx.decode_attn_shared_prefix(q, cache.page_table[1:], cache.state[1:], fork,
+                                                                  o, nreq, st))
     L = fork + suf
     E = L - W
     logical = float(nreq * (hkv * (tb * (E - S) + 512 * (S + W)) + 4 * ((E + 15) // 16)) + nreq * hq * D * 6)
     unique = float(hkv * tb * (fork - S) + nreq * hkv * (tb * (E - fork) + 512 * (S + W)) + nreq * hq * D * 6)
-    pre_us, pre_kernel_us, dec_us = max_over_ranks([pre_us, pre_kernel_us, dec_us], dist, device)
+    pre_us, pre_kernel_us, dec_us, shared_us = max_over_ranks([pre_us, pre_kernel_us, dec_us, shared_us], dist,
+                                                              device)
     # the tensor-core kernel's share of the bytes: the K / V of the tokens going
     # straight to INT2 and their codes + metadata
     pre_kernel_bytes = float(n_int2 * hkv * (2 * D * 2 + tb))
     return {"prefill_tokens": n, "prefill_us": pre_us, "prefill_bytes": pre_bytes,
             "prefill_kernel_us": pre_kernel_us, "prefill_kernel_bytes": pre_kernel_bytes,
-            "prefix_decode_us": dec_us, "prefix_logical_bytes": logical, "prefix_unique_bytes": unique}
+            "prefix_decode_us": dec_us, "prefix_shared_decode_us": shared_us,
+            "prefix_logical_bytes": logical, "prefix_unique_bytes": unique}
 
 
 def footprint(name):
@@ -704,6 +713,7 @@ def main():
                              "launch_us": round(pre["prefill_kernel_us"], 2),
                              "algorithmic_bytes_per_launch": pre["prefill_kernel_bytes"]},
                 "prefix16_decode_us": round(pre["prefix_decode_us"], 2),
+                "prefix16_shared_prefix_decode_us": round(pre["prefix_shared_decode_us"], 2),
                 "prefix16_logical_gbs": round(pre["prefix_logical_bytes"] / (pre["prefix_decode_us"] * 1e-6) / 1e9, 1),
                 "prefix16_unique_bytes": pre["prefix_unique_bytes"],
                 "prefix16_logical_bytes": pre["prefix_logical_bytes"],

@@ -78,6 +78,7 @@ _SIGS = {
                                                  _P, ctypes.c_int32, _P]),
     "oscar_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P]),
     "oscar_decode_attn_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P]),
+    "oscar_decode_attn_shared_prefix": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P]),
     "oscar_quant_append_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32, _P,
                                                 _P, _P]),
     "oscar_decode_splits": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
@@ -231,6 +232,12 @@ class Context:
     def decode_attn(self, q, page_table, state, o, batch, stream=None):
         _check(lib().oscar_decode_attn(self.handle, _ptr(q), _ptr(page_table), _ptr(state), _ptr(o),
                                        batch, _stream(stream)), self.handle)
+
+    def decode_attn_shared_prefix(self, q, page_table, state, prefix_tokens, o, batch, stream=None):
+        """decode_attn for requests whose first prefix_tokens positions map to the
+        same pages: the shared range is read once per pack of requests."""
+        _check(lib().oscar_decode_attn_shared_prefix(self.handle, _ptr(q), _ptr(page_table), _ptr(state),
+                                                     prefix_tokens, _ptr(o), batch, _stream(stream)), self.handle)
 
     def decode_splits(self, batch):
         s = ctypes.c_int32()

@@ -259,7 +259,7 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
   __nv_bfloat16* vrows = krows + kWinChunk * kHeadDim;                        // [64][128]
   float* sc = reinterpret_cast<float*>(vrows + kWinChunk * kHeadDim);         // [8][64]
   float* stat = sc + kMaxGqa * kWinChunk;                                     // [8][2]
-  const int nslots = p.win_slots + p.splits;
+  const int nslots = p.win_slots + p.prefix_splits + p.splits;
   float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots + chunk) * g * kPartFloats;
 
   const oscar_seq_state st = p.state[b];
@@ -524,35 +524,54 @@ __device__ __forceinline__ void zero_masked_value_meta(uint8_t* sbA, uint8_t* sb
   *chunk = x;
 }
 
-template <int NG>
-__device__ void int2_attention(const DecodeParams& p, int b, int h, int split, uint8_t* smem) {
+// INT2 positions [lo, hi) of KV head h, the split-th of nsplits slices of its
+// pages, for nreq requests r0 .. r0 + nreq - 1 that share those pages (nreq > 1
+// only over a shared prefix): column n of the tensor-core products is head n % g
+// of request r0 + n / g. Page ids come from request r0's page-table row. okmask
+// bit r: request r0 + r is consistent (else its partial is left empty). The
+// result goes to partial slot `slot` of every request. PACK: nreq may exceed 1
+// (otherwise both columns of a lane belong to request r0 and share its scale).
+template <int NG, bool PACK>
+__device__ void int2_attention(const DecodeParams& p, int h, int split, int nsplits, int r0, int nreq,
+                               uint32_t okmask, int lo, int hi, int slot, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int g = p.gqa, S = p.sink, W = p.recent;
-  __shared__ uint4 qs[8 * 32];  // q~ fragments of this (request, KV head), shared by all warps
+  const int g = p.gqa;
+  __shared__ uint4 qs[8 * 32];  // q~ fragments of the packed requests, shared by all warps
 
-  const oscar_seq_state st = p.state[b];
-  const int L = st.seq_len, E = st.int2_end;
-  const bool ok = state_ok(st, S, W, p.max_batch);
-  const int lo = S, hi = min(E, L);
   int npages = 0, first = 0;
-  if (ok && hi > lo) {
+  if (okmask != 0u && hi > lo) {
     first = lo / kPage;
     npages = (hi - 1) / kPage - first + 1;
   }
-  const int chunk = (npages + p.splits - 1) / p.splits;
+  const int chunk = (npages + nsplits - 1) / nsplits;
   const int pbeg = first + split * chunk;
   const int pend = min(pbeg + chunk, first + npages);
   const int nmine = pend - pbeg - warp > 0 ? (pend - pbeg - warp + kWarps - 1) / kWarps : 0;
 
-  // query operand fragments (see oscar_rotate_q_kernel)
-  const uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
-  for (int i = tid; i < 8 * 32; i += kThreads) qs[i] = reinterpret_cast<const uint4*>(rec)[i];
+  // query operand fragments (see oscar_rotate_q_kernel): column n = gid of lane
+  // (gid, tig) takes the fragment of head gid % g of request r0 + gid / g
+  auto record = [&](int r) { return p.qrec + ((size_t)(r0 + r) * p.num_kv_heads + h) * kQrecWords; };
+  for (int i = tid; i < 8 * 32; i += kThreads) {
+    if constexpr (PACK) {
+      const int l = i & 31, cr = (l >> 2) / g;
+      qs[i] = cr < nreq ? reinterpret_cast<const uint4*>(record(cr))[(i & ~31) | (4 * ((l >> 2) % g) + (l & 3))]
+                        : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      qs[i] = reinterpret_cast<const uint4*>(record(0))[i];
+    }
+  }
   // zero-point column operand: k rows 2 tig, 2 tig + 1 of head gid = group sums of
   // q~ (hi for tig 0 / 1, lo for tig 2 / 3), taken from the record's row layout
   uint32_t zqb;
   {
-    const uint2 zq = reinterpret_cast<const uint2*>(rec + 1024)[lane];
+    uint2 zq;
+    if constexpr (PACK) {
+      const int cr = gid / g;
+      zq = cr < nreq ? reinterpret_cast<const uint2*>(record(cr) + 1024)[4 * (gid % g) + tig] : make_uint2(0u, 0u);
+    } else {
+      zq = reinterpret_cast<const uint2*>(record(0) + 1024)[lane];
+    }
     const int src = NG == kGroups ? (lane & ~3) | (tig & 1) : lane & ~3;
     const uint32_t zx = __shfl_sync(0xffffffffu, zq.x, src);
     const uint32_t zy = __shfl_sync(0xffffffffu, zq.y, src);
@@ -561,8 +580,12 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     else
       zqb = tig == 0 ? zx : (tig == 1 ? zy : 0u);
   }
-  const float uscale = __uint_as_float(rec[1088]);
-  const float tau_u = kLazyLog2 / uscale;
+  // score units of columns 2 tig (index 0) and 2 tig + 1 (index 1): each request
+  // has its own query operand scale
+  const int cr0 = PACK ? (2 * tig) / g : 0, cr1 = PACK ? (2 * tig + 1) / g : 0;
+  const float us0 = !PACK || cr0 < nreq ? __uint_as_float(record(cr0)[1088]) : 1.f;
+  const float us1 = PACK ? (cr1 < nreq ? __uint_as_float(record(cr1)[1088]) : 1.f) : us0;
+  const float tau0 = kLazyLog2 / us0, tau1 = PACK ? kLazyLog2 / us1 : tau0;
   // probabilities enter the value product as fp16 p * pscale with p <= 2^8 (lazy
   // maximum); pv_scale is the largest power of two keeping 2^8 * pv_scale * s_v
   // (s_v <= 2 clip_V / 3) below the fp16 maximum
@@ -570,7 +593,7 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   const float lg_ps = log2f(pscale);
 
   uint8_t* sbuf = smem + warp * kStages * kBlockBytes;
-  const int32_t* ptrow = p.page_table + (size_t)b * p.pt_stride + pbeg + warp;
+  const int32_t* ptrow = p.page_table + (size_t)r0 * p.pt_stride + pbeg + warp;
   constexpr int kBB = block_bytes(NG);
   const uint8_t* pool_h = p.pool + (size_t)h * kBB + lane * 16;
   const size_t page_stride = (size_t)p.num_kv_heads * kBB;
@@ -675,15 +698,15 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     // then is the maximum over the head's 16 lanes taken.
     float mx0 = fmaxf(fmaxf(u[0], u[2]), fmaxf(u[4], u[6]));
     float mx1 = fmaxf(fmaxf(u[1], u[3]), fmaxf(u[5], u[7]));
-    if (__any_sync(0xffffffffu, mx0 > m0 + tau_u || mx1 > m1 + tau_u)) {
+    if (__any_sync(0xffffffffu, mx0 > m0 + tau0 || mx1 > m1 + tau1)) {
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
       }
-      const bool bump0 = mx0 > m0 + tau_u, bump1 = mx1 > m1 + tau_u;
-      const float a0 = bump0 ? ex2((m0 - mx0) * uscale) : 1.f;
-      const float a1 = bump1 ? ex2((m1 - mx1) * uscale) : 1.f;
+      const bool bump0 = mx0 > m0 + tau0, bump1 = mx1 > m1 + tau1;
+      const float a0 = bump0 ? ex2((m0 - mx0) * us0) : 1.f;
+      const float a1 = bump1 ? ex2((m1 - mx1) * us1) : 1.f;
       m0 = bump0 ? mx0 : m0;
       m1 = bump1 ? mx1 : m1;
 #pragma unroll
@@ -701,10 +724,10 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     // every head sees the same tokens: the maximum stays -inf (warp-uniformly)
     // until a valid token has been seen, and pairs before that add nothing
     if (m0 != -INFINITY) {
-    const float nb0 = fmaf(-m0, uscale, lg_ps), nb1 = fmaf(-m1, uscale, lg_ps);
+    const float nb0 = fmaf(-m0, us0, lg_ps), nb1 = fmaf(-m1, us1, lg_ps);
     float pr[8];  // p * pscale, p <= 2^8
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], uscale, (i & 1) ? nb1 : nb0));
+    for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], (i & 1) ? us1 : us0, (i & 1) ? nb1 : nb0));
     // token-major probabilities -> the (token, head) column operand of P.V
     const uint32_t PA01 = transpose8x8(f2_to_h2_bits(pr[0], pr[1]));
     const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
@@ -733,9 +756,9 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
   float* wml = wpart + kWarps * kMaxGqa * kHeadDim;           // [8 warps][8 heads][2]
   if (gid == 4) {
     // oz row 4: the sums of the probabilities of heads 2 tig, 2 tig + 1
-    wml[(warp * kMaxGqa + 2 * tig) * 2] = m0 * uscale;          // log2 units
+    wml[(warp * kMaxGqa + 2 * tig) * 2] = m0 * us0;             // log2 units
     wml[(warp * kMaxGqa + 2 * tig) * 2 + 1] = oz[0] * inv_ps;
-    wml[(warp * kMaxGqa + 2 * tig + 1) * 2] = m1 * uscale;
+    wml[(warp * kMaxGqa + 2 * tig + 1) * 2] = m1 * us1;
     wml[(warp * kMaxGqa + 2 * tig + 1) * 2 + 1] = oz[1] * inv_ps;
   }
 #pragma unroll
@@ -753,27 +776,29 @@ __device__ void int2_attention(const DecodeParams& p, int b, int h, int split, u
     base[ho * kHeadDim + ch + 8] = fmaf(acc[cb][3], sc, zo);
   }
   __syncthreads();
-  float* part = p.part + (((size_t)b * p.num_kv_heads + h) * (p.win_slots + p.splits) + p.win_slots +
-                           split) * g * kPartFloats;
-  for (int i = tid; i < g * kHeadDim; i += kThreads) {
-    const int m = i / kHeadDim, c = i % kHeadDim;
+  const int nslots = p.win_slots + p.prefix_splits + p.splits;
+  for (int i = tid; i < (PACK ? nreq : 1) * g * kHeadDim; i += kThreads) {
+    const int n = i / kHeadDim, c = i % kHeadDim;  // column n: head n % g of request r0 + n / g
+    const int cr = PACK ? n / g : 0;
+    const bool okr = (okmask >> cr) & 1u;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * kMaxGqa + m) * 2]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * kMaxGqa + n) * 2]);
     float o = 0.f, l = 0.f;
-    if (M != -INFINITY) {
+    if (okr && M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float mw = wml[(w * kMaxGqa + m) * 2];
+        const float mw = wml[(w * kMaxGqa + n) * 2];
         const float sw = mw == -INFINITY ? 0.f : exp2f(mw - M);
-        o = fmaf(sw, wpart[(w * kMaxGqa + m) * kHeadDim + c], o);
-        l = fmaf(sw, wml[(w * kMaxGqa + m) * 2 + 1], l);
+        o = fmaf(sw, wpart[(w * kMaxGqa + n) * kHeadDim + c], o);
+        l = fmaf(sw, wml[(w * kMaxGqa + n) * 2 + 1], l);
       }
     }
-    float* dst = part + (size_t)m * kPartFloats;
+    float* dst = p.part + ((((size_t)(r0 + cr) * p.num_kv_heads + h) * nslots + slot) * g + (PACK ? n % g : n)) *
+                              kPartFloats;
     dst[c] = o;
     if (c == 0) {
-      dst[kHeadDim] = M;
+      dst[kHeadDim] = okr ? M : -INFINITY;
       dst[kHeadDim + 1] = l;
     }
   }
@@ -784,11 +809,32 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_wait();  // cache, state and q~ come from earlier kernels
   pdl_trigger();
-  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  if (x < p.win_slots)
-    window_attention(p, b, h, x, smem);
-  else
-    int2_attention<NG>(p, b, h, x - p.win_slots, smem);
+  const int x = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  const int S = p.sink, W = p.recent, P = p.prefix_tokens;
+  if (x < p.win_slots) {
+    window_attention(p, z, h, x, smem);
+  } else if (x < p.win_slots + p.prefix_splits) {
+    // the shared prefix [S, P) once for requests z pack .. z pack + pack - 1; every
+    // one of them must hold [S, P) in INT2
+    const int r0 = z * p.pack;
+    if (r0 >= p.batch) return;
+    const int nreq = min(p.pack, p.batch - r0);
+    uint32_t okmask = 0u;
+    for (int r = 0; r < nreq; ++r) {
+      const oscar_seq_state st = p.state[r0 + r];
+      const bool ok = state_ok(st, S, W, p.max_batch) && P <= min(st.int2_end, st.seq_len);
+      okmask |= (uint32_t)ok << r;
+    }
+    if (okmask != (1u << nreq) - 1u && threadIdx.x == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_STATE);
+    int2_attention<NG, true>(p, h, x - p.win_slots, p.prefix_splits, r0, nreq, okmask, S, P, x, smem);
+  } else {
+    // the request's own INT2 positions after the shared prefix
+    const oscar_seq_state st = p.state[z];
+    const bool ok = state_ok(st, S, W, p.max_batch);
+    const int lo = max(S, P), hi = min(st.int2_end, st.seq_len);
+    int2_attention<NG, false>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo, hi, x,
+                              smem);
+  }
 }
 
 // --------------------------------------------------------------------------
@@ -811,7 +857,7 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   __shared__ float lsum_s[2];
   const int h = blockIdx.x, b = blockIdx.y, m0 = 2 * blockIdx.z, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int g = p.gqa, nslots = p.win_slots + p.splits, nwin = p.win_slots;
+  const int g = p.gqa, nslots = p.win_slots + p.prefix_splits + p.splits, nwin = p.win_slots;
   const int nh = min(2, g - m0);
   if (!p.fold_rv) stage_matrix(RT, p.R_VT + (size_t)h * kHeadDim * kHeadDim, tid, kMergeThreads);
   else cp_commit();
@@ -909,13 +955,13 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (p.win_slots + p.splits > kMaxSlots) return cudaErrorInvalidValue;
+  if (p.win_slots + p.prefix_splits + p.splits > kMaxSlots) return cudaErrorInvalidValue;
   cudaError_t e = launch_pdl(oscar_rotate_q_kernel, dim3(p.num_kv_heads, batch), dim3(kRotThreads), kRotSmem,
                              s, p);
   if (e == cudaSuccess && ev_before) e = cudaEventRecord(ev_before, s);
   if (e == cudaSuccess)
     e = launch_pdl(p.ngroups == kGroups ? oscar_decode_kernel<kGroups> : oscar_decode_kernel<2>,
-                   dim3(p.win_slots + p.splits, p.num_kv_heads, batch), dim3(kThreads),
+                   dim3(p.win_slots + p.prefix_splits + p.splits, p.num_kv_heads, batch), dim3(kThreads),
                    smem, s, p);
   if (e == cudaSuccess && ev_after) e = cudaEventRecord(ev_after, s);
   if (e == cudaSuccess)

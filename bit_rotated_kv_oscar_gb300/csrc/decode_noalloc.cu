@@ -153,6 +153,10 @@ extern "C" int oscar_decode_attn_noalloc(const oscar_config* cfg, const void* q,
   p.gqa = g;
   p.sink = cfg->sink;
   p.ngroups = kHeadDim / cfg->group_size;
+  p.batch = batch;
+  p.prefix_tokens = 0;
+  p.prefix_splits = 0;
+  p.pack = 1;
   p.recent = cfg->recent;
   p.splits = splits;
   p.fold_rv = cfg->fold_rv;

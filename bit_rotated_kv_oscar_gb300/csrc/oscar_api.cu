@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <string>
 #include <vector>
@@ -225,8 +226,8 @@ int oscar_create(const oscar_config* cfg, oscar_ctx** out) {
     e = dalloc(&ctx->qrec, (size_t)cfg->max_batch * hkv * kQrecWords * sizeof(uint32_t));
   }
   if (e == cudaSuccess)
-    e = dalloc(&ctx->part, (size_t)cfg->max_batch * hkv * (ctx->max_splits + win_slots(cfg)) * g *
-                               kPartFloats * sizeof(float));
+    e = dalloc(&ctx->part, (size_t)cfg->max_batch * hkv * (2 * ctx->max_splits + win_slots(cfg)) * g *
+                               kPartFloats * sizeof(float));  // shared-prefix calls: two sets of splits
   if (e == cudaSuccess) e = dalloc(&ctx->flags, 2 * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(ctx->flags, 0, 2 * sizeof(uint32_t));
   if (e != cudaSuccess) {
@@ -403,14 +404,41 @@ int oscar_decode_splits(const oscar_ctx* ctx, int32_t batch, int32_t* splits) {
   return OSCAR_OK;
 }
 
+// split counts of a shared-prefix call: the prefix pages are attended once per
+// pack of requests (8 / g of them side by side in the tensor-core columns), the
+// rest of every request as usual; both sets of slices fit the workspace
+static void shared_prefix_splits(const oscar_ctx* ctx, int batch, int prefix_tokens, int* pack, int* prefix_splits,
+                                 int* splits) {
+  const int g = ctx->cfg.num_q_heads / ctx->cfg.num_kv_heads;
+  *pack = std::min(kMaxGqa / g, (int)batch);
+  const int64_t groups = (batch + *pack - 1) / *pack;
+  const int64_t ppages = std::max(0, prefix_tokens / kPage - ctx->cfg.sink / kPage);
+  const int64_t units = groups * ctx->cfg.num_kv_heads;
+  int64_t by_wave = (kDecodeCtasPerSm * (int64_t)ctx->num_sms) / std::max<int64_t>(units, 1);
+  int64_t by_pages = (ppages + kSplitPages - 1) / kSplitPages;
+  int64_t ps = std::max(by_wave, by_pages);
+  ps = std::min<int64_t>(ps, std::max<int64_t>((ppages + 7) / 8, 1));  // >= 8 pages per slice
+  const int64_t spages = std::max<int64_t>(ctx->cfg.max_pages_per_seq - prefix_tokens / kPage, 1);
+  int64_t ss = std::max<int64_t>((spages + kSplitPages - 1) / kSplitPages, 1);
+  const int64_t cap = std::min<int64_t>(2 * ctx->max_splits, 256);
+  ss = std::min(ss, cap - 1);
+  ps = std::max<int64_t>(std::min(ps, cap - ss), 1);
+  *prefix_splits = (int)ps;
+  *splits = (int)ss;
+}
+
 static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table, const oscar_seq_state* state,
-                       float* o, int32_t batch, void* stream, cudaEvent_t ev_before, cudaEvent_t ev_after) {
+                       float* o, int32_t batch, void* stream, cudaEvent_t ev_before, cudaEvent_t ev_after,
+                       int32_t prefix_tokens = 0) {
   if (!ctx) return OSCAR_ERR_INVALID_ARG;
   if (!ctx->loaded) return fail(ctx, OSCAR_ERR_NOT_LOADED, "decode_attn: rotations not loaded");
   if (!ctx->pool) return fail(ctx, OSCAR_ERR_NOT_BOUND, "decode_attn: no cache bound");
   if (!q || !page_table || !state || !o) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_attn: null pointer");
   if (batch < 1) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_attn: batch >= 1");
   if (batch > ctx->cfg.max_batch) return fail(ctx, OSCAR_ERR_OUT_OF_RANGE, "decode_attn: batch exceeds max_batch");
+  if (prefix_tokens < 0 || prefix_tokens % kPage != 0 ||
+      (int64_t)prefix_tokens > (int64_t)ctx->cfg.max_pages_per_seq * kPage)
+    return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_attn: prefix_tokens must be a multiple of 16 within the page table");
   DecodeParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.page_table = page_table;
@@ -433,6 +461,14 @@ static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table,
   p.recent = ctx->cfg.recent;
   p.splits = auto_splits(ctx, batch);
   p.win_slots = win_slots(&ctx->cfg);
+  p.batch = batch;
+  p.prefix_tokens = 0;
+  p.prefix_splits = 0;
+  p.pack = 1;
+  if (prefix_tokens > 0) {
+    p.prefix_tokens = prefix_tokens;
+    shared_prefix_splits(ctx, batch, prefix_tokens, &p.pack, &p.prefix_splits, &p.splits);
+  }
   p.fold_rv = ctx->cfg.fold_rv;
   p.max_batch = ctx->cfg.max_batch;
   p.scale_log2 = ctx->cfg.softmax_scale * 1.4426950408889634f;
@@ -445,6 +481,12 @@ static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table,
 int oscar_decode_attn(oscar_ctx* ctx, const void* q, const int32_t* page_table,
                       const oscar_seq_state* state, float* o, int32_t batch, void* stream) {
   return decode_impl(ctx, q, page_table, state, o, batch, stream, nullptr, nullptr);
+}
+
+int oscar_decode_attn_shared_prefix(oscar_ctx* ctx, const void* q, const int32_t* page_table,
+                                    const oscar_seq_state* state, int32_t prefix_tokens, float* o, int32_t batch,
+                                    void* stream) {
+  return decode_impl(ctx, q, page_table, state, o, batch, stream, nullptr, nullptr, prefix_tokens);
 }
 
 int oscar_decode_attn_timed(oscar_ctx* ctx, const void* q, const int32_t* page_table,

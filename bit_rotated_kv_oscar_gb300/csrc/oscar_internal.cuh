@@ -116,6 +116,12 @@ struct DecodeParams {
   int32_t num_q_heads, num_kv_heads, gqa, sink, recent, splits, fold_rv, max_batch;
   int32_t win_slots;        // CTAs over the BF16 window, 64 tokens each
   int32_t ngroups;          // quantisation groups per token: 128 / group_size (4 or 2)
+  int32_t batch;            // requests of this call
+  // shared prefix: requests 0 .. batch-1 map positions [0, prefix_tokens) to the
+  // same pages; prefix CTAs attend over that range once for `pack` requests at a
+  // time (their query heads side by side in the tensor-core columns), split
+  // prefix_splits ways; prefix_tokens = 0: no shared range
+  int32_t prefix_tokens, prefix_splits, pack;
   float scale_log2;         // softmax_scale * log2(e)
   uint32_t* err_flags;
 };

@@ -208,6 +208,23 @@ int oscar_quant_append_traced(oscar_ctx* ctx, const int32_t* page_table,
 int oscar_decode_attn(oscar_ctx* ctx, const void* q, const int32_t* page_table,
                       const oscar_seq_state* state, float* o, int32_t batch, void* stream);
 
+/* Decode for requests that share a prefix: the same result as oscar_decode_attn,
+ * with the INT2 positions of the shared range read once per pack of requests.
+ * Prefix caching is kept in the paged cache ([ES] "El sistema de servicio"
+ * keeps prefix caching and paged attention); this call adds reading an aliased
+ * page once for several requests, which the pages leave open.
+ * Contract: requests 0 .. batch-1 map positions [0, prefix_tokens) to the same
+ * page ids (page_table rows equal on their first prefix_tokens / 16 entries,
+ * as after a fork), and prefix_tokens <= int2_end <= seq_len for each of them.
+ * prefix_tokens: a multiple of 16 (0 = no shared range: oscar_decode_attn).
+ * The shared range [sink, prefix_tokens) is attended once for every 8 / g
+ * requests (their g query heads side by side in the tensor-core columns), each
+ * request's own positions after it as usual. A request breaking the contract
+ * sets OSCAR_FLAG_BAD_STATE and gets no contribution from the shared range. */
+int oscar_decode_attn_shared_prefix(oscar_ctx* ctx, const void* q, const int32_t* page_table,
+                                    const oscar_seq_state* state, int32_t prefix_tokens, float* o,
+                                    int32_t batch, void* stream);
+
 /* Number of INT2 splits per (request, KV head) decode uses for `batch`. */
 int oscar_decode_splits(const oscar_ctx* ctx, int32_t batch, int32_t* splits);
 
