@@ -79,6 +79,9 @@ _SIGS = {
     "oscar_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P]),
     "oscar_decode_attn_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P]),
     "oscar_decode_attn_shared_prefix": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P]),
+    "oscar_calibration_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
+    "oscar_calibration_covariances": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                     ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]),
     "oscar_quant_append_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32, _P,
                                                 _P, _P]),
     "oscar_decode_splits": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
@@ -130,6 +133,22 @@ def make_config(num_q_heads, num_kv_heads, sink, recent, max_batch, max_pages_pe
 
 def check_config(cfg: OscarConfig) -> int:
     return lib().oscar_check_config(ctypes.byref(cfg))
+
+
+def calibration_covariances(q, k, v, softmax_scale: float = 0.0, stream=None):
+    """C_Q, C_S (device float32 [Hkv, 128, 128]) of calibration activations q
+    [N, Hq, 128], k, v [N, Hkv, 128] (device bf16), computed by the library."""
+    import torch
+
+    n, hq, _ = q.shape
+    hkv = k.shape[1]
+    c_q = torch.empty(hkv, 128, 128, dtype=torch.float32, device=q.device)
+    c_s = torch.empty_like(c_q)
+    nbytes = lib().oscar_calibration_workspace_bytes(n, hq)
+    ws = torch.empty(max(nbytes, 4) // 4, dtype=torch.float32, device=q.device)
+    _check(lib().oscar_calibration_covariances(_ptr(q), _ptr(k), _ptr(v), n, hq, hkv, softmax_scale, _ptr(c_q),
+                                               _ptr(c_s), _ptr(ws), nbytes, _stream(stream)))
+    return c_q, c_s
 
 
 def cache_bytes(cfg: OscarConfig, num_pages: int):

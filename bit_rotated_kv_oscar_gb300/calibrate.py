@@ -71,26 +71,53 @@ def calibrate(q_cal, k_cal, v_cal, percentile: float = 99.9, scale: float | None
     g = hq // hkv
     if scale is None:
         scale = d ** -0.5
-    hp = _hadamard(d) @ _bit_reversal(d)
     causal = torch.ones(n, n, dtype=torch.bool).triu(1)
+    c_q = torch.zeros(hkv, d, d, dtype=torch.float64)
+    c_s = torch.zeros(hkv, d, d, dtype=torch.float64)
+    for h in range(hkv):
+        for j in range(h * g, (h + 1) * g):
+            qj = q[:, j]
+            c_q[h] += qj.T @ qj / n
+            logits = (qj @ k[:, h].T * scale).masked_fill(causal, float("-inf"))
+            sv = torch.softmax(logits, dim=1) @ v[:, h]
+            c_s[h] += sv.T @ sv / n
+    return _rotations_and_clips(c_q / g, c_s / g, k, v, percentile, clip_percentile_k, clip_percentile_v)
+
+
+def calibrate_device(q_cal, k_cal, v_cal, percentile: float = 99.9, scale: float | None = None,
+                     clip_percentile_k: float | None = None, clip_percentile_v: float | None = None) -> dict:
+    """calibrate() with the covariances C_Q, C_S accumulated on the GPU by the
+    library (float32); eigendecomposition, rotations and clips on the host.
+    q_cal [N, Hq, d], k_cal / v_cal [N, Hkv, d]: the calibration activations."""
+    from . import abi
+
+    dev = torch.device("cuda")
+    q = torch.as_tensor(q_cal).to(dev, torch.bfloat16).contiguous()
+    k = torch.as_tensor(k_cal).to(dev, torch.bfloat16).contiguous()
+    v = torch.as_tensor(v_cal).to(dev, torch.bfloat16).contiguous()
+    c_q, c_s = abi.calibration_covariances(q, k, v, 0.0 if scale is None else float(scale))
+    torch.cuda.synchronize()
+    return _rotations_and_clips(c_q.cpu().to(torch.float64), c_s.cpu().to(torch.float64),
+                                k.cpu().to(torch.float64), v.cpu().to(torch.float64), percentile,
+                                clip_percentile_k, clip_percentile_v)
+
+
+def _rotations_and_clips(c_q, c_s, k, v, percentile, clip_percentile_k, clip_percentile_v) -> dict:
+    """R = U H P per KV head from the covariances [Hkv, d, d] (float64), then the
+    per-layer clips from the rotated calibration keys and values."""
+    hkv, d = c_q.shape[0], c_q.shape[1]
+    hp = _hadamard(d) @ _bit_reversal(d)
     r_k = torch.empty(hkv, d, d, dtype=torch.float64)
     r_v = torch.empty(hkv, d, d, dtype=torch.float64)
     for h in range(hkv):
-        cq = torch.zeros(d, d, dtype=torch.float64)
-        cs = torch.zeros(d, d, dtype=torch.float64)
-        for j in range(h * g, (h + 1) * g):
-            qj = q[:, j]
-            cq += qj.T @ qj / n
-            logits = (qj @ k[:, h].T * scale).masked_fill(causal, float("-inf"))
-            sv = torch.softmax(logits, dim=1) @ v[:, h]
-            cs += sv.T @ sv / n
-        r_k[h] = _eigvecs_desc(cq / g) @ hp
-        r_v[h] = _eigvecs_desc(cs / g) @ hp
+        r_k[h] = _eigvecs_desc(c_q[h]) @ hp
+        r_v[h] = _eigvecs_desc(c_s[h]) @ hp
     pk = percentile if clip_percentile_k is None else clip_percentile_k
     pv = percentile if clip_percentile_v is None else clip_percentile_v
     clip_k = _percentile(torch.einsum("nhi,hij->nhj", k, r_k).abs(), pk)
     clip_v = _percentile(torch.einsum("nhi,hij->nhj", v, r_v).abs(), pv)
     return {
+        "C_Q": c_q.numpy(), "C_S": c_s.numpy(),
         "R_K": r_k.to(torch.float32).numpy(),
         "R_V": r_v.to(torch.float32).numpy(),
         "clip_K": np.full(hkv, clip_k, dtype=np.float32),

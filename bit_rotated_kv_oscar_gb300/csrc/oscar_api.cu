@@ -512,4 +512,23 @@ const char* oscar_last_error(const oscar_ctx* ctx) {
   return ctx->last_error.c_str();
 }
 
+size_t oscar_calibration_workspace_bytes(int32_t n, int32_t num_q_heads) {
+  if (n < 1 || num_q_heads < 1) return 0;
+  return calib_workspace_bytes(n, num_q_heads);
+}
+
+int oscar_calibration_covariances(const void* q, const void* k, const void* v, int32_t n, int32_t num_q_heads,
+                                  int32_t num_kv_heads, float softmax_scale, float* c_q, float* c_s,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !c_q || !c_s || !workspace || n < 1 || num_kv_heads < 1 || num_q_heads < num_kv_heads ||
+      num_q_heads % num_kv_heads != 0 || !(softmax_scale >= 0.f) || isinf(softmax_scale))
+    return OSCAR_ERR_INVALID_ARG;
+  if (workspace_bytes < calib_workspace_bytes(n, num_q_heads)) return OSCAR_ERR_OUT_OF_RANGE;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)kHeadDim);
+  cudaError_t e = launch_calib_covariances(static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+                                           static_cast<const __nv_bfloat16*>(v), n, num_q_heads, num_kv_heads, scale,
+                                           c_q, c_s, static_cast<float*>(workspace), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -162,5 +162,11 @@ int prefill_image_bytes();
 cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cudaEvent_t ev_before = nullptr,
                           cudaEvent_t ev_after = nullptr);
 int decode_smem_bytes();
+// offline calibration: causal attention outputs of every query head into o_ws
+// (calib_workspace_bytes), then C_Q and C_S per KV head (fp32 [hkv][128][128])
+size_t calib_workspace_bytes(int n, int hq);
+cudaError_t launch_calib_covariances(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v, int n,
+                                     int hq, int hkv, float scale, float* c_q, float* c_s, float* o_ws,
+                                     cudaStream_t s);
 
 }  // namespace oscar

@@ -252,6 +252,27 @@ int oscar_quant_append_timed(oscar_ctx* ctx, const int32_t* page_table, oscar_se
                              const void* k, const void* v, int32_t batch, int32_t n_new, void* stream,
                              void* ev_before, void* ev_after);
 
+/* Offline calibration on the device (no context): the covariance targets of the
+ * rotations of one layer, "OSCAR: Offline Spectral Covariance-Aware Rotation
+ * ..." (gist.science, it), Riepilogo Tecnico 2.2 A "Stima della Covarianza".
+ * q: DEVICE bf16 [n][num_q_heads][128], k, v: DEVICE bf16 [n][num_kv_heads][128]
+ * (the calibration activations of the layer, token-major); c_q, c_s: DEVICE
+ * float32 [num_kv_heads][128][128], written:
+ *   c_q[h] = (1/(n g)) sum over h's g query heads j and tokens t of q_jt^T q_jt,
+ *   c_s[h] = (1/(n g)) sum_j (S_j V_h)^T (S_j V_h), S_j = causal softmax of
+ *            q_j k_h^T * softmax_scale (0: 1/sqrt(128)),
+ * accumulated in float32. workspace: caller-owned DEVICE memory of at least
+ * oscar_calibration_workspace_bytes(n, num_q_heads) bytes (the attention
+ * outputs S_j V_h). Asynchronous on stream. The rotations follow on the host:
+ * eigenvectors in descending eigenvalue order, R = U H P.
+ * Returns OSCAR_ERR_INVALID_ARG for a null pointer or inconsistent sizes,
+ * OSCAR_ERR_OUT_OF_RANGE for a workspace that is too small, OSCAR_ERR_CUDA
+ * for a launch failure. */
+size_t oscar_calibration_workspace_bytes(int32_t n, int32_t num_q_heads);
+int oscar_calibration_covariances(const void* q, const void* k, const void* v, int32_t n, int32_t num_q_heads,
+                                  int32_t num_kv_heads, float softmax_scale, float* c_q, float* c_s,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the fixed device array behind oscar_decode_attn_noalloc. */
 #define OSCAR_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -73,14 +73,23 @@ class Layer:
 
     def __init__(self, hq, hkv, sink, recent, max_batch, max_tokens, seed=0, n_cal=512,
                  shuffled=True, fold_rv=0, num_splits=0, extra_pages=0, spikes=False,
-                 device="cuda", group=32, clip_percentiles=(99.9, 99.9)):
+                 device="cuda", group=32, clip_percentiles=(99.9, 99.9), device_calibration=False):
         self.hq, self.hkv, self.sink, self.recent = hq, hkv, sink, recent
         self.group = group
         self.seed, self.spikes, self.device = seed, spikes, device
         q_cal = draw_queries(seed, 900, n_cal, hq, hkv, D).numpy()
         k_cal, v_cal = (t.numpy() for t in draw_kv(seed, 900, n_cal, hkv, D, spikes))
-        self.cal = oracle.calibrate(q_cal, k_cal, v_cal, clip_percentile_k=clip_percentiles[0],
-                                    clip_percentile_v=clip_percentiles[1])
+        if device_calibration:
+            # the library's device covariances, rotations and clips on the host; the
+            # oracle then runs with these float32 rotations like with its own
+            from bit_rotated_kv_oscar_gb300.calibrate import calibrate_device
+            d = calibrate_device(q_cal, k_cal, v_cal, clip_percentile_k=clip_percentiles[0],
+                                 clip_percentile_v=clip_percentiles[1])
+            self.cal = {"R_K32": d["R_K"], "R_V32": d["R_V"], "clip_K32": d["clip_K"], "clip_V32": d["clip_V"],
+                        "C_Q": d["C_Q"], "C_S": d["C_S"]}
+        else:
+            self.cal = oracle.calibrate(q_cal, k_cal, v_cal, clip_percentile_k=clip_percentiles[0],
+                                        clip_percentile_v=clip_percentiles[1])
         self.fold_rv = fold_rv
         max_pages = (max_tokens + 15) // 16
         self.cfg = abi.make_config(hq, hkv, sink, recent, max_batch, max_pages, fold_rv=fold_rv,
