@@ -79,6 +79,13 @@ def test_shared_prefix_of_the_pages_preset():
     assert layer.ctx.error_flags() == 0
 
 
+def test_shared_prefix_with_values_folded_into_the_projection():
+    layer = forked_layer(32, 8, 4, 1024, 1500, [100, 0, 333], seed=29, fold_rv=1)
+    q = layer.queries(4, 16)
+    check_against_oracle(layer, q, shared_decode(layer, q, 1024))
+    assert layer.ctx.error_flags() == 0
+
+
 @pytest.mark.parametrize("prefix", [0, 16, 512])
 def test_shorter_declared_prefix(prefix):
     # declaring less than what is shared is still correct: the rest is read per request

@@ -26,9 +26,10 @@ def _lib():
     abi.lib()
 
 
-def test_noalloc_matches_context_decode_twice():
+@pytest.mark.parametrize("group", [32, 64])
+def test_noalloc_matches_context_decode_twice(group):
     lengths = [2500, 700, 1900]
-    layer = Layer(32, 8, 4, 128, len(lengths), 3000, seed=61)
+    layer = Layer(32, 8, 4, 128, len(lengths), 3000, seed=61, group=group)
     for b, n in enumerate(lengths):
         k, v = layer.draw(n)
         layer.append(b, k, v)
