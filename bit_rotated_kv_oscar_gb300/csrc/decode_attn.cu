@@ -10,10 +10,14 @@
 // Three launches on one stream:
 //   1. oscar_rotate_q_kernel   q~ = q R_K * scale * log2(e) per (request, KV head),
 //      written as ready-to-use tensor-core operand fragments (fp16 hi + lo).
-//   2. oscar_decode_kernel     grid (1 + splits, Hkv, B): CTA x = 0 attends over
-//      the BF16 sink + recent ring in the raw basis; CTA x >= 1 streams a slice of
-//      the INT2 pages, computing scores and the P.V product on the tensor cores
-//      with exact 2-bit operands, in the R_V basis.
+//   2. oscar_decode_kernel<NG> grid (window chunks + prefix splits + splits, Hkv,
+//      B), NG = 128 / group size: the first CTAs attend over the BF16 sink +
+//      recent ring in the raw basis (64 tokens each); the others stream a slice
+//      of the INT2 pages, computing scores and the P.V product on the tensor
+//      cores with exact 2-bit operands, in the R_V basis. With a shared prefix
+//      (oscar_decode_attn_shared_prefix) the prefix CTAs attend over the shared
+//      pages once for a pack of requests, their query heads side by side in the
+//      tensor-core columns, and the per-request CTAs over what follows.
 //   3. oscar_merge_kernel      log-sum-exp merge of all partials, R_V^T applied to
 //      the INT2 part, normalisation.
 //
