@@ -843,60 +843,46 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
 
 // --------------------------------------------------------------------------
 // 3. merge of the partials, un-rotation, normalisation; CTA z handles query
-//    heads 2z and 2z + 1 of (request y, KV head x)
+//    heads 2z and 2z + 1 of (request y, KV head x). The partial rows (o, m, l)
+//    are staged in rounds of up to kMergeChunk slots, all in flight at once, and
+//    folded in with a running maximum, so a call with up to kMergeChunk slots
+//    waits for the level-2 cache once.
 // --------------------------------------------------------------------------
 constexpr int kMergeThreads = 256;
 constexpr int kMaxSlots = 256 + kMaxWindow / kWinChunk;   // INT2 splits + window chunks
-constexpr int kMergeChunk = 32;                            // partial rows staged per round
-constexpr int kMergeSmem = kRotSmem + kMergeChunk * 2 * kPartFloats * 4 + kMaxSlots * 4 * 4 +
-                           2 * kHeadDim * 4;
+constexpr int kMergeChunk = 64;                            // slots staged per round
+__host__ __device__ constexpr int merge_smem_bytes(int nslots) {
+  return kRotSmem + (nslots < kMergeChunk ? nslots : kMergeChunk) * 2 * kPartFloats * 4 + 2 * kHeadDim * 4;
+}
+constexpr int kMergeSmem = merge_smem_bytes(kMergeChunk);
 
 __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
-  float* RT = reinterpret_cast<float*>(dsm);                   // R_V^T[h], [128][128]
-  float* rows = RT + kHeadDim * kHeadDim;                       // [32 slots][2 heads][kPartFloats]
-  float* wts = rows + kMergeChunk * 2 * kPartFloats;            // [slots][2] max, then weight
-  float* lsl = wts + kMaxSlots * 2;                             // [slots][2] row sums
-  float* orot = lsl + kMaxSlots * 2;                            // [2][128]
-  __shared__ float lsum_s[2];
-  const int h = blockIdx.x, b = blockIdx.y, m0 = 2 * blockIdx.z, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
   const int g = p.gqa, nslots = p.win_slots + p.prefix_splits + p.splits, nwin = p.win_slots;
+  const int chunk = nslots < kMergeChunk ? nslots : kMergeChunk;
+  float* RT = reinterpret_cast<float*>(dsm);                   // R_V^T[h], [128][128]
+  float* rows = RT + kHeadDim * kHeadDim;                       // [chunk slots][2 heads][kPartFloats]
+  float* orot = rows + chunk * 2 * kPartFloats;                 // [2][128]
+  const int h = blockIdx.x, b = blockIdx.y, m0 = 2 * blockIdx.z, tid = threadIdx.x;
   const int nh = min(2, g - m0);
   if (!p.fold_rv) stage_matrix(RT, p.R_VT + (size_t)h * kHeadDim * kHeadDim, tid, kMergeThreads);
   else cp_commit();
   pdl_wait();  // the partials come from the decode kernel
   pdl_trigger();
   const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
-  for (int i = tid; i < nslots * nh; i += kMergeThreads) {
-    const int sidx = i / nh, hh = i % nh;
-    const float* ps = part + ((size_t)sidx * g + m0 + hh) * kPartFloats;
-    wts[sidx * 2 + hh] = ps[kHeadDim];
-    lsl[sidx * 2 + hh] = ps[kHeadDim + 1];
-  }
-  __syncthreads();
-  // weights exp2(m_s - M), one warp per head
-  if (warp < nh) {
-    float M = -INFINITY;
-    for (int sidx = lane; sidx < nslots; sidx += 32) M = fmaxf(M, wts[sidx * 2 + warp]);
-    M = warp_maxf(M);
-    float l = 0.f;
-    for (int sidx = lane; sidx < nslots; sidx += 32) {
-      const float ms = wts[sidx * 2 + warp];
-      const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      wts[sidx * 2 + warp] = w;
-      l += w * lsl[sidx * 2 + warp];
-    }
-    l = warp_sum(l);
-    if (lane == 0) lsum_s[warp] = l;
-  }
-  __syncthreads();
-  // thread (head hh, channel c): weighted sums of the window and INT2 partials
+  // warp hh < nh keeps the running maximum and row sum of head hh and writes the
+  // round's slot weights; thread (head hh, channel c) keeps the weighted sums of
+  // the window and INT2 partials, relative to the running maximum
+  __shared__ float wts[kMergeChunk * 2];   // [slot][head] weights of the round
+  __shared__ float resc[2], lsum[2];       // per head: the round's rescale factor, the row sum
+  const int warp = tid >> 5, lane = tid & 31;
   const int c = tid & (kHeadDim - 1), hh = tid >> 7;
-  float owin = 0.f, orr = 0.f;
+  float Mw = -INFINITY, lw = 0.f;
+  float owin = 0.f, orr0 = 0.f, orr1 = 0.f;
   constexpr int kChunks16 = kPartFloats / 4;  // 16-byte pieces per row
-  for (int s0 = 0; s0 < nslots; s0 += kMergeChunk) {
-    const int n = min(kMergeChunk, nslots - s0);
+  for (int s0 = 0; s0 < nslots; s0 += chunk) {
+    const int n = min(chunk, nslots - s0);
+    if (s0 > 0) __syncthreads();  // the previous round's rows and weights are consumed
     for (int i = tid; i < n * nh * kChunks16; i += kMergeThreads) {
       const int r = i / kChunks16, u = i % kChunks16;
       const int sidx = s0 + r / nh, h2 = r % nh;
@@ -905,18 +891,44 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
     cp_commit();
     cp_wait<0>();
     __syncthreads();
-    if (hh < nh) {
-      for (int r = 0; r < n; ++r) {
-        const int sidx = s0 + r;
-        const float v = wts[sidx * 2 + hh] * rows[(r * nh + hh) * kPartFloats + c];
-        if (sidx < nwin)
-          owin += v;
-        else
-          orr += v;
+    if (warp < nh) {
+      float mx = Mw;
+      for (int r = lane; r < n; r += 32) mx = fmaxf(mx, rows[(r * nh + warp) * kPartFloats + kHeadDim]);
+      mx = warp_maxf(mx);
+      const float a = Mw == -INFINITY ? 0.f : exp2f(Mw - mx);  // accumulators are 0 while Mw is -inf
+      float ls = 0.f;
+      for (int r = lane; r < n; r += 32) {
+        const float* row = rows + (r * nh + warp) * kPartFloats;
+        const float ms = row[kHeadDim];
+        const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+        wts[r * 2 + warp] = w;
+        ls = fmaf(w, row[kHeadDim + 1], ls);
+      }
+      ls = warp_sum(ls);
+      lw = fmaf(lw, a, ls);
+      Mw = mx;
+      if (lane == 0) {
+        resc[warp] = a;
+        lsum[warp] = lw;
       }
     }
     __syncthreads();
+    if (hh < nh) {
+      const float a = resc[hh];
+      owin *= a;
+      orr0 *= a;
+      orr1 *= a;
+      const int nw = min(max(nwin - s0, 0), n);  // the round's window slots come first
+      for (int r = 0; r < nw; ++r) owin = fmaf(wts[r * 2 + hh], rows[(r * nh + hh) * kPartFloats + c], owin);
+      int r = nw;
+      for (; r + 1 < n; r += 2) {
+        orr0 = fmaf(wts[r * 2 + hh], rows[(r * nh + hh) * kPartFloats + c], orr0);
+        orr1 = fmaf(wts[r * 2 + 2 + hh], rows[((r + 1) * nh + hh) * kPartFloats + c], orr1);
+      }
+      if (r < n) orr0 = fmaf(wts[r * 2 + hh], rows[(r * nh + hh) * kPartFloats + c], orr0);
+    }
   }
+  const float orr = orr0 + orr1;
   if (hh < nh) orot[hh * kHeadDim + c] = orr;
   cp_wait<0>();
   __syncthreads();
@@ -925,11 +937,16 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
     if (p.fold_rv) {
       oi = orr;
     } else {
-      oi = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < kHeadDim; ++j) oi = fmaf(orot[hh * kHeadDim + j], RT[j * kHeadDim + c], oi);
+      // four independent accumulation chains over j
+      float o4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int j = 0; j < kHeadDim; j += 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o4[k] = fmaf(orot[hh * kHeadDim + j + k], RT[(j + k) * kHeadDim + c], o4[k]);
+      }
+      oi = (o4[0] + o4[1]) + (o4[2] + o4[3]);
     }
-    const float l = lsum_s[hh];
+    const float l = lsum[hh];
     p.o[((size_t)b * p.num_q_heads + h * g + m0 + hh) * kHeadDim + c] = l > 0.f ? (oi + owin) / l : 0.f;
   }
 }
@@ -970,7 +987,7 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
   if (e == cudaSuccess && ev_after) e = cudaEventRecord(ev_after, s);
   if (e == cudaSuccess)
     e = launch_pdl(oscar_merge_kernel, dim3(p.num_kv_heads, batch, (p.gqa + 1) / 2), dim3(kMergeThreads),
-                   kMergeSmem, s, p);
+                   merge_smem_bytes(p.win_slots + p.prefix_splits + p.splits), s, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
