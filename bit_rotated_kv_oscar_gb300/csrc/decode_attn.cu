@@ -851,8 +851,14 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
 constexpr int kMergeThreads = 256;
 constexpr int kMaxSlots = 256 + kMaxWindow / kWinChunk;   // INT2 splits + window chunks
 constexpr int kMergeChunk = 64;                            // slots staged per round
+// floats of the staged rows (also the un-rotation partials, 4 x 128 floats)
+__host__ __device__ constexpr int merge_rows_floats(int nslots) {
+  return (nslots < kMergeChunk ? nslots : kMergeChunk) * 2 * kPartFloats > 4 * kHeadDim
+             ? (nslots < kMergeChunk ? nslots : kMergeChunk) * 2 * kPartFloats
+             : 4 * kHeadDim;
+}
 __host__ __device__ constexpr int merge_smem_bytes(int nslots) {
-  return kRotSmem + (nslots < kMergeChunk ? nslots : kMergeChunk) * 2 * kPartFloats * 4 + 2 * kHeadDim * 4;
+  return kRotSmem + merge_rows_floats(nslots) * 4 + 2 * kHeadDim * 4;
 }
 constexpr int kMergeSmem = merge_smem_bytes(kMergeChunk);
 
@@ -862,7 +868,7 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   const int chunk = nslots < kMergeChunk ? nslots : kMergeChunk;
   float* RT = reinterpret_cast<float*>(dsm);                   // R_V^T[h], [128][128]
   float* rows = RT + kHeadDim * kHeadDim;                       // [chunk slots][2 heads][kPartFloats]
-  float* orot = rows + chunk * 2 * kPartFloats;                 // [2][128]
+  float* orot = rows + merge_rows_floats(nslots);               // [2][128]
   const int h = blockIdx.x, b = blockIdx.y, m0 = 2 * blockIdx.z, tid = threadIdx.x;
   const int nh = min(2, g - m0);
   if (!p.fold_rv) stage_matrix(RT, p.R_VT + (size_t)h * kHeadDim * kHeadDim, tid, kMergeThreads);
@@ -921,6 +927,7 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
       const int nw = min(max(nwin - s0, 0), n);  // the round's window slots come first
       for (int r = 0; r < nw; ++r) owin = fmaf(wts[r * 2 + hh], rows[(r * nh + hh) * kPartFloats + c], owin);
       int r = nw;
+#pragma unroll 4
       for (; r + 1 < n; r += 2) {
         orr0 = fmaf(wts[r * 2 + hh], rows[(r * nh + hh) * kPartFloats + c], orr0);
         orr1 = fmaf(wts[r * 2 + 2 + hh], rows[((r + 1) * nh + hh) * kPartFloats + c], orr1);
@@ -932,20 +939,35 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   if (hh < nh) orot[hh * kHeadDim + c] = orr;
   cp_wait<0>();
   __syncthreads();
-  if (hh < nh) {
-    float oi;
-    if (p.fold_rv) {
-      oi = orr;
-    } else {
-      // four independent accumulation chains over j
-      float o4[4] = {0.f, 0.f, 0.f, 0.f};
+  float oi = orr;
+  if (!p.fold_rv) {
+    // un-rotation: thread (channel c, half hh) takes rows j of its half for both
+    // heads, so every R_V^T entry is read from shared memory once; the two halves
+    // meet in shared memory (rows is free by now)
+    float* acc2 = rows;   // [2 halves][2 heads][128]
+    const int j0 = hh * (kHeadDim / 2);
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll 4
-      for (int j = 0; j < kHeadDim; j += 4) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o4[k] = fmaf(orot[hh * kHeadDim + j + k], RT[(j + k) * kHeadDim + c], o4[k]);
-      }
-      oi = (o4[0] + o4[1]) + (o4[2] + o4[3]);
+    for (int j = j0; j < j0 + kHeadDim / 2; j += 4) {
+      const float4 x0 = *reinterpret_cast<const float4*>(orot + j);
+      const float4 x1 = *reinterpret_cast<const float4*>(orot + kHeadDim + j);
+      const float r0 = RT[j * kHeadDim + c], r1 = RT[(j + 1) * kHeadDim + c];
+      const float r2 = RT[(j + 2) * kHeadDim + c], r3 = RT[(j + 3) * kHeadDim + c];
+      a0 = fmaf(x0.x, r0, a0);
+      a1 = fmaf(x0.y, r1, a1);
+      a0 = fmaf(x0.z, r2, a0);
+      a1 = fmaf(x0.w, r3, a1);
+      b0 = fmaf(x1.x, r0, b0);
+      b1 = fmaf(x1.y, r1, b1);
+      b0 = fmaf(x1.z, r2, b0);
+      b1 = fmaf(x1.w, r3, b1);
     }
+    acc2[(hh * 2 + 0) * kHeadDim + c] = a0 + a1;
+    acc2[(hh * 2 + 1) * kHeadDim + c] = b0 + b1;
+    __syncthreads();
+    if (hh < nh) oi = acc2[(0 * 2 + hh) * kHeadDim + c] + acc2[(1 * 2 + hh) * kHeadDim + c];
+  }
+  if (hh < nh) {
     const float l = lsum[hh];
     p.o[((size_t)b * p.num_q_heads + h * g + m0 + hh) * kHeadDim + c] = l > 0.f ? (oi + owin) / l : 0.f;
   }
