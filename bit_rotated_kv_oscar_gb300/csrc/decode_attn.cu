@@ -811,9 +811,15 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
 template <int NG>
 __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  const int x = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  // R_V^T[h] (constant) into the level-2 cache for the merge, whose CTAs only
+  // become resident as these retire: one bulk prefetch per KV head
+  if (x == 0 && z == 0 && threadIdx.x == 0 && !p.fold_rv) {
+    const float* rvt = p.R_VT + (size_t)h * kHeadDim * kHeadDim;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(rvt), "r"(kHeadDim * kHeadDim * 4) : "memory");
+  }
   pdl_wait();  // cache, state and q~ come from earlier kernels
   pdl_trigger();
-  const int x = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   const int S = p.sink, W = p.recent, P = p.prefix_tokens;
   if (x < p.win_slots) {
     window_attention(p, z, h, x, smem);
@@ -873,9 +879,17 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   const int nh = min(2, g - m0);
   if (!p.fold_rv) stage_matrix(RT, p.R_VT + (size_t)h * kHeadDim * kHeadDim, tid, kMergeThreads);
   else cp_commit();
+  const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
+  // touch the partials' address range while the decode kernel still runs, so the
+  // copies below find their address translations cached (a level-2 prefetch
+  // returns no data, so what the decode kernel writes later is not bypassed)
+  if (tid < 32) {
+    const size_t span = (size_t)nslots * g * kPartFloats * 4;
+    for (size_t off = (size_t)tid * 4096; off < span; off += 32 * 4096)
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char*>(part) + off));
+  }
   pdl_wait();  // the partials come from the decode kernel
   pdl_trigger();
-  const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
   // warp hh < nh keeps the running maximum and row sum of head hh and writes the
   // round's slot weights; thread (head hh, channel c) keeps the weighted sums of
   // the window and INT2 partials, relative to the running maximum
@@ -889,10 +903,11 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   for (int s0 = 0; s0 < nslots; s0 += chunk) {
     const int n = min(chunk, nslots - s0);
     if (s0 > 0) __syncthreads();  // the previous round's rows and weights are consumed
-    for (int i = tid; i < n * nh * kChunks16; i += kMergeThreads) {
-      const int r = i / kChunks16, u = i % kChunks16;
-      const int sidx = s0 + r / nh, h2 = r % nh;
-      cp_async16(rows + r * kPartFloats + 4 * u, part + ((size_t)sidx * g + m0 + h2) * kPartFloats + 4 * u);
+    // a slot's rows of both heads are contiguous: one warp per slot, no divisions
+    for (int r = warp; r < n; r += kMergeThreads / 32) {
+      const float* src = part + ((size_t)(s0 + r) * g + m0) * kPartFloats;
+      float* dst = rows + r * nh * kPartFloats;
+      for (int u = lane; u < nh * kChunks16; u += 32) cp_async16(dst + 4 * u, src + 4 * u);
     }
     cp_commit();
     cp_wait<0>();

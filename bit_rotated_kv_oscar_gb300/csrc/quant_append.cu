@@ -58,13 +58,16 @@ oscar_quant_append_kernel(AppendParams p) {
   const int Hkv = p.num_kv_heads;
 
   __shared__ oscar_seq_state s_st;
-  __shared__ int s_last, s_page;
+  __shared__ int s_page;
+  __shared__ __align__(16) __nv_bfloat16 s_in[2][kHeadDim];   // K, V of the CTA's first token
   __shared__ float xs[2][kHeadDim];            // token being quantised, K and V
   __shared__ float red[2][2][kHeadDim];        // partial dot products
   __shared__ uint8_t codes[2][kHeadDim];
   __shared__ __half meta[2][kGroups][2];
   __shared__ float wmm[2][4][2];  // per kind and warp: min, max of its 32 clipped channels
 
+  // copies of 16 bytes need 16-byte aligned inputs (otherwise read in place)
+  const bool staged = j0 < j1 && ((reinterpret_cast<uintptr_t>(p.k) | reinterpret_cast<uintptr_t>(p.v)) & 15) == 0;
   // the rotations are constant: stage them before waiting for earlier kernels
   {
     const float* rk = p.R_K + (size_t)h * kHeadDim * kHeadDim;
@@ -74,15 +77,25 @@ oscar_quant_append_kernel(AppendParams p) {
       cp_async16(Rs + 4 * i, rk + 4 * i);
       if (!p.fold_rv) cp_async16(Rs + kHeadDim * kHeadDim + 4 * i, rv + 4 * i);
     }
+    // the CTA's first new token: the caller's input, which no kernel of this
+    // library writes, so it is read before waiting for earlier kernels
+    if (staged && tid < 2 * (kHeadDim / 8)) {
+      const int jf = !p.tail_only ? j0 : (j0 < S ? j0 : p.n_new - W + (j0 - S));
+      const size_t off = (((size_t)b * p.n_new + jf) * Hkv + h) * kHeadDim;
+      const int kind = tid >> 4, u = tid & 15;
+      cp_async16(&s_in[kind][8 * u], (kind ? p.v : p.k) + off + 8 * u);
+    }
     asm volatile("cp.async.commit_group;\n" ::);
   }
   pdl_wait();
   pdl_trigger();
+  // ticket: taken once the state is read; its value is needed only at the end,
+  // where the CTA holding the last one publishes the new states
+  unsigned ticket = 0u;
   if (tid == 0) {
     s_st = p.state[b];
     __threadfence();
-    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
-    s_last = (atomicAdd(p.counter, 1u) == total - 1u);
+    ticket = atomicAdd(p.counter, 1u);
   }
   asm volatile("cp.async.wait_group 0;\n" ::);  // rotations staged, visible after the barrier
   __syncthreads();
@@ -107,6 +120,8 @@ oscar_quant_append_kernel(AppendParams p) {
       // with tail_only the tokens going straight to INT2 belong to the prefill kernel
       if (p.tail_only && q >= S && q < E2) continue;
       const size_t in_off = (((size_t)b * p.n_new + j) * Hkv + h) * kHeadDim;
+      const __nv_bfloat16* in_k = staged && jv == j0 ? s_in[0] : p.k + in_off;
+      const __nv_bfloat16* in_v = staged && jv == j0 ? s_in[1] : p.v + in_off;
       // what this token quantises: -1 none, else the position, and where it comes from
       int64_t qpos = -1;
       const __nv_bfloat16* src_k = nullptr;
@@ -115,13 +130,13 @@ oscar_quant_append_kernel(AppendParams p) {
       if (q < S) {
         // sink token: BF16 copy
         if (tid < kHeadDim) {
-          win_k[(size_t)q * kHeadDim + tid] = p.k[in_off + tid];
-          win_v[(size_t)q * kHeadDim + tid] = p.v[in_off + tid];
+          win_k[(size_t)q * kHeadDim + tid] = in_k[tid];
+          win_v[(size_t)q * kHeadDim + tid] = in_v[tid];
         }
       } else if (q < E2) {
         qpos = q;
-        src_k = p.k + in_off;
-        src_v = p.v + in_off;
+        src_k = in_k;
+        src_v = in_v;
       } else {
         // ring occupant; the entry at its slot may have to be quantised first
         const int64_t pe = q - (int64_t)W * ((q - L) / W + 1);
@@ -150,7 +165,7 @@ oscar_quant_append_kernel(AppendParams p) {
       if (ring_slot_new >= 0 && tid < 2 * kHeadDim) {
         const int kind = tid >> 7, c = tid & 127;
         __nv_bfloat16* dst = (kind ? win_v : win_k) + (size_t)ring_slot_new * kHeadDim;
-        dst[c] = (kind ? p.v : p.k)[in_off + c];
+        dst[c] = (kind ? in_v : in_k)[c];
       }
 
       if (qpos >= 0) {
@@ -260,7 +275,7 @@ oscar_quant_append_kernel(AppendParams p) {
   }
 
   // the CTA that took the last ticket publishes the new state of every request
-  if (s_last && tid == 0) {
+  if (tid == 0 && ticket == gridDim.x * gridDim.y * gridDim.z - 1u) {
     __threadfence();
     for (int bb = 0; bb < p.batch; ++bb) {
       oscar_seq_state sb = p.state[bb];
