@@ -143,13 +143,12 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
   __shared__ __half hs[2][kMaxGqa][kHeadDim];
   __shared__ float wsum[kMaxGqa][4];  // per head and warp: 2^(k-24) times the sum of its 32 channels of q~
   __shared__ float wmax[4];
+  __shared__ int s_k;
   stage_matrix(Rs, p.R_K + (size_t)h * kHeadDim * kHeadDim, tid, kRotThreads);  // constant data
-  // No wait here: every kernel of this library lets its dependents start only
-  // after its own prerequisites completed, so by the time this kernel runs, q
-  // (written before the preceding kernel) is final and the previous decode no
-  // longer reads qrec. The preceding kernel itself (typically the append) may
-  // still run: the wait at the end makes this kernel finish after it, so the
-  // attention kernel's wait covers both.
+  // Everything up to the wait reads only R_K and the caller's q, which no
+  // kernel of this library writes, so it may run beside earlier kernels (the
+  // append lets this kernel start at once); qrec, which the previous decode
+  // reads, is written only after the wait.
   for (int i = tid; i < g * kHeadDim; i += kRotThreads)
     qs[i >> 7][i & 127] = __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g) * kHeadDim + i]);
   cp_wait<0>();
@@ -198,7 +197,6 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
       hs[0][m][c] = hi;
       hs[1][m][c] = __float2half_rn(a - __half2float(hi));
     }
-    uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
     // sums of q~ per head and 32 channels, scaled like the mma results
     // (2^(k-24) sum q~); the group sums below are the zero-point operand
     const float gscale = ldexpf(1.f, k - 24);
@@ -207,17 +205,20 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
       const float sm = warp_sum(acc[m]) * gscale;
       if ((c & 31) == 0) wsum[m][c >> 5] = sm;
     }
-    if (c == 0) {
-      rec[1088] = __float_as_uint(ldexpf(1.f, 24 - k));
-      for (int w = 1089; w < kQrecWords; ++w) rec[w] = 0u;
-    }
+    if (c == 0) s_k = k;
   }
   __syncthreads();
+  pdl_wait();  // earlier kernels (the previous decode reads qrec) are complete
+  pdl_trigger();
+  uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
+  if (tid == 0) {
+    rec[1088] = __float_as_uint(ldexpf(1.f, 24 - s_k));
+    for (int w = 1089; w < kQrecWords; ++w) rec[w] = 0u;
+  }
   // column fragments of m16n8k16 (k = channel, n = head): per slot kb and lane
   // (gid, tig) four words, hi parts of head gid at channels 16 kb + 2 tig (+1) and
   // + 8 (+9), then the lo parts at the same channels, so that each operand pair
   // is one aligned half of the 16-byte record entry
-  uint32_t* rec = p.qrec + ((size_t)b * p.num_kv_heads + h) * kQrecWords;
 #pragma unroll
   for (int n = 0; n < 4; ++n) {
     const int widx = tid + kRotThreads * n;
@@ -248,8 +249,6 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
     }
     rec[1024 + tid] = w;
   }
-  pdl_wait();
-  pdl_trigger();
 }
 
 // --------------------------------------------------------------------------
@@ -880,14 +879,6 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   if (!p.fold_rv) stage_matrix(RT, p.R_VT + (size_t)h * kHeadDim * kHeadDim, tid, kMergeThreads);
   else cp_commit();
   const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
-  // touch the partials' address range while the decode kernel still runs, so the
-  // copies below find their address translations cached (a level-2 prefetch
-  // returns no data, so what the decode kernel writes later is not bypassed)
-  if (tid < 32) {
-    const size_t span = (size_t)nslots * g * kPartFloats * 4;
-    for (size_t off = (size_t)tid * 4096; off < span; off += 32 * 4096)
-      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char*>(part) + off));
-  }
   pdl_wait();  // the partials come from the decode kernel
   pdl_trigger();
   // warp hh < nh keeps the running maximum and row sum of head hh and writes the

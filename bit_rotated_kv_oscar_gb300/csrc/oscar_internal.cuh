@@ -127,11 +127,17 @@ struct DecodeParams {
 };
 
 // Programmatic dependent launch: kernels launched with launch_pdl may start
-// while the previous kernel on the stream is still running. Each of them stages
-// constant data first, calls pdl_wait before it touches anything an earlier
-// kernel writes or reads, and only then lets its own dependents start
-// (pdl_trigger): so when a kernel starts, everything before its predecessor has
-// completed. The query rotation relies on that to run beside the append.
+// while the previous kernel on the stream is still running. Before its
+// pdl_wait a kernel touches only constant data (rotations, their images), reads
+// caller inputs that no kernel of this library writes (q, k, v) and host-set
+// fields that kernels only rewrite unchanged (a request's window row), and
+// issues level-2 prefetches, which return no data; every kernel calls pdl_wait
+// before it exits. So a kernel's predecessor completes
+// only after the predecessor's own predecessor did, and by induction everything
+// after a kernel's pdl_wait runs once all earlier kernels on the stream have
+// completed, wherever those kernels placed their pdl_trigger. The append lets
+// its dependents start at once, so that the query rotation stages R_K and
+// computes q~ beside it.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::); }
 

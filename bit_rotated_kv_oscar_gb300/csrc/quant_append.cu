@@ -87,8 +87,30 @@ oscar_quant_append_kernel(AppendParams p) {
     }
     asm volatile("cp.async.commit_group;\n" ::);
   }
-  pdl_wait();
+  // level-2 prefetches (they return no data): the request's BF16 window rows of
+  // this head, where the entry a token evicts is read, and the request's page
+  // table row (host-written). The window row index is set by the host; kernels
+  // only ever rewrite it unchanged.
+  if (blockIdx.x == 0) {
+    const int wr = p.state[b].window_row;
+    if (wr >= 0 && wr < p.max_batch) {
+      const size_t slots = (size_t)(S + W);
+      const char* wbase = reinterpret_cast<const char*>(p.window + ((size_t)wr * Hkv + h) * 2 * slots * kHeadDim);
+      const size_t wbytes = 2 * slots * kHeadDim * sizeof(__nv_bfloat16);
+      for (size_t off = (size_t)tid * 128; off < wbytes; off += (size_t)kThreads * 128)
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(wbase + off));
+    }
+    if (h == 0) {
+      const char* pt = reinterpret_cast<const char*>(p.page_table + (size_t)b * p.pt_stride);
+      const size_t pbytes = (size_t)p.pt_stride * sizeof(int32_t);
+      for (size_t off = (size_t)tid * 128; off < pbytes; off += (size_t)kThreads * 128)
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(pt + off));
+    }
+  }
+  // dependents may start now: before their own wait they touch only constant
+  // data and caller inputs
   pdl_trigger();
+  pdl_wait();
   // ticket: taken once the state is read; its value is needed only at the end,
   // where the CTA holding the last one publishes the new states
   unsigned ticket = 0u;
@@ -278,7 +300,7 @@ oscar_quant_append_kernel(AppendParams p) {
   if (tid == 0 && ticket == gridDim.x * gridDim.y * gridDim.z - 1u) {
     __threadfence();
     for (int bb = 0; bb < p.batch; ++bb) {
-      oscar_seq_state sb = p.state[bb];
+      oscar_seq_state sb = bb == b ? s_st : p.state[bb];   // this CTA's own request is at hand
       if (!state_ok(sb, S, W, p.max_batch)) continue;
       const int64_t nl = (int64_t)sb.seq_len + p.n_new;
       int64_t ne = nl - W;
