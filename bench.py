@@ -374,17 +374,15 @@ def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True
 
 
 def run_e2e(wl, args, device, i0, dist):
-    """Same steps through the public API with host buffers: per step the new
-    q / k / v go host->device from pinned memory and o comes back."""
+    """Same steps through the public API with host buffers: per step one
+    oscar_decode_step_host call copies the new q / k / v host->device from pinned
+    memory, appends, decodes and copies o back."""
     stream = torch.cuda.current_stream(device)
     # each step's q, k, v packed in one pinned host buffer: one host->device copy
     nq, nk, nv = wl.q[0].numel(), wl.k[0].numel(), wl.v[0].numel()
     hbuf = [torch.cat([wl.q[j].reshape(-1), wl.k[j].reshape(-1), wl.v[j].reshape(-1)]).cpu().pin_memory()
             for j in range(wl.n_inputs)]
     dbuf = torch.empty(nq + nk + nv, dtype=wl.q[0].dtype, device=device)
-    qd = dbuf[:nq].view(wl.q[0].shape)
-    kd = dbuf[nq:nq + nk].view(wl.k[0].shape)
-    vd = dbuf[nq + nk:].view(wl.v[0].shape)
     ho = torch.empty(wl.o.shape, dtype=wl.o.dtype).pin_memory()
     h2d = dbuf.numel() * dbuf.element_size()
     d2h = ho.numel() * 4
@@ -392,10 +390,7 @@ def run_e2e(wl, args, device, i0, dist):
     def one(k):
         ctx, cache = wl.layers[k % len(wl.layers)]
         j = k % wl.n_inputs
-        dbuf.copy_(hbuf[j], non_blocking=True)
-        ctx.quant_append(cache.page_table, cache.state, kd, vd, wl.B, 1, stream)
-        ctx.decode_attn(qd, cache.page_table, cache.state, wl.o, wl.B, stream)
-        ho.copy_(wl.o, non_blocking=True)
+        ctx.decode_step_host(cache.page_table, cache.state, hbuf[j], dbuf, wl.o, ho, wl.B, stream)
 
     for k in range(max(3, args.warmup)):
         one(i0 + k)

@@ -79,6 +79,7 @@ _SIGS = {
     "oscar_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P]),
     "oscar_decode_attn_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P]),
     "oscar_decode_attn_shared_prefix": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P]),
+    "oscar_decode_step_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int32, _P]),
     "oscar_calibration_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
     "oscar_calibration_covariances": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                      ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -257,6 +258,13 @@ class Context:
         same pages: the shared range is read once per pack of requests."""
         _check(lib().oscar_decode_attn_shared_prefix(self.handle, _ptr(q), _ptr(page_table), _ptr(state),
                                                      prefix_tokens, _ptr(o), batch, _stream(stream)), self.handle)
+
+    def decode_step_host(self, page_table, state, h_qkv, d_qkv, o, h_o, batch, stream=None):
+        """oscar_decode_step_host: one new token per request and one decode query,
+        inputs from host memory h_qkv (bf16 q, k, v back to back) through the device
+        staging buffer d_qkv, output o (device) copied to host memory h_o."""
+        _check(lib().oscar_decode_step_host(self.handle, _ptr(page_table), _ptr(state), _ptr(h_qkv), _ptr(d_qkv),
+                                            _ptr(o), _ptr(h_o), batch, _stream(stream)), self.handle)
 
     def decode_splits(self, batch):
         s = ctypes.c_int32()

@@ -90,6 +90,16 @@ int check_config_msg(const oscar_config* c, std::string* msg) {
   return OSCAR_OK;
 }
 
+// device address of page-locked host memory, nullptr for other memory
+void* mapped_host(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 int win_slots(const oscar_config* c) { return (c->sink + c->recent + kWindowChunk - 1) / kWindowChunk; }
 
 int auto_splits(const oscar_ctx* ctx, int batch) {
@@ -494,6 +504,44 @@ int oscar_decode_attn_timed(oscar_ctx* ctx, const void* q, const int32_t* page_t
                             void* ev_before, void* ev_after) {
   return decode_impl(ctx, q, page_table, state, o, batch, stream, static_cast<cudaEvent_t>(ev_before),
                      static_cast<cudaEvent_t>(ev_after));
+}
+
+int oscar_decode_step_host(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
+                           const void* h_qkv, void* d_qkv, float* o, float* h_o, int32_t batch,
+                           void* stream) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  if (!h_qkv || !h_o) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_step_host: null pointer");
+  if (batch < 1) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_step_host: batch >= 1");
+  if (batch > ctx->cfg.max_batch)
+    return fail(ctx, OSCAR_ERR_OUT_OF_RANGE, "decode_step_host: batch exceeds max_batch");
+  // page-locked host memory is addressed by the kernels directly (over the
+  // host-device link); other host memory goes through the staging buffer and
+  // the device output with copies
+  const uint8_t* in = static_cast<const uint8_t*>(mapped_host(h_qkv));
+  float* out = static_cast<float*>(mapped_host(h_o));
+  if (!in && !d_qkv) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_step_host: null pointer (d_qkv)");
+  if (!in && (reinterpret_cast<uintptr_t>(d_qkv) & 15))
+    return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_step_host: d_qkv must be 16-byte aligned");
+  if (!out && !o) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_step_host: null pointer (o)");
+  const size_t qbytes = (size_t)batch * ctx->cfg.num_q_heads * kHeadDim * sizeof(__nv_bfloat16);
+  const size_t kbytes = (size_t)batch * ctx->cfg.num_kv_heads * kHeadDim * sizeof(__nv_bfloat16);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (!in) {
+    e = cudaMemcpyAsync(d_qkv, h_qkv, qbytes + 2 * kbytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "decode_step_host: input copy");
+    in = static_cast<const uint8_t*>(d_qkv);
+  }
+  int st = append_impl(ctx, page_table, state, in + qbytes, in + qbytes + kbytes, batch, 1, nullptr, 0, stream);
+  if (st != OSCAR_OK) return st;
+  st = decode_impl(ctx, in, page_table, state, out ? out : o, batch, stream, nullptr, nullptr);
+  if (st != OSCAR_OK) return st;
+  if (!out) {
+    e = cudaMemcpyAsync(h_o, o, (size_t)batch * ctx->cfg.num_q_heads * kHeadDim * sizeof(float),
+                        cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "decode_step_host: output copy");
+  }
+  return OSCAR_OK;
 }
 
 int oscar_error_flags(oscar_ctx* ctx, uint32_t* flags, int32_t clear) {

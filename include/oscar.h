@@ -225,6 +225,29 @@ int oscar_decode_attn_shared_prefix(oscar_ctx* ctx, const void* q, const int32_t
                                     const oscar_seq_state* state, int32_t prefix_tokens, float* o,
                                     int32_t batch, void* stream);
 
+/* One serving step with host-side inputs and output: every request gets one
+ * new token, written to the cache, then one decode query over the cache that
+ * now holds it ([ES] "El sistema de servicio": the new K / V enter the BF16
+ * ring and the oldest ring entry is quantised, then the step attends over sink,
+ * ring and INT2 history).
+ * h_qkv: HOST bf16, q [batch][num_q_heads][128], then k and v
+ * [batch][num_kv_heads][128] each, back to back. h_o: HOST float32
+ * [batch][num_q_heads][128], written. On `stream`: oscar_quant_append(k, v,
+ * n_new = 1), then oscar_decode_attn(q) into the output; asynchronous, h_o
+ * holds the result once the stream has passed the call.
+ * Page-locked host memory (cudaHostAlloc / cudaHostRegister) is read and
+ * written by the kernels in place over the host-device link: then d_qkv and o
+ * are not used and may be NULL. Other host memory goes through copies: h_qkv
+ * to d_qkv (DEVICE staging buffer of the same layout and size, 16-byte
+ * aligned, caller-owned) before, and o (DEVICE float32 of h_o's size) to h_o
+ * after. h_qkv must stay unchanged until the stream has passed the call.
+ * Statuses as for those calls, and OSCAR_ERR_INVALID_ARG for a null pointer
+ * that is needed or a misaligned staging buffer, OSCAR_ERR_CUDA for a failed
+ * copy. */
+int oscar_decode_step_host(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
+                           const void* h_qkv, void* d_qkv, float* o, float* h_o, int32_t batch,
+                           void* stream);
+
 /* Number of INT2 splits per (request, KV head) decode uses for `batch`. */
 int oscar_decode_splits(const oscar_ctx* ctx, int32_t batch, int32_t* splits);
 
