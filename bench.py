@@ -50,6 +50,10 @@ FALLBACK_HBM_GBS = 6800.0
 # helpers
 # ---------------------------------------------------------------------------
 
+# GB300's nominal HBM3e bandwidth, reported beside the measured denominator
+NOMINAL_HBM_GBS = 7900.0
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -661,6 +665,7 @@ def main():
         achieved = r["kernel_bytes"] / (r["kernel_us"] * 1e-6) / 1e9
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic(r["workload"]),
+                "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
                 "kernel": "oscar_decode_kernel", "launch_us": round(r["kernel_us"], 3),
                 "algorithmic_bytes_per_launch": r["kernel_bytes"]}
@@ -703,7 +708,8 @@ def main():
                 "quant_append_us": round(pre["prefill_us"], 2),
                 "quant_append_gbs": round(ach, 1), "quant_append_frac": round(ach / peak, 4),
                 "roofline": {"bound": "hbm", "achieved": round(kach, 1), "peak": peak, "unit": "GB/s",
-                             "frac": round(kach / peak, 4),
+                             "frac": round(kach / peak, 4), "nominal_peak": NOMINAL_HBM_GBS,
+                             "frac_of_nominal": round(kach / NOMINAL_HBM_GBS, 4),
                              "traffic": profiled_traffic("prefill_128k_prefix16", "prefill"),
                              "kernel": "oscar_prefill_append_kernel",
                              "launch_us": round(pre["prefill_kernel_us"], 2),
