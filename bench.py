@@ -684,6 +684,7 @@ def main():
                        "l2": "inputs larger than L2: %d independent layer caches cycled" % main_res["layers_cycled"]},
             "decode_us": round(main_res["decode_us"], 3), "append_us": round(main_res["append_us"], 3),
             "decode_gbs": round(main_res["decode_bytes"] / (main_res["decode_us"] * 1e-6) / 1e9, 1),
+            "append_gbs": round(main_res["append_bytes"] / (main_res["append_us"] * 1e-6) / 1e9, 1),
             "roofline": roof(main_res),
             "cpu_baseline": cpu,
             "e2e": main_res["e2e"],
@@ -698,6 +699,7 @@ def main():
                 "us_per_step": round(r["us_per_step"], 3),
                 "decode_us": round(r["decode_us"], 3), "append_us": round(r["append_us"], 3),
                 "decode_gbs": round(r["decode_bytes"] / (r["decode_us"] * 1e-6) / 1e9, 1),
+                "append_gbs": round(r["append_bytes"] / (r["append_us"] * 1e-6) / 1e9, 1),
                 "roofline": roof(r), "clocks": r["clocks"], "layers_cycled": r["layers_cycled"],
             })
         if pre is not None:
