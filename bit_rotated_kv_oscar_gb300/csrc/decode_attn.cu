@@ -290,14 +290,10 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
 #pragma unroll
   for (int m = 0; m < kMaxGqa; ++m) {
     if (m < g) {
-      const uint2 w = *reinterpret_cast<const uint2*>(
-          p.q + ((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + 4 * lane);
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
-      const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
-      qr[m][0] = a.x * p.scale_log2;
-      qr[m][1] = a.y * p.scale_log2;
-      qr[m][2] = c.x * p.scale_log2;
-      qr[m][3] = c.y * p.scale_log2;
+      // element loads: q needs no alignment beyond its element size
+      const __nv_bfloat16* qp = p.q + ((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + 4 * lane;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) qr[m][e] = __bfloat162float(qp[e]) * p.scale_log2;
     } else {
       qr[m][0] = qr[m][1] = qr[m][2] = qr[m][3] = 0.f;
     }

@@ -31,11 +31,15 @@ def _vp(t, offset=0):
     return ctypes.c_void_p(t.data_ptr() + offset)
 
 
-@pytest.mark.parametrize("group,pinned", [(32, True), (64, True), (32, False)])
-def test_step_host_matches_separate_calls(group, pinned):
+@pytest.mark.parametrize("group,pinned,fold_rv,offset",
+                         [(32, True, 0, 0), (64, True, 0, 0), (32, False, 0, 0), (32, True, 1, 0),
+                          (64, True, 0, 2)])
+def test_step_host_matches_separate_calls(group, pinned, fold_rv, offset):
+    """offset: bytes the inputs start after a 16-byte boundary of the page-locked
+    buffer (2: the append reads them with plain loads instead of 16-byte copies)."""
     bsz, hq, hkv = 3, 16, 4
-    a = Layer(hq, hkv, 4, 64, bsz, 1400, seed=21, group=group)
-    b = Layer(hq, hkv, 4, 64, bsz, 1400, seed=21, group=group)
+    a = Layer(hq, hkv, 4, 64, bsz, 1400, seed=21, group=group, fold_rv=fold_rv)
+    b = Layer(hq, hkv, 4, 64, bsz, 1400, seed=21, group=group, fold_rv=fold_rv)
     for r, n in enumerate((700, 300, 65)):
         k, v = a.draw(n)
         a.append(r, k, v)
@@ -62,7 +66,11 @@ def test_step_host_matches_separate_calls(group, pinned):
         a.ctx.decode_attn(qd, a.cache.page_table, a.cache.state, o_a, bsz)
         h_qkv = torch.cat([qd.reshape(-1), kd.reshape(-1), vd.reshape(-1)]).cpu()
         if pinned:
-            h_qkv = h_qkv.pin_memory()
+            pad = offset // 2
+            buf = torch.zeros(h_qkv.numel() + pad, dtype=torch.bfloat16).pin_memory()
+            buf[pad:].copy_(h_qkv)
+            h_qkv = buf[pad:]
+            assert h_qkv.data_ptr() % 16 == offset
             b.ctx.decode_step_host(b.cache.page_table, b.cache.state, h_qkv, None, None, h_o, bsz)
         else:
             b.ctx.decode_step_host(b.cache.page_table, b.cache.state, h_qkv, d_qkv, o_b, h_o, bsz)
@@ -108,4 +116,24 @@ def test_step_host_statuses():
     torch.cuda.synchronize()
     assert tuple(layer.device_state()[0][:2]) == (layer.len[0] + 1, max(layer.e[0], layer.len[0] + 1 - 32))
     assert torch.isfinite(hop).all()
+    assert layer.ctx.error_flags() == 0
+
+
+def test_decode_query_needs_only_element_alignment():
+    # q two bytes past a 16-byte boundary gives the same output as an aligned q
+    layer = Layer(16, 4, 4, 64, 2, 900, seed=8)
+    for r, n in enumerate((500, 130)):
+        k, v = layer.draw(n)
+        layer.append(r, k, v)
+    q = layer.queries(2, 5).to(torch.bfloat16).cuda().contiguous()
+    buf = torch.zeros(q.numel() + 1, dtype=torch.bfloat16, device="cuda")
+    buf[1:].copy_(q.reshape(-1))
+    q_off = buf[1:].view(q.shape)
+    assert q_off.data_ptr() % 16 == 2
+    o1 = torch.empty(2, 16, D, device="cuda")
+    o2 = torch.empty_like(o1)
+    layer.ctx.decode_attn(q, layer.cache.page_table, layer.cache.state, o1, 2)
+    layer.ctx.decode_attn(q_off, layer.cache.page_table, layer.cache.state, o2, 2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
     assert layer.ctx.error_flags() == 0
