@@ -204,7 +204,7 @@ def test_ragged_batch_shuffled_pool():
     check_decode(layer, len(lengths), stream=99)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+@pytest.mark.parametrize("splits", [1, 2, 7, 64, 200])
 def test_split_counts(splits):
     layer = Layer(32, 8, 4, 128, 1, 5000, seed=21, num_splits=splits)
     k, v = layer.draw(5000)
