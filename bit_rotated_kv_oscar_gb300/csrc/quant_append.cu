@@ -116,7 +116,7 @@ oscar_quant_append_kernel(AppendParams p) {
   unsigned ticket = 0u;
   if (tid == 0) {
     s_st = p.state[b];
-    __threadfence();
+    asm volatile("fence.acq_rel.gpu;\n" ::: "memory");   // the state read comes before the ticket
     ticket = atomicAdd(p.counter, 1u);
   }
   asm volatile("cp.async.wait_group 0;\n" ::);  // rotations staged, visible after the barrier
@@ -298,7 +298,9 @@ oscar_quant_append_kernel(AppendParams p) {
 
   // the CTA that took the last ticket publishes the new state of every request
   if (tid == 0 && ticket == gridDim.x * gridDim.y * gridDim.z - 1u) {
-    __threadfence();
+    // every other CTA read its state before taking its ticket; the writes below
+    // come after all of those reads (kernel completion publishes them)
+    asm volatile("fence.acq_rel.gpu;\n" ::: "memory");
     for (int bb = 0; bb < p.batch; ++bb) {
       oscar_seq_state sb = bb == b ? s_st : p.state[bb];   // this CTA's own request is at hand
       if (!state_ok(sb, S, W, p.max_batch)) continue;
@@ -311,7 +313,6 @@ oscar_quant_append_kernel(AppendParams p) {
       p.state[bb] = sb;
     }
     *p.counter = 0u;
-    __threadfence();
   }
 }
 
