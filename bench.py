@@ -572,7 +572,16 @@ def oracle_step_sample(name, kv_heads_in_sample=1, seed_offset=0):
     return dt, scale
 
 
-def run_reference(args, name, rank):
+def workload_config(name, world):
+    """The JSON line's config of a workload (both arms)."""
+    spec = WORKLOADS[name]
+    return {"workload": name, "batch": spec.batch, "context": spec.context,
+            "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "head_dim": D,
+            "page": spec.page_size, "group": spec.group_size, "sink": spec.sink,
+            "recent": spec.recent, "parallelism": "replicas x%d" % world}
+
+
+def run_reference(args, name, rank, world=1):
     """The oracle as the reference arm: each step one bounded sample."""
     cores = os.cpu_count()
     times = []
@@ -584,10 +593,10 @@ def run_reference(args, name, rank):
     sample = "per step: 1 of %d KV heads of request 0 (oracle decode step: append + float64 attention " \
              "over the whole cache), scaled to the full batch" % WORKLOADS[name].num_kv_heads
     return {
-        "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": 0, "steps": args.steps,
+        "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "impl": "reference", "config": {"workload": name},
+        "impl": "reference", "config": dict(workload_config(name, world), host="oracle on the host cores"),
         "cpu_baseline": {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -619,7 +628,7 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, args.workload, rank)))
+            print(json.dumps(run_reference(args, args.workload, rank, world)))
         return
 
     dist = None
@@ -671,17 +680,13 @@ def main():
                 "algorithmic_bytes_per_launch": r["kernel_bytes"]}
 
     if rank == 0:
-        spec = WORKLOADS[args.workload]
         out = {
             "metric": METRIC, "value": round(main_res["us_per_step"], 3), "unit": "us/step",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(main_res["us_per_step"] / 1000.0, 6), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": args.workload, "batch": spec.batch, "context": spec.context,
-                       "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads, "head_dim": D,
-                       "page": spec.page_size, "group": spec.group_size, "sink": spec.sink,
-                       "recent": spec.recent, "parallelism": "replicas x%d" % world,
-                       "l2": "inputs larger than L2: %d independent layer caches cycled" % main_res["layers_cycled"]},
+            "config": dict(workload_config(args.workload, world),
+                           l2="inputs larger than L2: %d independent layer caches cycled" % main_res["layers_cycled"]),
             "decode_us": round(main_res["decode_us"], 3), "append_us": round(main_res["append_us"], 3),
             "decode_gbs": round(main_res["decode_bytes"] / (main_res["decode_us"] * 1e-6) / 1e9, 1),
             "append_gbs": round(main_res["append_bytes"] / (main_res["append_us"] * 1e-6) / 1e9, 1),
