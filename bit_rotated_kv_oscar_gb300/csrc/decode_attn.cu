@@ -50,7 +50,7 @@ constexpr int kStages = OSCAR_DEC_STAGES;
 constexpr int kStageBytes = kWarps * kStages * kBlockBytes;   // 48 KB with 4 stages
 static_assert((kStages & (kStages - 1)) == 0 && kStages >= 2, "page ring depth must be a power of two");
 constexpr int kMaxWindow = 1024;                                // sink + recent limit
-constexpr int kWinChunk = kWindowChunk;                         // window tokens per CTA
+constexpr int kWinChunk = kWindowChunkMax;                      // window tokens per CTA, at most
 
 // factor of a code read from slot i (see the file comment)
 __host__ __device__ constexpr float slot_factor(int i) {
@@ -253,14 +253,15 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
 
 // --------------------------------------------------------------------------
 // 2a. BF16 sink + recent ring: CTA x < win_slots attends over window tokens
-//     [64 x, 64 x + 64) (sink first, then the ring in position order)
+//     [c x, c x + c), c = p.win_chunk (sink first, then the ring in position
+//     order)
 // --------------------------------------------------------------------------
 __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = p.gqa, S = p.sink, W = p.recent;
-  __nv_bfloat16* krows = reinterpret_cast<__nv_bfloat16*>(smem);             // [64][128]
-  __nv_bfloat16* vrows = krows + kWinChunk * kHeadDim;                        // [64][128]
-  float* sc = reinterpret_cast<float*>(vrows + kWinChunk * kHeadDim);         // [8][64]
+  __nv_bfloat16* krows = reinterpret_cast<__nv_bfloat16*>(smem);             // [chunk][128]
+  __nv_bfloat16* vrows = krows + kWinChunk * kHeadDim;                        // [chunk][128]
+  float* sc = reinterpret_cast<float*>(vrows + kWinChunk * kHeadDim);         // [8][chunk]
   float* stat = sc + kMaxGqa * kWinChunk;                                     // [8][2]
   const int nslots = p.win_slots + p.prefix_splits + p.splits;
   float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots + chunk) * g * kPartFloats;
@@ -271,8 +272,8 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
   const int ns = ok ? min(S, L) : 0;
   const int rb = max(E, S);
   const int nr = ok && L > rb ? L - rb : 0;
-  const int t0 = chunk * kWinChunk;
-  const int n = max(0, min(kWinChunk, ns + nr - t0));
+  const int t0 = chunk * p.win_chunk;
+  const int n = max(0, min(p.win_chunk, ns + nr - t0));
   const size_t slots = (size_t)(S + W);
   const size_t wrow = ok ? (size_t)st.window_row : 0;
   const __nv_bfloat16* wk = p.window + ((wrow * p.num_kv_heads + h) * 2 + 0) * slots * kHeadDim;
@@ -850,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
 //    waits for the level-2 cache once.
 // --------------------------------------------------------------------------
 constexpr int kMergeThreads = 256;
-constexpr int kMaxSlots = 256 + kMaxWindow / kWinChunk;   // INT2 splits + window chunks
+constexpr int kMaxSlots = 256 + kMaxWindow / kWindowChunkSmall;   // INT2 splits + window chunks
 constexpr int kMergeChunk = 64;                            // slots staged per round
 // floats of the staged rows (also the un-rotation partials, 4 x 128 floats)
 __host__ __device__ constexpr int merge_rows_floats(int nslots) {
@@ -1001,6 +1002,7 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
     attr_set = true;
   }
   if (p.win_slots + p.prefix_splits + p.splits > kMaxSlots) return cudaErrorInvalidValue;
+  if (p.win_chunk < 1 || p.win_chunk > kWinChunk) return cudaErrorInvalidValue;
   cudaError_t e = launch_pdl(oscar_rotate_q_kernel, dim3(p.num_kv_heads, batch), dim3(kRotThreads), kRotSmem,
                              s, p);
   if (e == cudaSuccess && ev_before) e = cudaEventRecord(ev_before, s);

@@ -43,7 +43,7 @@ int noalloc_splits(const oscar_config* c, int num_sms, int batch) {
   if (c->num_splits > 0) return c->num_splits;
   const int64_t units = (int64_t)batch * c->num_kv_heads;
   const int64_t pages = c->max_pages_per_seq;
-  const int64_t wins = units * ((c->sink + c->recent + kWindowChunk - 1) / kWindowChunk);
+  const int64_t wins = units * window_slots(c->sink + c->recent, window_chunk(c->sink + c->recent, units, num_sms));
   int64_t by_wave = (kDecodeCtasPerSm * (int64_t)num_sms - wins) / units;
   int64_t by_pages = (pages + kSplitPages - 1) / kSplitPages;
   int64_t s = by_wave > by_pages ? by_wave : by_pages;
@@ -105,7 +105,8 @@ extern "C" int oscar_decode_attn_noalloc(const oscar_config* cfg, const void* q,
 
   const int hkv = cfg->num_kv_heads, g = cfg->num_q_heads / cfg->num_kv_heads;
   const int splits = noalloc_splits(cfg, num_sms, batch);
-  const int win_slots = (cfg->sink + cfg->recent + kWindowChunk - 1) / kWindowChunk;
+  const int win_chunk = window_chunk(cfg->sink + cfg->recent, (int64_t)batch * cfg->num_kv_heads, num_sms);
+  const int win_slots = window_slots(cfg->sink + cfg->recent, win_chunk);
   // scratch layout: R_V^T | pv_scale | error word | q~ records | split-K partials
   const size_t off_rvt = 0;
   const size_t off_pv = off_rvt + round256((size_t)hkv * kHeadDim * kHeadDim * sizeof(float));
@@ -162,6 +163,7 @@ extern "C" int oscar_decode_attn_noalloc(const oscar_config* cfg, const void* q,
   p.fold_rv = cfg->fold_rv;
   p.max_batch = cfg->max_batch;
   p.win_slots = win_slots;
+  p.win_chunk = win_chunk;
   const float scale = cfg->softmax_scale == 0.f ? 1.f / sqrtf((float)kHeadDim) : cfg->softmax_scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.err_flags = flags;

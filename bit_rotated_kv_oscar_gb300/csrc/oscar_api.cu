@@ -100,7 +100,11 @@ void* mapped_host(const void* p) {
   return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
-int win_slots(const oscar_config* c) { return (c->sink + c->recent + kWindowChunk - 1) / kWindowChunk; }
+// window CTAs per (request, KV head): at most this many (the short chunks)
+int win_slots(const oscar_config* c) { return window_slots(c->sink + c->recent, kWindowChunkSmall); }
+int win_chunk_for(const oscar_ctx* ctx, int batch) {
+  return window_chunk(ctx->cfg.sink + ctx->cfg.recent, (int64_t)batch * ctx->cfg.num_kv_heads, ctx->num_sms);
+}
 
 int auto_splits(const oscar_ctx* ctx, int batch) {
   if (ctx->cfg.num_splits > 0) return ctx->cfg.num_splits;
@@ -108,7 +112,7 @@ int auto_splits(const oscar_ctx* ctx, int batch) {
   const int64_t pages = ctx->cfg.max_pages_per_seq;
   // fill one wave of decode CTAs together with the BF16-window CTAs; at most
   // kSplitPages pages per CTA
-  const int64_t wins = units * win_slots(&ctx->cfg);
+  const int64_t wins = units * window_slots(ctx->cfg.sink + ctx->cfg.recent, win_chunk_for(ctx, batch));
   int64_t by_wave = (kDecodeCtasPerSm * (int64_t)ctx->num_sms - wins) / units;
   int64_t by_pages = (pages + kSplitPages - 1) / kSplitPages;
   int64_t s = by_wave > by_pages ? by_wave : by_pages;
@@ -470,7 +474,8 @@ static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table,
   p.ngroups = kHeadDim / ctx->cfg.group_size;
   p.recent = ctx->cfg.recent;
   p.splits = auto_splits(ctx, batch);
-  p.win_slots = win_slots(&ctx->cfg);
+  p.win_chunk = win_chunk_for(ctx, batch);
+  p.win_slots = window_slots(ctx->cfg.sink + ctx->cfg.recent, p.win_chunk);
   p.batch = batch;
   p.prefix_tokens = 0;
   p.prefix_splits = 0;

@@ -42,7 +42,11 @@ constexpr int kMaxGqa = 8;
 // the per-group sums of q~ (hi/lo), [1088] the score scale, rest zero
 constexpr int kQrecWords = 1104;
 constexpr int kPartFloats = kHeadDim + 4;    // o[128], m, l, 2 pad (rows stay 16-byte aligned)
-constexpr int kWindowChunk = 64;             // BF16 window tokens per decode CTA
+// BF16 window tokens per decode CTA: short chunks while the window CTAs are few
+// (they then run beside the INT2 CTAs, and their latency is what counts), long
+// ones when they are many (fewer CTAs: less fixed cost per token)
+constexpr int kWindowChunkSmall = 64;
+constexpr int kWindowChunkMax = 160;
 // INT2 pages one decode CTA streams at most when the split count is automatic
 #ifndef OSCAR_SPLIT_PAGES
 #define OSCAR_SPLIT_PAGES 512
@@ -50,6 +54,12 @@ constexpr int kWindowChunk = 64;             // BF16 window tokens per decode CT
 constexpr int kSplitPages = OSCAR_SPLIT_PAGES;
 // decode CTAs resident per SM (registers and shared memory are sized for it)
 constexpr int kDecodeCtasPerSm = 2;
+// window chunk of a decode call with `units` (request, KV head) pairs
+inline int window_chunk(int window_tokens, int64_t units, int num_sms) {
+  const int64_t small = units * ((window_tokens + kWindowChunkSmall - 1) / kWindowChunkSmall);
+  return 4 * small <= (int64_t)kDecodeCtasPerSm * num_sms ? kWindowChunkSmall : kWindowChunkMax;
+}
+inline int window_slots(int window_tokens, int chunk) { return (window_tokens + chunk - 1) / chunk; }
 
 struct AppendParams {
   const int32_t* page_table;
@@ -114,7 +124,8 @@ struct DecodeParams {
   float* o;                 // [B][Hq][128]
   const float* pv_scale;    // [Hkv] power of two applied to p * s_v before fp16 rounding
   int32_t num_q_heads, num_kv_heads, gqa, sink, recent, splits, fold_rv, max_batch;
-  int32_t win_slots;        // CTAs over the BF16 window, 64 tokens each
+  int32_t win_slots;        // CTAs over the BF16 window, win_chunk tokens each
+  int32_t win_chunk;        // kWindowChunkSmall or kWindowChunkMax (window_chunk)
   int32_t ngroups;          // quantisation groups per token: 128 / group_size (4 or 2)
   int32_t batch;            // requests of this call
   // shared prefix: requests 0 .. batch-1 map positions [0, prefix_tokens) to the
