@@ -12,9 +12,9 @@
 //      written as ready-to-use tensor-core operand fragments (fp16 hi + lo).
 //   2. oscar_decode_kernel<NG> grid (window chunks + prefix splits + splits, Hkv,
 //      B), NG = 128 / group size: the first CTAs attend over the BF16 sink +
-//      recent ring in the raw basis (64 tokens each); the others stream a slice
-//      of the INT2 pages, computing scores and the P.V product on the tensor
-//      cores with exact 2-bit operands, in the R_V basis. With a shared prefix
+//      recent ring in the raw basis (64 or 160 tokens each, per call); the
+//      others stream a slice of the INT2 pages, computing scores and the P.V
+//      product on the tensor cores with exact 2-bit operands, in the R_V basis. With a shared prefix
 //      (oscar_decode_attn_shared_prefix) the prefix CTAs attend over the shared
 //      pages once for a pack of requests, their query heads side by side in the
 //      tensor-core columns, and the per-request CTAs over what follows.
