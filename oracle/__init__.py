@@ -19,7 +19,9 @@ Parity status per function (what pins it, see tests/test_oracle_*.py):
   bit_reverse_index / matrix ...... pinned (textbook d=8 table, tier property)
   query_covariance ................ pinned (logit-error identity, closed form)
   score_weighted_value_covariance . pinned (brute-force double sum)
-  eig_desc / composite_rotation ... pinned (orthogonality, Lemma 1 on R^T C R)
+  eig_desc / composite_rotation ... pinned (orthogonality, Lemma 1 on R^T C R, key logit
+                                    error below Hadamard-only when keys share the
+                                    queries' leading directions)
   quantize_groups ................. pinned (brute force over all code vectors)
   layout codec .................... pinned (hand-worked byte fixture, round trip)
   decode_attention ................ pinned (torch SDPA float64, rotation equivalence)

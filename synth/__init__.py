@@ -16,6 +16,7 @@ from .generators import (  # noqa: F401
     query_basis,
     draw_kv,
     draw_queries,
+    draw_shared_direction_qk,
     draw_page_pool,
     draw_ragged_lengths,
 )

@@ -181,6 +181,27 @@ def draw_queries(seed: int, stream: int, n_tokens: int, num_q_heads: int, num_kv
     return q.to(torch.bfloat16).to(torch.float32).contiguous()
 
 
+def draw_shared_direction_qk(seed: int, stream: int, n_tokens: int, head_dim: int,
+                             n_shared: int = 4, shared_mult: float = 20.0, decay: float = 0.9):
+    """One head's queries and keys that share their leading directions.
+
+    Queries as in ``draw_queries`` (covariance B diag(decay**i) B^T, B the random
+    orthonormal basis of KV head 0); keys i.i.d. N(0, 1) plus independent
+    N(0, shared_mult**2) components along the first ``n_shared`` columns of B,
+    so the keys' large components lie along the queries' high-energy
+    directions, the structure query and key projections of one attention head
+    have in common. Returns bf16-exact float32 tensors (q [n, d], k [n, d]).
+    """
+    basis = torch.as_tensor(query_basis(seed, 1, head_dim)[0], dtype=torch.float32)
+    sd = torch.tensor([decay ** (0.5 * i) for i in range(head_dim)], dtype=torch.float32)
+    g = _gen(seed, 7000 + stream)
+    q = (torch.randn(n_tokens, head_dim, generator=g) * sd) @ basis.T
+    k = torch.randn(n_tokens, head_dim, generator=g)
+    k = k + (torch.randn(n_tokens, n_shared, generator=g) * shared_mult) @ basis[:, :n_shared].T
+    return (q.to(torch.bfloat16).to(torch.float32).contiguous(),
+            k.to(torch.bfloat16).to(torch.float32).contiguous())
+
+
 # --------------------------------------------------------------------------
 # Paging
 # --------------------------------------------------------------------------

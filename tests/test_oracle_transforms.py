@@ -106,3 +106,18 @@ def test_composite_rotation_orthogonal_and_equalises(seed):
     assert np.allclose(np.diag(r.T @ c @ r), np.trace(c) / d, rtol=1e-10, atol=0)
     r_bad = hadamard(d) @ u @ bit_reversal_matrix(d)
     assert not np.allclose(np.diag(r_bad.T @ c @ r_bad), np.trace(c) / d, rtol=1e-3)
+
+
+@pytest.mark.parametrize("group", [16, 32, 64])
+def test_leading_axes_become_group_offsets(group):
+    # why R = U_Q H P_br protects the queries' leading directions at INT2: after
+    # U_Q (eigenvalues descending) those directions are the first coordinate
+    # axes; H maps axis i to the i-th Sylvester row, and after P_br rows
+    # 0 .. d/group - 1 are constant inside every group of `group` consecutive
+    # channels, so a key component along them is a per-group offset that the
+    # asymmetric zero point absorbs. Checked row by row: exactly those rows are
+    # group-constant.
+    d = 128
+    hp = hadamard(d) @ bit_reversal_matrix(d)
+    const = [i for i in range(d) if np.all(np.ptp(hp[i].reshape(-1, group), axis=1) == 0)]
+    assert const == list(range(d // group))
