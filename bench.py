@@ -540,10 +540,11 @@ def footprint(name):
 # CPU oracle timing (the reference arm and the cpu_baseline leg)
 # ---------------------------------------------------------------------------
 
-def oracle_step_sample(name, kv_heads_in_sample=1, seed_offset=0):
+def oracle_step_sample(name, kv_heads_in_sample=1, seed_offset=0, runs=1):
     """Time one oracle decode step (append of one token + float64 attention over
-    the whole cache) for request 0 restricted to `kv_heads_in_sample` KV heads.
-    Returns (seconds, scale) where scale converts to one full batch step."""
+    the whole cache) for request 0 restricted to `kv_heads_in_sample` KV heads,
+    `runs` times on the same cache. Returns (seconds per run, scale) where scale
+    converts one run to one full batch step."""
     import oracle
     from oracle import OracleCache, decode_attention, next_state
 
@@ -560,16 +561,75 @@ def oracle_step_sample(name, kv_heads_in_sample=1, seed_offset=0):
     L0, E0 = next_state(0, spec.sink, L, spec.recent, spec.sink)
     cache = OracleCache(cal["R_K32"], cal["R_V32"], cal["clip_K32"], cal["clip_V32"], spec.sink)
     cache.build(k, v, L0, E0)
-    t0 = time.perf_counter()
-    # the appended token evicts one ring entry: rotate + quantise it (K and V), then attend
-    p = max(E0, spec.sink)
-    for x, r, c in ((k, cal["R_K32"], cal["clip_K32"]), (v, cal["R_V32"], cal["clip_V32"])):
-        xr = np.einsum("nhi,hij->nhj", x[p:p + 1].astype(np.float64), r.astype(np.float64))
-        oracle.quantize_groups(xr.astype(np.float32), c.reshape(1, -1, 1))
-    decode_attention(q, cache)
-    dt = time.perf_counter() - t0
+    times = []
+    for _ in range(runs):
+        t0 = time.perf_counter()
+        # the appended token evicts one ring entry: rotate + quantise it (K and V), then attend
+        p = max(E0, spec.sink)
+        for x, r, c in ((k, cal["R_K32"], cal["clip_K32"]), (v, cal["R_V32"], cal["clip_V32"])):
+            xr = np.einsum("nhi,hij->nhj", x[p:p + 1].astype(np.float64), r.astype(np.float64))
+            oracle.quantize_groups(xr.astype(np.float32), c.reshape(1, -1, 1))
+        decode_attention(q, cache)
+        times.append(time.perf_counter() - t0)
     scale = spec.batch * spec.num_kv_heads / hkv
-    return dt, scale
+    return (times[0] if runs == 1 else times), scale
+
+
+def oracle_prefill_sample(tokens=8192, runs=3):
+    """Time the oracle's write path of the 131072-token prefill (rotate in float64,
+    clip, quantise, pack into page blocks; K and V) on `tokens` tokens of one KV
+    head, `runs` times. Returns (seconds per run, scale to the whole prefill)."""
+    import oracle
+
+    spec = WORKLOADS["prefill_128k_prefix16"]
+    q_cal = draw_queries(spec.seed, 900, 512, spec.gqa, 1, D).numpy()
+    k_cal, v_cal = (t.numpy() for t in draw_kv(spec.seed, 900, 512, 1, D))
+    cal = oracle.calibrate(q_cal, k_cal, v_cal)
+    k, v = (t.numpy() for t in draw_kv(spec.seed, 1, tokens, 1, D))
+    times = []
+    for _ in range(runs):
+        t0 = time.perf_counter()
+        out = []
+        for x, r, c in ((k, cal["R_K32"], cal["clip_K32"]), (v, cal["R_V32"], cal["clip_V32"])):
+            xr = np.einsum("nhi,hij->nhj", x.astype(np.float64), r.astype(np.float64))
+            out.append(oracle.quantize_groups(xr.astype(np.float32), c.reshape(1, -1, 1)))
+        (kc, ks, kz), (vc, vs, vz) = out
+        npg = tokens // 16
+        oracle.encode_page_block(kc[:, 0].reshape(npg, 16, D), vc[:, 0].reshape(npg, 16, D),
+                                 ks[:, 0].reshape(npg, 16, -1), kz[:, 0].reshape(npg, 16, -1),
+                                 vs[:, 0].reshape(npg, 16, -1), vz[:, 0].reshape(npg, 16, -1))
+        times.append(time.perf_counter() - t0)
+    return times, spec.context / tokens * spec.num_kv_heads
+
+
+def blas_threads():
+    """Threads of the BLAS numpy is linked against (threadpoolctl when present,
+    else the OpenBLAS entry point found among the loaded libraries), or None."""
+    try:
+        import threadpoolctl
+        info = [d for d in threadpoolctl.threadpool_info() if d.get("user_api") == "blas"]
+        if info:
+            return int(info[0]["num_threads"])
+    except Exception:
+        pass
+    try:
+        import ctypes
+        libs = set()
+        with open("/proc/self/maps") as f:
+            for line in f:
+                path = line.split()[-1]
+                if "openblas" in path.lower() and ".so" in path:
+                    libs.add(path)
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                        "openblas_get_num_threads"):
+                fn = getattr(lib, sym, None)
+                if fn is not None:
+                    return int(fn())
+    except Exception:
+        pass
+    return None
 
 
 def workload_config(name, world):
@@ -660,11 +720,16 @@ def main():
     pre = None if args.no_prefill else run_prefill(args, device, rank, dist)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        dt, scale = oracle_step_sample(args.workload, 2)
-        cpu = {"value": dt * scale * 1e6, "unit": "us/step", "cores": os.cpu_count(), "kind": "oracle",
+        ts, scale = oracle_step_sample(args.workload, 2, runs=3)
+        pts, pscale = oracle_prefill_sample()
+        cpu = {"value": float(np.median(ts)) * scale * 1e6, "unit": "us/step", "cores": os.cpu_count(),
+               "blas_threads": blas_threads(), "kind": "oracle", "runs": 3, "statistic": "median",
                "sample": "one decode step (append + float64 attention over the whole cache) of KV heads "
-                         "0-1 of request 0, scaled to all %d KV heads x %d requests" %
-                         (WORKLOADS[args.workload].num_kv_heads, WORKLOADS[args.workload].batch)}
+                         "0-1 of request 0, scaled to all %d KV heads x %d requests; median of 3" %
+                         (WORKLOADS[args.workload].num_kv_heads, WORKLOADS[args.workload].batch),
+               "prefill_us": round(float(np.median(pts)) * pscale * 1e6, 1),
+               "prefill_sample": "131072-token prefill write path (float64 rotation, clip, quantise, pack; "
+                                 "K and V): 8192 tokens of 1 of 8 KV heads, scaled by %d; median of 3" % pscale}
 
     def roof(r):
         # the dominant kernel: split-K attention over the paged cache; algorithmic
@@ -684,7 +749,7 @@ def main():
             "metric": METRIC, "value": round(main_res["us_per_step"], 3), "unit": "us/step",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(main_res["us_per_step"] / 1000.0, 6), "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16 hi+lo q~ x u2 codes (mma.sync), f32 accumulate", "data": "synthetic",
             "config": dict(workload_config(args.workload, world),
                            l2="inputs larger than L2: %d independent layer caches cycled" % main_res["layers_cycled"]),
             "decode_us": round(main_res["decode_us"], 3), "append_us": round(main_res["append_us"], 3),
@@ -729,6 +794,19 @@ def main():
             }
         out["footprint"] = [footprint(n) for n in ("qwen3_32b_bs28_100k", "qwen3_8b_bs1_32k",
                                                    "qwen3_32b_bs28_100k_pages", "qwen3_8b_bs1_32k_pages")]
+        # one flat object per further decode workload, last on the line, so a
+        # reader that keeps only top-level scalars (or only the line's tail) still
+        # has each workload's kernel time and roofline fraction
+        short = {"qwen3_32b_bs28_100k": "bs28_100k", "qwen3_8b_bs16_ragged": "bs16_ragged",
+                 "qwen3_32b_bs28_100k_pages": "bs28_100k_pages"}
+        for r in extras:
+            rf = roof(r)
+            out[short.get(r["workload"], r["workload"])] = {
+                "workload": r["workload"], "kernel_us": round(r["kernel_us"], 2),
+                "kernel_gbs": rf["achieved"], "frac": rf["frac"], "frac_of_nominal": rf["frac_of_nominal"],
+                "traffic": rf["traffic"], "kernel_bytes": r["kernel_bytes"],
+                "decode_us": round(r["decode_us"], 2), "us_per_step": round(r["us_per_step"], 2),
+                "sm_mhz": r["clocks"].get("sm_mhz"), "clock_reasons": ",".join(r["clocks"].get("reasons", []))}
         print(json.dumps(out))
     if dist:
         dist.destroy_process_group()

@@ -37,7 +37,7 @@ def _sources():
 
 def _deps():
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
-        [os.path.join(ROOT, "include", "oscar.h")]
+        sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [os.path.join(ROOT, "include", "oscar.h")]
 
 
 def up_to_date() -> bool:

@@ -155,13 +155,11 @@ size_t calib_workspace_bytes(int n, int hq) { return (size_t)hq * n * kHeadDim *
 cudaError_t launch_calib_covariances(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v, int n,
                                      int hq, int hkv, float scale, float* c_q, float* c_s, float* o_ws,
                                      cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(oscar_calib_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCalSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attrs;
+  const cudaError_t ea = once_for_current_device(attrs, [] {
+    return cudaFuncSetAttribute(oscar_calib_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCalSmem);
+  });
+  if (ea != cudaSuccess) return ea;
   oscar_calib_attention_kernel<<<dim3((n + kCalRows - 1) / kCalRows, hq), kCalThreads, kCalSmem, s>>>(
       q, k, v, n, hq, hkv, scale * 1.4426950408889634f, o_ws);
   oscar_calib_cov_kernel<<<dim3(kHeadDim / 32, hkv, 2), kCovThreads, 0, s>>>(q, o_ws, n, hq, hkv, c_q, c_s);

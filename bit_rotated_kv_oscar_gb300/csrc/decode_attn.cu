@@ -987,9 +987,9 @@ int decode_smem_bytes() {
 
 cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cudaEvent_t ev_before,
                           cudaEvent_t ev_after) {
-  static bool attr_set = false;
+  static PerDeviceOnce attrs;
   const int smem = decode_smem_bytes();
-  if (!attr_set) {
+  cudaError_t ea = once_for_current_device(attrs, [&] {
     cudaError_t e =
         cudaFuncSetAttribute(oscar_decode_kernel<kGroups>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
@@ -998,9 +998,9 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
       e = cudaFuncSetAttribute(oscar_rotate_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(oscar_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   if (p.win_slots + p.prefix_splits + p.splits > kMaxSlots) return cudaErrorInvalidValue;
   if (p.win_chunk < 1 || p.win_chunk > kWinChunk) return cudaErrorInvalidValue;
   cudaError_t e = launch_pdl(oscar_rotate_q_kernel, dim3(p.num_kv_heads, batch), dim3(kRotThreads), kRotSmem,

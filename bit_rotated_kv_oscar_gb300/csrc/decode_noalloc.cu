@@ -32,7 +32,6 @@ static __device__ __align__(256) uint8_t oscar_noalloc_scratch[kNoallocScratchBy
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch[kMaxDevices] = {};
 

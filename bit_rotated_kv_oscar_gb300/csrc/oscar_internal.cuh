@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "../../include/oscar.h"
+#include "per_device_once.h"
 
 namespace oscar {
 
@@ -149,6 +150,14 @@ struct DecodeParams {
 // completed, wherever those kernels placed their pdl_trigger. The append lets
 // its dependents start at once, so that the query rotation stages R_K and
 // computes q~ beside it.
+// One exception to "constant data": the no-alloc decode keeps R_V^T and the
+// probability scales in its shared scratch array and rewrites them at every
+// call with an ordinary (non-overlapping) preparation launch, while the merge
+// kernel stages R_V^T before its pdl_wait. That stays ordered because the
+// decode kernel, the merge's predecessor, triggers its dependents only after
+// its own pdl_wait, which runs after the query rotation and hence after the
+// preparation kernel. A decode kernel that triggered before its wait would let
+// the merge read the previous call's R_V^T.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::); }
 
@@ -166,6 +175,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// run `setup` (returning a cudaError_t) once for the current device
+template <typename F>
+cudaError_t once_for_current_device(PerDeviceOnce& once, F&& setup) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int r = once.run_on(dev, [&] { return (int)setup(); });
+  return r < 0 ? cudaErrorInvalidDevice : (cudaError_t)r;
 }
 
 // launchers (return cudaGetLastError())

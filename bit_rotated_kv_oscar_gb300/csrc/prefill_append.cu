@@ -472,15 +472,15 @@ bool prefill_supported(const void* k, const void* v) {
 
 cudaError_t launch_prefill_append(const PrefillParams& p_in, int ctas_per_head, cudaStream_t s,
                                   cudaEvent_t ev_before, cudaEvent_t ev_after) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceOnce attrs;
+  const cudaError_t ea = once_for_current_device(attrs, [] {
     cudaError_t e = cudaFuncSetAttribute(oscar_prefill_append_kernel<kGroups>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(oscar_prefill_append_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   if (p_in.ngroups != kGroups && p_in.ngroups != 2) return cudaErrorInvalidValue;
   PrefillParams p = p_in;
   if (!encode_map(&p.tmap_k, p.k, p.num_kv_heads, p.n_new, p.batch) ||

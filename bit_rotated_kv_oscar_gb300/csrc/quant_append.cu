@@ -318,20 +318,18 @@ oscar_quant_append_kernel(AppendParams p) {
 
 cudaError_t launch_quant_append(const AppendParams& p, cudaStream_t s, cudaEvent_t ev_before,
                                 cudaEvent_t ev_after) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(oscar_quant_append_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || num_sms < 1)
-      num_sms = 1;
-  }
+  static PerDeviceOnce attrs;
+  static PerDeviceValue sm_count;
+  const cudaError_t ea = once_for_current_device(attrs, [] {
+    return cudaFuncSetAttribute(oscar_quant_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem);
+  });
+  if (ea != cudaSuccess) return ea;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const int num_sms = sm_count.get(dev, [dev] {
+    int n = 0;
+    return cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0 ? n : 1;
+  });
   // tokens are walked one after another inside a CTA: spread them over one wave
   // of CTAs (one per SM), at most kMaxTokensPerCta each
   AppendParams q = p;

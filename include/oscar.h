@@ -178,7 +178,8 @@ int oscar_load_rotations(oscar_ctx* ctx, const float* R_K, const float* R_V,
  * position below the new int2_end. state: DEVICE [batch], read and updated.
  * With E' = max(E, sink, L + n_new - recent): positions below sink go to the
  * sink, positions in [E, E') are rotated (x @ R), clipped to [-c, c],
- * quantised per group of 32 channels with s = fp16((max-min)/3), z = fp16(min),
+ * quantised per group of group_size channels (32 or 64, from the config) with
+ * s = fp16((max-min)/3), z = fp16(min),
  * code = clamp(rint((x - z) * fp32(1/s)), 0, 3) (0 when s == 0), and packed; taken from
  * the ring when already cached, else from k/v. The remaining new positions go
  * to the ring. Afterwards state = {L + n_new, E'}. */
