@@ -86,6 +86,15 @@ __device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t 
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
+// d = a b with k = 8 (a: rows gid / gid + 8 at k 2 tig, 2 tig + 1; b: k 2 tig, 2 tig + 1
+// of column gid)
+__device__ __forceinline__ void mma1688_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%7,%7,%7};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0), "f"(0.f));
+}
+
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
@@ -389,20 +398,18 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
     constexpr int zpair = kzero_off(NG, 8, 0) - kzero_off(NG, 0, 0);  // token gid + 8
     const bool zon = NG == kGroups || tig < 2;
     float zA[4], zB[4];
-    mma16816_z(zA, zon ? *reinterpret_cast<const uint32_t*>(sbA + zo) : 0u,
-               zon ? *reinterpret_cast<const uint32_t*>(sbA + zo + zpair) : 0u, 0u, 0u, zqb, 0u);
-    mma16816_z(zB, zon ? *reinterpret_cast<const uint32_t*>(sbB + zo) : 0u,
-               zon ? *reinterpret_cast<const uint32_t*>(sbB + zo + zpair) : 0u, 0u, 0u, zqb, 0u);
+    mma1688_z(zA, zon ? *reinterpret_cast<const uint32_t*>(sbA + zo) : 0u,
+              zon ? *reinterpret_cast<const uint32_t*>(sbA + zo + zpair) : 0u, zqb);
+    mma1688_z(zB, zon ? *reinterpret_cast<const uint32_t*>(sbB + zo) : 0u,
+              zon ? *reinterpret_cast<const uint32_t*>(sbB + zo + zpair) : 0u, zqb);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       u[i] = zA[i];
       u[4 + i] = zB[i];
     }
   }
-  // K scales of tokens gid (pair 0) and gid + 8 (pair 1): halves at
-  // 1024 + 8 NG (gid / 2) + 8 gq + 2 (gid % 2) and 4 bytes further
-  const int so = kscale_off(NG, gid & ~1, 0);
-  const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
+  // K scales of tokens gid and gid + 8: the two halves of word gq at kscale_off(gid, gq)
+  const int so = kscale_off(NG, gid, 0);
 #pragma unroll
   for (int gq = 0; gq < NG; ++gq) {
     float a[4], c[4];
@@ -428,10 +435,8 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
       if (gq == 1) { OSCAR_QK(4, mma16816_z) OSCAR_QK(5, mma16816) OSCAR_QK(6, mma16816) OSCAR_QK(7, mma16816) }
     }
 #undef OSCAR_QK
-    const uint2 kA = *reinterpret_cast<const uint2*>(sbA + so + 8 * gq);
-    const uint2 kB = *reinterpret_cast<const uint2*>(sbB + so + 8 * gq);
-    const float2 sA = h2_bits_to_f2(__byte_perm(kA.x, kA.y, sel));   // (token gid, token gid + 8)
-    const float2 sB = h2_bits_to_f2(__byte_perm(kB.x, kB.y, sel));
+    const float2 sA = h2_bits_to_f2(*reinterpret_cast<const uint32_t*>(sbA + so + 4 * gq));  // (gid, gid + 8)
+    const float2 sB = h2_bits_to_f2(*reinterpret_cast<const uint32_t*>(sbB + so + 4 * gq));
     u[0] = fmaf(sA.x, a[0], u[0]);
     u[1] = fmaf(sA.x, a[1], u[1]);
     u[2] = fmaf(sA.y, a[2], u[2]);
@@ -467,10 +472,10 @@ __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_
   constexpr int vbase = vscale_off(NG, 0, 0);
 #pragma unroll
   for (int gq = 0; gq < NG; ++gq) {
+    // scales of tokens (2 tig, 2 tig + 1) and (2 tig + 8, 2 tig + 9): one 8-byte load
     const uint2 mv = *reinterpret_cast<const uint2*>(sb + vbase + 16 * (4 * gq + tig));
-    const uint2 mv2 = *reinterpret_cast<const uint2*>(sb + vbase + 16 * (4 * gq + tig) + 8);
     const uint32_t B0 = hmul2_bits(P01, mv.x);
-    const uint32_t B1 = hmul2_bits(P23, mv2.x);
+    const uint32_t B1 = hmul2_bits(P23, mv.y);
 #define OSCAR_PV(CB)                                                                          \
   mma16816(acc[CB], slot_bits<CB>(vw.x, vwh.x), slot_bits<CB>(vw.y, vwh.y), slot_bits<CB>(vw.z, vwh.z),   \
            slot_bits<CB>(vw.w, vwh.w),                                                                    \
@@ -487,10 +492,10 @@ __device__ __forceinline__ void page_values(const uint8_t* sb, int lane, uint32_
 #undef OSCAR_PV
   }
   // rows 0 .. NG-1: the value zeros of the groups; row 4: ones
-  const uint8_t* mz = sb + vbase + 16 * (4 * (gid & (NG - 1)) + tig);
   constexpr uint32_t kOnes = 0x3c003c00u;  // fp16 (1, 1)
-  const uint32_t za0 = gid < NG ? *reinterpret_cast<const uint32_t*>(mz + 4) : (gid == 4 ? kOnes : 0u);
-  const uint32_t za2 = gid < NG ? *reinterpret_cast<const uint32_t*>(mz + 12) : (gid == 4 ? kOnes : 0u);
+  uint2 mz = make_uint2(gid == 4 ? kOnes : 0u, gid == 4 ? kOnes : 0u);
+  if (gid < NG) mz = *reinterpret_cast<const uint2*>(sb + vbase + 16 * (4 * gid + tig) + 8);
+  const uint32_t za0 = mz.x, za2 = mz.y;
   mma16816(oz, za0, 0u, za2, 0u, P01, P23);
 }
 
@@ -503,7 +508,7 @@ __device__ __forceinline__ uint32_t page_token_bits(bool ok, int pos, int lo, in
 // zero the value scales and zeros of the tokens of two staged pages whose bit in
 // `valid` is clear (bit t: page A token t, bit 16 + t: page B token t); lane:
 // page lane / 16, 16-byte chunk c = 4 g + bb of the value metadata, whose 32-bit
-// word w holds tokens 8 (w / 2) + 2 bb and + 1 (scales for even w, zeros for odd)
+// word w holds tokens 8 (w % 2) + 2 bb and + 1 (scales for w < 2, zeros after)
 template <int NG>
 __device__ __forceinline__ void zero_masked_value_meta(uint8_t* sbA, uint8_t* sbB, uint32_t valid, int lane) {
   const int c = lane & 15;
@@ -513,7 +518,7 @@ __device__ __forceinline__ void zero_masked_value_meta(uint8_t* sbA, uint8_t* sb
   uint32_t keep[4];
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    const int tw = 8 * (w >> 1) + 2 * (c & 3);
+    const int tw = 8 * (w & 1) + 2 * (c & 3);
     keep[w] = (((vpage >> tw) & 1u) ? 0x0000ffffu : 0u) | (((vpage >> (tw + 1)) & 1u) ? 0xffff0000u : 0u);
   }
   uint4 x = *chunk;
@@ -597,8 +602,6 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   constexpr int kBB = block_bytes(NG);
   const uint8_t* pool_h = p.pool + (size_t)h * kBB + lane * 16;
   const size_t page_stride = (size_t)p.num_kv_heads * kBB;
-  unsigned valid_bits = 0;  // bit (j % kStages): page j of this warp has a valid id
-
   // page ids of this warp's first 64 pages, two per lane, loaded once together with
   // their validity (a ballot); pages beyond that, possible only with more than 512
   // pages per split, load on use. A page whose id is outside the pool is not
@@ -609,22 +612,23 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   const uint32_t good1 = __ballot_sync(0xffffffffu, id1 >= 0 && id1 < p.num_pages);
   bool bad_id = good0 != 0xffffffffu || good1 != 0xffffffffu;
   const uint32_t stride = (uint32_t)page_stride;   // heads x 1536 bytes, far below 2^32
-  // stage page j into ring slot sl (= j % kStages)
-  auto issue = [&](int j, int sl) {
+  // id of page j of this warp and whether it lies in the pool
+  auto page_id = [&](int j, bool& good) {
     int id;
-    bool good;
-    if (j < 32) {
-      id = __shfl_sync(0xffffffffu, id0, j);
-      good = (good0 >> j) & 1u;
-    } else if (j < 64) {
-      id = __shfl_sync(0xffffffffu, id1, j - 32);
-      good = (good1 >> (j - 32)) & 1u;
+    if (j < 64) {  // warp-uniform
+      id = __shfl_sync(0xffffffffu, j < 32 ? id0 : id1, j & 31);
+      good = ((j < 32 ? good0 : good1) >> (j & 31)) & 1u;
     } else {
       id = ptrow[kWarps * j];
       good = id >= 0 && id < p.num_pages;
       bad_id |= !good;
     }
-    valid_bits = (valid_bits & ~(1u << sl)) | ((uint32_t)good << sl);
+    return id;
+  };
+  // stage page j into ring slot sl (= j % kStages)
+  auto issue = [&](int j, int sl) {
+    bool good;
+    const int id = page_id(j, good);
     if (good) {
       const uint8_t* src = pool_h + (uint64_t)(uint32_t)id * stride;
       uint8_t* dst = sbuf + sl * kBlockBytes + lane * 16;
@@ -633,6 +637,17 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
       if (NG == kGroups || lane < 16) cp_async16(dst + 1024, src + 1024);  // metadata: 128 NG bytes
     }
   };
+  // pages j in [jlo, jhi) lie wholly inside [lo, hi) (page j starts at position
+  // base + 128 j; only a split's first and last pages can be cut by lo / hi) and
+  // every id is in the pool; pairs inside that range need no masking. With a bad
+  // id (or ids loaded on use) every pair takes the masking path.
+  // (rlo, rhi: the bounds relative to the warp's first page, kept in shared
+  // memory for the masking path so they hold no registers in the page loop)
+  __shared__ int2 wbounds[kWarps];
+  const int rlo = lo - (pbeg + warp) * kPage, rhi = hi - (pbeg + warp) * kPage;
+  const int jlo = bad_id || nmine > 64 ? nmine : (rlo <= 0 ? 0 : (rlo + kWarps * kPage - 1) / (kWarps * kPage));
+  const int jhi = min(nmine, rhi < kPage ? 0 : (rhi - kPage) / (kWarps * kPage) + 1);
+  if (lane == 0) wbounds[warp] = make_int2(rlo, rhi);
 
 #pragma unroll
   for (int s = 0; s < kStages; ++s) {
@@ -653,31 +668,33 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
 
   // Pages are consumed two at a time (one softmax update per pair), pair j in ring
   // slots SA, SA + 1 with SA = j % kStages; the loop below is unrolled over the two
-  // slot pairs so that every ring address and valid bit is a constant.
+  // slot pairs so that every ring address is a constant.
   static_assert(kStages == 4, "the page loop is unrolled over two slot pairs");
   auto consume_pair = [&](int j, auto sa_const) {
     constexpr int SA = decltype(sa_const)::value;
-    const bool two = j + 1 < nmine;
     // the copy groups of pages j and j + 1 (empty when a page does not exist) are
     // the oldest two of the kStages in flight
     cp_wait<kStages - 2>();
     __syncwarp();
     uint8_t* sbA = sbuf + SA * kBlockBytes;
     uint8_t* sbB = sbA + kBlockBytes;
-    const bool okA = (valid_bits >> SA) & 1u;
-    const bool okB = two && ((valid_bits >> (SA + 1)) & 1u);
-    const int posA = (pbeg + warp + kWarps * j) * kPage;
-    const int posB = posA + kWarps * kPage;
-    const bool full = okA && okB && posA >= lo && posA + kPage <= hi && posB >= lo && posB + kPage <= hi;
 
     float u[8];
     pair_scores<NG>(sbA, sbB, qs, zqb, lane, u);
-    if (!full) {
+    if (!(j >= jlo && j + 1 < jhi)) {
       // tokens outside [lo, hi), on a page with a bad id or on a missing second
       // page: scores -inf, and their value scales and zeros set to 0 in shared
       // memory (the bytes there may be stale), so the value product is the same
       // code for every pair
-      const uint32_t valid = page_token_bits(okA, posA, lo, hi) | (page_token_bits(okB, posB, lo, hi) << 16);
+      const bool two = j + 1 < nmine;
+      bool okA, okB;
+      page_id(j, okA);
+      if (two) page_id(j + 1, okB);
+      else okB = false;
+      const int posA = kWarps * kPage * j;   // relative to the warp's first page, like rlo / rhi
+      const int posB = posA + kWarps * kPage;
+      const int2 rb = wbounds[warp];
+      const uint32_t valid = page_token_bits(okA, posA, rb.x, rb.y) | (page_token_bits(okB, posB, rb.x, rb.y) << 16);
       const bool a0v = (valid >> gid) & 1u, a1v = (valid >> (gid + 8)) & 1u;
       const bool b0v = (valid >> (gid + 16)) & 1u, b1v = (valid >> (gid + 24)) & 1u;
       u[0] = a0v ? u[0] : -INFINITY;
@@ -724,17 +741,17 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     // every head sees the same tokens: the maximum stays -inf (warp-uniformly)
     // until a valid token has been seen, and pairs before that add nothing
     if (m0 != -INFINITY) {
-    const float nb0 = fmaf(-m0, us0, lg_ps), nb1 = fmaf(-m1, us1, lg_ps);
-    float pr[8];  // p * pscale, p <= 2^8
+      const float nb0 = fmaf(-m0, us0, lg_ps), nb1 = fmaf(-m1, us1, lg_ps);
+      float pr[8];  // p * pscale, p <= 2^8
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], (i & 1) ? us1 : us0, (i & 1) ? nb1 : nb0));
-    // token-major probabilities -> the (token, head) column operand of P.V
-    const uint32_t PA01 = transpose8x8(f2_to_h2_bits(pr[0], pr[1]));
-    const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
-    const uint32_t PB01 = transpose8x8(f2_to_h2_bits(pr[4], pr[5]));
-    const uint32_t PB23 = transpose8x8(f2_to_h2_bits(pr[6], pr[7]));
-    page_values<NG>(sbA, lane, PA01, PA23, acc, oz);
-    page_values<NG>(sbB, lane, PB01, PB23, acc, oz);
+      for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], (i & 1) ? us1 : us0, (i & 1) ? nb1 : nb0));
+      // token-major probabilities -> the (token, head) column operand of P.V
+      const uint32_t PA01 = transpose8x8(f2_to_h2_bits(pr[0], pr[1]));
+      const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
+      const uint32_t PB01 = transpose8x8(f2_to_h2_bits(pr[4], pr[5]));
+      const uint32_t PB23 = transpose8x8(f2_to_h2_bits(pr[6], pr[7]));
+      page_values<NG>(sbA, lane, PA01, PA23, acc, oz);
+      page_values<NG>(sbB, lane, PB01, PB23, acc, oz);
     }
     __syncwarp();
     if (j + kStages < nmine) issue(j + kStages, SA);

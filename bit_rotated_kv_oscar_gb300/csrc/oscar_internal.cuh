@@ -28,13 +28,17 @@ constexpr int kBlockBytes = OSCAR_PAGE_BLOCK_BYTES;   // block of the default gr
 // Page block of a group size with ng = 128 / group_size groups per token: codes
 // as for every group size, then the fp16 metadata (see include/oscar.h).
 __host__ __device__ constexpr int block_bytes(int ng) { return 1024 + 128 * ng; }
+// K scales: word gq of chunk t % 8 holds (scale of slot t % 8, scale of slot t % 8 + 8)
 __host__ __device__ constexpr int kscale_off(int ng, int t, int gq) {
-  return 1024 + 8 * ng * ((t & 7) >> 1) + 8 * gq + 4 * (t >> 3) + 2 * (t & 1);
+  return 1024 + 4 * ng * (t & 7) + 4 * gq + 2 * (t >> 3);
 }
 __host__ __device__ constexpr int kzero_off(int ng, int t, int gq) { return 1024 + 32 * ng + 2 * ng * t + 2 * gq; }
+// V scales of slots (2b, 2b + 1) and (2b + 8, 2b + 9) in the first two words of chunk
+// 4 gq + b, b = (t % 8) / 2; the zeros in the same order in the next two (vzero_off)
 __host__ __device__ constexpr int vscale_off(int ng, int t, int gq) {
-  return 1024 + 64 * ng + 16 * (4 * gq + ((t & 7) >> 1)) + 8 * (t >> 3) + 2 * (t & 1);
+  return 1024 + 64 * ng + 16 * (4 * gq + ((t & 7) >> 1)) + 4 * (t >> 3) + 2 * (t & 1);
 }
+__host__ __device__ constexpr int vzero_off(int ng, int t, int gq) { return vscale_off(ng, t, gq) + 8; }
 static_assert(block_bytes(kGroups) == kBlockBytes, "the default block size");
 static_assert(block_bytes(2) == OSCAR_PAGE_BLOCK_BYTES_FOR(64), "the group-64 block size");
 constexpr int kMaxGqa = 8;

@@ -200,9 +200,8 @@ __device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos,
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
       if (g < ng) {
-        uint8_t* m = blk + vscale_off(ng, t, g);
-        *reinterpret_cast<uint16_t*>(m) = (uint16_t)sz[g];
-        *reinterpret_cast<uint16_t*>(m + 4) = (uint16_t)(sz[g] >> 16);
+        *reinterpret_cast<uint16_t*>(blk + vscale_off(ng, t, g)) = (uint16_t)sz[g];
+        *reinterpret_cast<uint16_t*>(blk + vzero_off(ng, t, g)) = (uint16_t)(sz[g] >> 16);
       }
     }
   }

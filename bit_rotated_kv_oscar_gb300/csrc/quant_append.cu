@@ -284,9 +284,8 @@ oscar_quant_append_kernel(AppendParams p) {
                 *reinterpret_cast<__half*>(blk + kscale_off(ng, t, gq)) = meta[0][gq][0];
                 *reinterpret_cast<__half*>(blk + kzero_off(ng, t, gq)) = meta[0][gq][1];
               } else {
-                uint8_t* m = blk + vscale_off(ng, t, gq);
-                *reinterpret_cast<__half*>(m) = meta[1][gq][0];
-                *reinterpret_cast<__half*>(m + 4) = meta[1][gq][1];
+                *reinterpret_cast<__half*>(blk + vscale_off(ng, t, gq)) = meta[1][gq][0];
+                *reinterpret_cast<__half*>(blk + vzero_off(ng, t, gq)) = meta[1][gq][1];
               }
             }
           }

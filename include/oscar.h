@@ -53,11 +53,11 @@
  *       i = c/16, r = c%16, x = r/8, a = r%8, tt = t/8, b = (t%8)/2, hi = t%2;
  *       word at byte 512 + 16*(4a+b) + 4*(2*tt+x), bit 16*hi+2*i.
  *     fp16 scale and zero of group gq (channels group_size*gq ..) of slot t,
- *       with b = (t%8)/2, pair = t/8, half = t%2 (bytes [1024, BB)):
- *       K scale at byte 1024 + 8*NG*b + 8*gq + 4*pair + 2*half;
+ *       with a = t%8, b = (t%8)/2, pair = t/8, half = t%2 (bytes [1024, BB)):
+ *       K scale at byte 1024 + 4*NG*a + 4*gq + 2*pair;
  *       K zero  at byte 1024 + 32*NG + 2*NG*t + 2*gq;
- *       V scale at byte 1024 + 64*NG + 16*(4*gq + b) + 4*(2*pair) + 2*half,
- *       V zero 4 bytes later.
+ *       V scale at byte 1024 + 64*NG + 16*(4*gq + b) + 4*pair + 2*half,
+ *       V zero 8 bytes later.
  *   Slots of positions outside [sink, int2_end) are never read.
  *
  *   Window: bf16 [max_batch][num_kv_heads][2 (K, V)][sink + recent][128],

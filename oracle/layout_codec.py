@@ -19,10 +19,10 @@ every 32-bit word is little-endian.
       byte = 512 + 16 * (4a + b) + 4 * (2 tt + x) + (16 hi + 2 i) // 8
   bit inside that byte = (16 hi + 2 i) % 8
   metadata, bytes [1024, 1024 + 128 NG) with NG = 128 / group groups per token,
-      one fp16 each; b = (t % 8) // 2, pair = t // 8, half = t % 2, group gq:
-      K scale: 1024 + 8 NG b + 8 gq + 4 pair + 2 half
+      one fp16 each; a = t % 8, b = (t % 8) // 2, pair = t // 8, half = t % 2, group gq:
+      K scale: 1024 + 4 NG a + 4 gq + 2 pair
       K zero:  1024 + 32 NG + 2 NG t + 2 gq
-      V scale: 1024 + 64 NG + 16 (4 gq + b) + 4 (2 pair) + 2 half;  V zero: 4 bytes after it
+      V scale: 1024 + 64 NG + 16 (4 gq + b) + 4 pair + 2 half;  V zero: 8 bytes after it
 """
 
 from __future__ import annotations
@@ -66,12 +66,12 @@ def meta_location(kind: int, t: int, gq: int, field: int, group: int = GROUP) ->
     """Byte offset of the fp16 scale (field 0) or zero (field 1) of group gq,
     token slot t, kind 0 = K / 1 = V."""
     ng = HEAD_DIM // group
-    b, pair, half = (t % 8) // 2, t // 8, t % 2
+    a, b, pair, half = t % 8, (t % 8) // 2, t // 8, t % 2
     if kind == 0 and field == 0:
-        return 1024 + 8 * ng * b + 8 * gq + 4 * pair + 2 * half
+        return 1024 + 4 * ng * a + 4 * gq + 2 * pair
     if kind == 0:
         return 1024 + 32 * ng + 2 * ng * t + 2 * gq
-    return 1024 + 64 * ng + 16 * (4 * gq + b) + 4 * (2 * pair + field) + 2 * half
+    return 1024 + 64 * ng + 16 * (4 * gq + b) + 8 * field + 4 * pair + 2 * half
 
 
 def _tables(group: int = GROUP):
