@@ -113,6 +113,11 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem));
 }
+// the same with a shared-space address and a source size of 16 or 0 bytes (0:
+// nothing is read, the 16 bytes are zero-filled)
+__device__ __forceinline__ void cp_async16_s(uint32_t saddr, const void* gmem, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(gmem), "r"(src_bytes));
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
@@ -536,13 +541,18 @@ __device__ __forceinline__ void zero_masked_value_meta(uint8_t* sbA, uint8_t* sb
 // bit r: request r0 + r is consistent (else its partial is left empty). The
 // result goes to partial slot `slot` of every request. PACK: nreq may exceed 1
 // (otherwise both columns of a lane belong to request r0 and share its scale).
-template <int NG, bool PACK>
+// FEW: every warp of the CTA streams at most 64 pages (splits of up to 512
+// pages, the automatic split sizes), so all of a warp's page ids fit two
+// registers per lane.
+template <int NG, bool PACK, bool FEW>
 __device__ void int2_attention(const DecodeParams& p, int h, int split, int nsplits, int r0, int nreq,
-                               uint32_t okmask, int lo, int hi, int slot, uint8_t* smem) {
+                               uint32_t okmask, int lo, int hi, int slot, uint8_t* smem, uint4* qs,
+                               int2* wbounds) {
+  // qs [8 x 32]: q~ fragments of the packed requests, shared by all warps;
+  // wbounds [kWarps]: each warp's [lo, hi) relative to its first page
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int g = p.gqa;
-  __shared__ uint4 qs[8 * 32];  // q~ fragments of the packed requests, shared by all warps
 
   int npages = 0, first = 0;
   if (okmask != 0u && hi > lo) {
@@ -552,7 +562,12 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   const int chunk = (npages + nsplits - 1) / nsplits;
   const int pbeg = first + split * chunk;
   const int pend = min(pbeg + chunk, first + npages);
+  // Warp w takes pages pbeg + w + 8 j, nmine of them. Every warp runs the same
+  // npw iterations (the CTA's count) so that the page loop's control flow is
+  // the same in all warps; a warp's steps past its own pages read nothing and
+  // are masked like tokens outside [lo, hi).
   const int nmine = pend - pbeg - warp > 0 ? (pend - pbeg - warp + kWarps - 1) / kWarps : 0;
+  const int npw = pend > pbeg ? (pend - pbeg + kWarps - 1) / kWarps : 0;
 
   // query operand fragments (see oscar_rotate_q_kernel): column n = gid of lane
   // (gid, tig) takes the fragment of head gid % g of request r0 + gid / g
@@ -602,59 +617,61 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   constexpr int kBB = block_bytes(NG);
   const uint8_t* pool_h = p.pool + (size_t)h * kBB + lane * 16;
   const size_t page_stride = (size_t)p.num_kv_heads * kBB;
-  // page ids of this warp's first 64 pages, two per lane, loaded once together with
-  // their validity (a ballot); pages beyond that, possible only with more than 512
-  // pages per split, load on use. A page whose id is outside the pool is not
-  // copied, is masked out of the attention and reported after the loop.
-  const int id0 = lane < nmine ? ptrow[kWarps * lane] : 0;
-  const int id1 = lane + 32 < nmine ? ptrow[kWarps * (lane + 32)] : 0;
-  const uint32_t good0 = __ballot_sync(0xffffffffu, id0 >= 0 && id0 < p.num_pages);
-  const uint32_t good1 = __ballot_sync(0xffffffffu, id1 >= 0 && id1 < p.num_pages);
-  bool bad_id = good0 != 0xffffffffu || good1 != 0xffffffffu;
+  // Page ids, two per lane for the first 64 pages of the warp (FEW: all of them),
+  // -1 for a page the warp does not have; an id outside the pool is reported
+  // after the loop and treated like a missing page: nothing is read (its ring
+  // slot is zero-filled) and its tokens are masked.
   const uint32_t stride = (uint32_t)page_stride;   // heads x 1536 bytes, far below 2^32
-  // id of page j of this warp and whether it lies in the pool
-  auto page_id = [&](int j, bool& good) {
-    int id;
-    if (j < 64) {  // warp-uniform
-      id = __shfl_sync(0xffffffffu, j < 32 ? id0 : id1, j & 31);
-      good = ((j < 32 ? good0 : good1) >> (j & 31)) & 1u;
-    } else {
+  bool bad = false;
+  auto load_id = [&](int j) {
+    int id = -1;
+    if (j < nmine) {
       id = ptrow[kWarps * j];
-      good = id >= 0 && id < p.num_pages;
-      bad_id |= !good;
+      if (id < 0 || id >= p.num_pages) {
+        bad = true;
+        id = -1;
+      }
     }
     return id;
   };
-  // stage page j into ring slot sl (= j % kStages)
-  auto issue = [&](int j, int sl) {
-    bool good;
-    const int id = page_id(j, good);
-    if (good) {
-      const uint8_t* src = pool_h + (uint64_t)(uint32_t)id * stride;
-      uint8_t* dst = sbuf + sl * kBlockBytes + lane * 16;
-      cp_async16(dst, src);
-      cp_async16(dst + 512, src + 512);
-      if (NG == kGroups || lane < 16) cp_async16(dst + 1024, src + 1024);  // metadata: 128 NG bytes
-    }
+  const int id0 = load_id(lane);
+  const int id1 = load_id(lane + 32);
+  // id of page j of the warp, -1 when it has none (or its id is outside the pool)
+  auto page_id = [&](int j) {
+    if (FEW || j < 64) return __shfl_sync(0xffffffffu, j < 32 ? id0 : id1, j & 31);
+    return load_id(j);
   };
-  // pages j in [jlo, jhi) lie wholly inside [lo, hi) (page j starts at position
-  // base + 128 j; only a split's first and last pages can be cut by lo / hi) and
-  // every id is in the pool; pairs inside that range need no masking. With a bad
-  // id (or ids loaded on use) every pair takes the masking path.
-  // (rlo, rhi: the bounds relative to the warp's first page, kept in shared
-  // memory for the masking path so they hold no registers in the page loop)
-  __shared__ int2 wbounds[kWarps];
-  const int rlo = lo - (pbeg + warp) * kPage, rhi = hi - (pbeg + warp) * kPage;
-  const int jlo = bad_id || nmine > 64 ? nmine : (rlo <= 0 ? 0 : (rlo + kWarps * kPage - 1) / (kWarps * kPage));
-  const int jhi = min(nmine, rhi < kPage ? 0 : (rhi - kPage) / (kWarps * kPage) + 1);
-  if (lane == 0) wbounds[warp] = make_int2(rlo, rhi);
+  // stage page j into ring slot sl (= j % kStages)
+  const uint32_t sring = (uint32_t)__cvta_generic_to_shared(sbuf) + lane * 16;
+  auto issue = [&](int j, int sl) {
+    const int id = page_id(j);
+    const uint32_t nb = id >= 0 ? 16u : 0u;
+    const uint8_t* src = pool_h + (uint64_t)(uint32_t)max(id, 0) * stride;
+    const uint32_t dst = sring + sl * kBlockBytes;
+    cp_async16_s(dst, src, nb);
+    cp_async16_s(dst + 512, src + 512, nb);
+    if (NG == kGroups || lane < 16) cp_async16_s(dst + 1024, src + 1024, nb);  // metadata: 128 NG bytes
+  };
+  // pages j in [jlo, jhi) of the warp lie wholly inside [lo, hi) (page j starts
+  // at position base + 128 j; only a split's first and last pages can be cut by
+  // lo / hi) and every id is in the pool: pairs inside that range need no
+  // masking. The bounds relative to the warp's first page live in shared memory
+  // for the masking path, so that they hold no registers in the page loop.
+  bool bad_id = __any_sync(0xffffffffu, bad);
+  int jlo, jhi;
+  {
+    const int rlo = lo - (pbeg + warp) * kPage, rhi = hi - (pbeg + warp) * kPage;
+    jlo = bad_id || (!FEW && nmine > 64) ? npw : (rlo <= 0 ? 0 : (rlo + kWarps * kPage - 1) / (kWarps * kPage));
+    jhi = min(nmine, rhi < kPage ? 0 : (rhi - kPage) / (kWarps * kPage) + 1);
+    if (lane == 0) wbounds[warp] = make_int2(rlo, rhi);
+  }
 
 #pragma unroll
   for (int s = 0; s < kStages; ++s) {
-    if (s < nmine) issue(s, s);
+    if (s < npw) issue(s, s);
     cp_commit();
   }
-  __syncthreads();  // q~ fragments visible to every warp
+  __syncthreads();  // q~ fragments and the bounds visible to every warp
 
   // running (lazy) max in score units u (log2 units = u * uscale), running sum and
   // accumulators in units of pscale
@@ -682,15 +699,11 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     float u[8];
     pair_scores<NG>(sbA, sbB, qs, zqb, lane, u);
     if (!(j >= jlo && j + 1 < jhi)) {
-      // tokens outside [lo, hi), on a page with a bad id or on a missing second
-      // page: scores -inf, and their value scales and zeros set to 0 in shared
-      // memory (the bytes there may be stale), so the value product is the same
-      // code for every pair
-      const bool two = j + 1 < nmine;
-      bool okA, okB;
-      page_id(j, okA);
-      if (two) page_id(j + 1, okB);
-      else okB = false;
+      // tokens outside [lo, hi), on a page the warp does not have or whose id is
+      // outside the pool: scores -inf, and their value scales and zeros set to 0
+      // in shared memory, so the value product is the same code for every pair
+      const bool okA = page_id(j) >= 0;
+      const bool okB = page_id(j + 1) >= 0;
       const int posA = kWarps * kPage * j;   // relative to the warp's first page, like rlo / rhi
       const int posB = posA + kWarps * kPage;
       const int2 rb = wbounds[warp];
@@ -738,30 +751,30 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
       oz[2] *= a0;
       oz[3] *= a1;
     }
-    // every head sees the same tokens: the maximum stays -inf (warp-uniformly)
-    // until a valid token has been seen, and pairs before that add nothing
-    if (m0 != -INFINITY) {
-      const float nb0 = fmaf(-m0, us0, lg_ps), nb1 = fmaf(-m1, us1, lg_ps);
-      float pr[8];  // p * pscale, p <= 2^8
+    // every head sees the same tokens: the maximum stays -inf until a valid
+    // token has been seen, and the probabilities of such pairs are 0 (the
+    // offset is 0 then, so that -inf scores give 2^-inf = 0)
+    const float nb0 = m0 == -INFINITY ? 0.f : fmaf(-m0, us0, lg_ps);
+    const float nb1 = m1 == -INFINITY ? 0.f : fmaf(-m1, us1, lg_ps);
+    float pr[8];  // p * pscale, p <= 2^8
 #pragma unroll
-      for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], (i & 1) ? us1 : us0, (i & 1) ? nb1 : nb0));
-      // token-major probabilities -> the (token, head) column operand of P.V
-      const uint32_t PA01 = transpose8x8(f2_to_h2_bits(pr[0], pr[1]));
-      const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
-      const uint32_t PB01 = transpose8x8(f2_to_h2_bits(pr[4], pr[5]));
-      const uint32_t PB23 = transpose8x8(f2_to_h2_bits(pr[6], pr[7]));
-      page_values<NG>(sbA, lane, PA01, PA23, acc, oz);
-      page_values<NG>(sbB, lane, PB01, PB23, acc, oz);
-    }
+    for (int i = 0; i < 8; ++i) pr[i] = ex2(fmaf(u[i], (i & 1) ? us1 : us0, (i & 1) ? nb1 : nb0));
+    // token-major probabilities -> the (token, head) column operand of P.V
+    const uint32_t PA01 = transpose8x8(f2_to_h2_bits(pr[0], pr[1]));
+    const uint32_t PA23 = transpose8x8(f2_to_h2_bits(pr[2], pr[3]));
+    const uint32_t PB01 = transpose8x8(f2_to_h2_bits(pr[4], pr[5]));
+    const uint32_t PB23 = transpose8x8(f2_to_h2_bits(pr[6], pr[7]));
+    page_values<NG>(sbA, lane, PA01, PA23, acc, oz);
+    page_values<NG>(sbB, lane, PB01, PB23, acc, oz);
     __syncwarp();
-    if (j + kStages < nmine) issue(j + kStages, SA);
+    if (j + kStages < npw) issue(j + kStages, SA);
     cp_commit();
-    if (j + 1 + kStages < nmine) issue(j + 1 + kStages, SA + 1);
+    if (j + 1 + kStages < npw) issue(j + 1 + kStages, SA + 1);
     cp_commit();
   };
-  for (int j = 0; j < nmine; j += 4) {
+  for (int j = 0; j < npw; j += 4) {
     consume_pair(j, std::integral_constant<int, 0>{});
-    if (j + 2 < nmine) consume_pair(j + 2, std::integral_constant<int, 2>{});
+    if (j + 2 < npw) consume_pair(j + 2, std::integral_constant<int, 2>{});
   }
   cp_wait<0>();
   if (__any_sync(0xffffffffu, bad_id) && lane == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
@@ -821,9 +834,20 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   }
 }
 
+// whether every warp of a CTA over INT2 positions [lo, hi) split `nsplits` ways
+// streams at most 64 pages (the split arithmetic of int2_attention)
+__device__ __forceinline__ bool few_pages(int lo, int hi, int nsplits) {
+  if (hi <= lo) return true;
+  const int npages = (hi - 1) / kPage - lo / kPage + 1;
+  const int chunk = (npages + nsplits - 1) / nsplits;
+  return chunk <= 64 * kWarps;
+}
+
 template <int NG>
 __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint4 qs[8 * 32];
+  __shared__ int2 wb[kWarps];
   const int x = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
   // R_V^T[h] (constant) into the level-2 cache for the merge, whose CTAs only
   // become resident as these retire: one bulk prefetch per KV head
@@ -849,14 +873,21 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
       okmask |= (uint32_t)ok << r;
     }
     if (okmask != (1u << nreq) - 1u && threadIdx.x == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_STATE);
-    int2_attention<NG, true>(p, h, x - p.win_slots, p.prefix_splits, r0, nreq, okmask, S, P, x, smem);
+    if (few_pages(S, P, p.prefix_splits))
+      int2_attention<NG, true, true>(p, h, x - p.win_slots, p.prefix_splits, r0, nreq, okmask, S, P, x, smem, qs, wb);
+    else
+      int2_attention<NG, true, false>(p, h, x - p.win_slots, p.prefix_splits, r0, nreq, okmask, S, P, x, smem, qs, wb);
   } else {
     // the request's own INT2 positions after the shared prefix
     const oscar_seq_state st = p.state[z];
     const bool ok = state_ok(st, S, W, p.max_batch);
     const int lo = max(S, P), hi = min(st.int2_end, st.seq_len);
-    int2_attention<NG, false>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo, hi, x,
-                              smem);
+    if (few_pages(lo, hi, p.splits))
+      int2_attention<NG, false, true>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo,
+                                      hi, x, smem, qs, wb);
+    else
+      int2_attention<NG, false, false>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo,
+                                       hi, x, smem, qs, wb);
   }
 }
 
