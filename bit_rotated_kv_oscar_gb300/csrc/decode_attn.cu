@@ -10,7 +10,7 @@
 // Three launches on one stream:
 //   1. oscar_rotate_q_kernel   q~ = q R_K * scale * log2(e) per (request, KV head),
 //      written as ready-to-use tensor-core operand fragments (fp16 hi + lo).
-//   2. oscar_decode_kernel<NG> grid (window chunks + prefix splits + splits, Hkv,
+//   2. oscar_decode_kernel<NG, FEW> grid (window chunks + prefix splits + splits, Hkv,
 //      B), NG = 128 / group size: the first CTAs attend over the BF16 sink +
 //      recent ring in the raw basis (64 or 160 tokens each, per call); the
 //      others stream a slice of the INT2 pages, computing scores and the P.V
@@ -641,10 +641,11 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     if (FEW || j < 64) return __shfl_sync(0xffffffffu, j < 32 ? id0 : id1, j & 31);
     return load_id(j);
   };
-  // stage page j into ring slot sl (= j % kStages)
+  // stage page j into ring slot sl (= j % kStages); nothing is read when `want`
+  // is false (the slot is zero-filled)
   const uint32_t sring = (uint32_t)__cvta_generic_to_shared(sbuf) + lane * 16;
-  auto issue = [&](int j, int sl) {
-    const int id = page_id(j);
+  auto issue = [&](int j, int sl, bool want) {
+    const int id = want ? page_id(j) : -1;
     const uint32_t nb = id >= 0 ? 16u : 0u;
     const uint8_t* src = pool_h + (uint64_t)(uint32_t)max(id, 0) * stride;
     const uint32_t dst = sring + sl * kBlockBytes;
@@ -668,7 +669,7 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
 
 #pragma unroll
   for (int s = 0; s < kStages; ++s) {
-    if (s < npw) issue(s, s);
+    issue(s, s, s < npw);
     cp_commit();
   }
   __syncthreads();  // q~ fragments and the bounds visible to every warp
@@ -687,18 +688,22 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   // slots SA, SA + 1 with SA = j % kStages; the loop below is unrolled over the two
   // slot pairs so that every ring address is a constant.
   static_assert(kStages == 4, "the page loop is unrolled over two slot pairs");
-  auto consume_pair = [&](int j, auto sa_const) {
-    constexpr int SA = decltype(sa_const)::value;
+  // MASKED: the pair may hold tokens outside [lo, hi) or pages the warp does
+  // not have; pairs wholly inside are consumed by the same code without masking
+  auto consume_pair = [&](int j, auto masked_const) {
+    constexpr bool MASKED = decltype(masked_const)::value;
+    // ring slots j % kStages and the next (j is even)
+    const int sa = j & (kStages - 1);
     // the copy groups of pages j and j + 1 (empty when a page does not exist) are
     // the oldest two of the kStages in flight
     cp_wait<kStages - 2>();
     __syncwarp();
-    uint8_t* sbA = sbuf + SA * kBlockBytes;
+    uint8_t* sbA = sbuf + sa * kBlockBytes;
     uint8_t* sbB = sbA + kBlockBytes;
 
     float u[8];
     pair_scores<NG>(sbA, sbB, qs, zqb, lane, u);
-    if (!(j >= jlo && j + 1 < jhi)) {
+    if (MASKED) {
       // tokens outside [lo, hi), on a page the warp does not have or whose id is
       // outside the pool: scores -inf, and their value scales and zeros set to 0
       // in shared memory, so the value product is the same code for every pair
@@ -767,15 +772,20 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     page_values<NG>(sbA, lane, PA01, PA23, acc, oz);
     page_values<NG>(sbB, lane, PB01, PB23, acc, oz);
     __syncwarp();
-    if (j + kStages < npw) issue(j + kStages, SA);
+    // the pages kStages further on replace these two in the ring (copies past the
+    // warp's last step read nothing)
+    issue(j + kStages, sa, j + kStages < npw);
     cp_commit();
-    if (j + 1 + kStages < npw) issue(j + 1 + kStages, SA + 1);
+    issue(j + 1 + kStages, sa + 1, j + 1 + kStages < npw);
     cp_commit();
   };
-  for (int j = 0; j < npw; j += 4) {
-    consume_pair(j, std::integral_constant<int, 0>{});
-    if (j + 2 < npw) consume_pair(j + 2, std::integral_constant<int, 2>{});
-  }
+  // pairs j, j + 1 (j even) with j >= jlo and j + 1 < jhi need no masking: a
+  // masked head (the split's first page may start before lo), the unmasked
+  // middle, a masked tail
+  int j = 0;
+  for (; j < npw && j < jlo; j += 2) consume_pair(j, std::true_type{});
+  for (; j + 1 < jhi; j += 2) consume_pair(j, std::false_type{});
+  for (; j < npw; j += 2) consume_pair(j, std::true_type{});
   cp_wait<0>();
   if (__any_sync(0xffffffffu, bad_id) && lane == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
 
@@ -834,16 +844,11 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   }
 }
 
-// whether every warp of a CTA over INT2 positions [lo, hi) split `nsplits` ways
-// streams at most 64 pages (the split arithmetic of int2_attention)
-__device__ __forceinline__ bool few_pages(int lo, int hi, int nsplits) {
-  if (hi <= lo) return true;
-  const int npages = (hi - 1) / kPage - lo / kPage + 1;
-  const int chunk = (npages + nsplits - 1) / nsplits;
-  return chunk <= 64 * kWarps;
-}
-
-template <int NG>
+// FEW: no split holds more than 64 pages per warp (kFewPages per CTA), so the
+// INT2 CTAs keep all their page ids in registers; the host picks the instance
+// from the page-table width and the split counts (few_pages_call)
+constexpr int kFewPages = 64 * kWarps;
+template <int NG, bool FEW>
 __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint4 qs[8 * 32];
@@ -873,21 +878,14 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
       okmask |= (uint32_t)ok << r;
     }
     if (okmask != (1u << nreq) - 1u && threadIdx.x == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_STATE);
-    if (few_pages(S, P, p.prefix_splits))
-      int2_attention<NG, true, true>(p, h, x - p.win_slots, p.prefix_splits, r0, nreq, okmask, S, P, x, smem, qs, wb);
-    else
-      int2_attention<NG, true, false>(p, h, x - p.win_slots, p.prefix_splits, r0, nreq, okmask, S, P, x, smem, qs, wb);
+    int2_attention<NG, true, FEW>(p, h, x - p.win_slots, p.prefix_splits, r0, nreq, okmask, S, P, x, smem, qs, wb);
   } else {
     // the request's own INT2 positions after the shared prefix
     const oscar_seq_state st = p.state[z];
     const bool ok = state_ok(st, S, W, p.max_batch);
     const int lo = max(S, P), hi = min(st.int2_end, st.seq_len);
-    if (few_pages(lo, hi, p.splits))
-      int2_attention<NG, false, true>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo,
-                                      hi, x, smem, qs, wb);
-    else
-      int2_attention<NG, false, false>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo,
-                                       hi, x, smem, qs, wb);
+    int2_attention<NG, false, FEW>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo, hi,
+                                   x, smem, qs, wb);
   }
 }
 
@@ -1039,9 +1037,13 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
   const int smem = decode_smem_bytes();
   cudaError_t ea = once_for_current_device(attrs, [&] {
     cudaError_t e =
-        cudaFuncSetAttribute(oscar_decode_kernel<kGroups>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(oscar_decode_kernel<kGroups, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(oscar_decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      e = cudaFuncSetAttribute(oscar_decode_kernel<kGroups, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(oscar_decode_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(oscar_decode_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(oscar_rotate_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmem);
     if (e == cudaSuccess)
@@ -1051,11 +1053,17 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
   if (ea != cudaSuccess) return ea;
   if (p.win_slots + p.prefix_splits + p.splits > kMaxSlots) return cudaErrorInvalidValue;
   if (p.win_chunk < 1 || p.win_chunk > kWinChunk) return cudaErrorInvalidValue;
+  // every split of the call streams at most kFewPages pages: a request's INT2
+  // pages fit its page-table row, the shared prefix its own page count
+  const int64_t prefix_pages = (int64_t)(p.prefix_tokens + kPage - 1) / kPage;
+  const bool few = (p.pt_stride + p.splits - 1) / p.splits <= kFewPages &&
+                   (p.prefix_splits == 0 || (prefix_pages + p.prefix_splits - 1) / p.prefix_splits <= kFewPages);
   cudaError_t e = launch_pdl(oscar_rotate_q_kernel, dim3(p.num_kv_heads, batch), dim3(kRotThreads), kRotSmem,
                              s, p);
   if (e == cudaSuccess && ev_before) e = cudaEventRecord(ev_before, s);
   if (e == cudaSuccess)
-    e = launch_pdl(p.ngroups == kGroups ? oscar_decode_kernel<kGroups> : oscar_decode_kernel<2>,
+    e = launch_pdl(p.ngroups == kGroups ? (few ? oscar_decode_kernel<kGroups, true> : oscar_decode_kernel<kGroups, false>)
+                                        : (few ? oscar_decode_kernel<2, true> : oscar_decode_kernel<2, false>),
                    dim3(p.win_slots + p.prefix_splits + p.splits, p.num_kv_heads, batch), dim3(kThreads),
                    smem, s, p);
   if (e == cudaSuccess && ev_after) e = cudaEventRecord(ev_after, s);

@@ -212,6 +212,17 @@ def test_split_counts(splits):
     check_decode(layer, 1)
 
 
+@pytest.mark.parametrize("splits", [1, 2])
+def test_long_splits(splits):
+    # 12000 tokens in one split of 750 pages (more than 64 per warp: the kernel
+    # instance for long splits, page ids past the first 64 loaded on use) and in
+    # two splits of 375 pages
+    layer = Layer(32, 8, 4, 128, 1, 12000, seed=23, num_splits=splits)
+    k, v = layer.draw(12000)
+    layer.append(0, k, v)
+    check_decode(layer, 1)
+
+
 def test_fold_rv_keeps_values_rotated():
     layer = Layer(8, 2, 4, 64, 1, 1000, seed=31, fold_rv=1)
     k, v = layer.draw(1000)
