@@ -559,7 +559,9 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     first = lo / kPage;
     npages = (hi - 1) / kPage - first + 1;
   }
-  const int chunk = (npages + nsplits - 1) / nsplits;
+  // split size rounded up to whole page pairs of every warp, so that all warps of
+  // a split but the last one stream the same even number of pages
+  const int chunk = ((npages + nsplits - 1) / nsplits + 2 * kWarps - 1) / (2 * kWarps) * (2 * kWarps);
   const int pbeg = first + split * chunk;
   const int pend = min(pbeg + chunk, first + npages);
   // Warp w takes pages pbeg + w + 8 j, nmine of them. Every warp runs the same
@@ -644,11 +646,11 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   // stage page j into ring slot sl (= j % kStages); nothing is read when `want`
   // is false (the slot is zero-filled)
   const uint32_t sring = (uint32_t)__cvta_generic_to_shared(sbuf) + lane * 16;
-  auto issue = [&](int j, int sl, bool want) {
+  auto issue = [&](int j, uint32_t slot_off, bool want) {
     const int id = want ? page_id(j) : -1;
     const uint32_t nb = id >= 0 ? 16u : 0u;
     const uint8_t* src = pool_h + (uint64_t)(uint32_t)max(id, 0) * stride;
-    const uint32_t dst = sring + sl * kBlockBytes;
+    const uint32_t dst = sring + slot_off;
     cp_async16_s(dst, src, nb);
     cp_async16_s(dst + 512, src + 512, nb);
     if (NG == kGroups || lane < 16) cp_async16_s(dst + 1024, src + 1024, nb);  // metadata: 128 NG bytes
@@ -669,7 +671,7 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
 
 #pragma unroll
   for (int s = 0; s < kStages; ++s) {
-    issue(s, s, s < npw);
+    issue(s, s * kBlockBytes, s < npw);
     cp_commit();
   }
   __syncthreads();  // q~ fragments and the bounds visible to every warp
@@ -692,13 +694,13 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   // not have; pairs wholly inside are consumed by the same code without masking
   auto consume_pair = [&](int j, auto masked_const) {
     constexpr bool MASKED = decltype(masked_const)::value;
-    // ring slots j % kStages and the next (j is even)
-    const int sa = j & (kStages - 1);
+    // ring slots j % kStages and the next (j is even): byte offset soff
+    const uint32_t soff = (j & 2) ? 2 * kBlockBytes : 0;
     // the copy groups of pages j and j + 1 (empty when a page does not exist) are
     // the oldest two of the kStages in flight
     cp_wait<kStages - 2>();
     __syncwarp();
-    uint8_t* sbA = sbuf + sa * kBlockBytes;
+    uint8_t* sbA = sbuf + soff;
     uint8_t* sbB = sbA + kBlockBytes;
 
     float u[8];
@@ -774,9 +776,9 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     __syncwarp();
     // the pages kStages further on replace these two in the ring (copies past the
     // warp's last step read nothing)
-    issue(j + kStages, sa, j + kStages < npw);
+    issue(j + kStages, soff, j + kStages < npw);
     cp_commit();
-    issue(j + 1 + kStages, sa + 1, j + 1 + kStages < npw);
+    issue(j + 1 + kStages, soff + kBlockBytes, j + 1 + kStages < npw);
     cp_commit();
   };
   // pairs j, j + 1 (j even) with j >= jlo and j + 1 < jhi need no masking: a
