@@ -41,6 +41,22 @@ __device__ __forceinline__ uint8_t* block_of(const AppendParams& p, int32_t id, 
 }
 
 constexpr int kMaxTokensPerCta = 16;
+
+// whether a tail_only CTA with virtual tokens [j0, j1) quantises anything: a
+// ring token at position q >= E2 evicts the entry at q - W ((q - L) / W + 1),
+// which goes to INT2 when it lies in [max(E, S), E2) (the token loop's rule)
+__device__ __forceinline__ bool any_quantised(const AppendParams& p, int j0, int j1, int L, int E, int64_t E2) {
+  const int S = p.sink, W = p.recent;
+  for (int jv = j0; jv < j1; ++jv) {
+    const int j = jv < S ? jv : p.n_new - W + (jv - S);
+    const int64_t q = (int64_t)L + j;
+    if (q >= E2) {
+      const int64_t pe = q - (int64_t)W * ((q - L) / W + 1);
+      if (pe >= E && pe < E2 && pe >= S) return true;
+    }
+  }
+  return false;
+}
 constexpr int kAppendSmem = 2 * kHeadDim * kHeadDim * 4;  // R_K[h] and R_V[h]
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -68,8 +84,11 @@ oscar_quant_append_kernel(AppendParams p) {
 
   // copies of 16 bytes need 16-byte aligned inputs (otherwise read in place)
   const bool staged = j0 < j1 && ((reinterpret_cast<uintptr_t>(p.k) | reinterpret_cast<uintptr_t>(p.v)) & 15) == 0;
-  // the rotations are constant: stage them before waiting for earlier kernels
-  {
+  // the rotations are constant: stage them before waiting for earlier kernels.
+  // A launch for the sink / ring tokens of a long append (tail_only) quantises
+  // only ring entries that the new tokens evict, usually none: it stages them
+  // after reading the state, and only when it needs them.
+  auto stage_rotations = [&]() {
     const float* rk = p.R_K + (size_t)h * kHeadDim * kHeadDim;
     const float* rv = p.R_V + (size_t)h * kHeadDim * kHeadDim;
     constexpr int n4 = kHeadDim * kHeadDim / 4;
@@ -77,6 +96,9 @@ oscar_quant_append_kernel(AppendParams p) {
       cp_async16(Rs + 4 * i, rk + 4 * i);
       if (!p.fold_rv) cp_async16(Rs + kHeadDim * kHeadDim + 4 * i, rv + 4 * i);
     }
+  };
+  {
+    if (!p.tail_only) stage_rotations();
     // the CTA's first new token: the caller's input, which no kernel of this
     // library writes, so it is read before waiting for earlier kernels
     if (staged && tid < 2 * (kHeadDim / 8)) {
@@ -134,9 +156,39 @@ oscar_quant_append_kernel(AppendParams p) {
     const size_t wrow = (size_t)st.window_row;
     __nv_bfloat16* win_k = p.window + ((wrow * Hkv + h) * 2 + 0) * slots * kHeadDim;
     __nv_bfloat16* win_v = p.window + ((wrow * Hkv + h) * 2 + 1) * slots * kHeadDim;
+    if (p.tail_only) {
+      // the ring entries this CTA's ring tokens evict that go to INT2 (see the
+      // token loop below); stage the rotations if there are any
+      const bool need = any_quantised(p, j0, j1, L, E, E2);
+      if (need) {
+        stage_rotations();
+        asm volatile("cp.async.commit_group;\n" ::);
+        asm volatile("cp.async.wait_group 0;\n" ::);
+        __syncthreads();
+      }
+    }
+    // Without entries to quantise the sink and ring tokens are plain copies:
+    // all of the CTA's tokens at once, 16 bytes per thread (a long append's
+    // inputs are 16-byte aligned), instead of one token after another.
+    const bool copies_only = p.tail_only && !any_quantised(p, j0, j1, L, E, E2);
+    if (copies_only) {
+      for (int idx = tid; idx < (j1 - j0) * 32; idx += kThreads) {
+        const int jv = j0 + (idx >> 5), kind = (idx >> 4) & 1, ch = idx & 15;
+        const int j = jv < S ? jv : p.n_new - W + (jv - S);
+        const int64_t q = (int64_t)L + j;
+        int64_t slot = -1;
+        if (q < S) slot = q;
+        else if (q >= E2) slot = S + q % W;
+        if (slot >= 0) {
+          const size_t in_off = (((size_t)b * p.n_new + j) * Hkv + h) * kHeadDim + 8 * ch;
+          const uint4 x = *reinterpret_cast<const uint4*>((kind ? p.v : p.k) + in_off);
+          *reinterpret_cast<uint4*>((kind ? win_v : win_k) + (size_t)slot * kHeadDim + 8 * ch) = x;
+        }
+      }
+    }
 
 
-    for (int jv = j0; jv < j1; ++jv) {
+    for (int jv = copies_only ? j1 : j0; jv < j1; ++jv) {
       const int j = !p.tail_only ? jv : (jv < S ? jv : p.n_new - W + (jv - S));
       const int64_t q = (int64_t)L + j;
       // with tail_only the tokens going straight to INT2 belong to the prefill kernel

@@ -1,7 +1,8 @@
 """Full-size parity: every workload at its own sizes, driven the way the
 benchmark drives it (16384-token population chunks, one 131072-token append,
 the full decode batch with the automatic split count), and checked on samples
-the oracle computes one by one:
+the oracle computes one by one (the 32k workload runs its 100 decode steps;
+the batch-28 workload populates three of its requests independently):
   * the codes, scales and zeros of sampled pages bit-exact against the oracle
     quantising the GPU's rotated values, and those rotated values within 1e-5
     of the float64 rotation;
@@ -143,8 +144,12 @@ def clone_request(layer, src, dst):
 # ---------------------------------------------------------------------------
 
 def test_fullsize_qwen3_8b_bs1_32k():
+    # the workload's 100 decode steps, each appending one token (which evicts the
+    # oldest recent token into INT2) before decoding; outputs of every KV head
+    # checked at steps 0, 50 and 99
     spec = WORKLOADS["qwen3_8b_bs1_32k"]
-    n, steps = spec.context, 3
+    n, steps = spec.context, spec.decode_steps
+    assert steps == 100
     layer = spec_layer(spec, 1, n + steps + 16)
     trace = layer.new_trace(n + steps)
     populate(layer, 0, n, 10_000, trace)
@@ -156,8 +161,13 @@ def test_fullsize_qwen3_8b_bs1_32k():
         layer.append(0, k.view(1, layer.hkv, D), v.view(1, layer.hkv, D), trace)
         q = draw_queries(layer.seed, 100 + step, 1, layer.hq, layer.hkv, D)
         o = decode_rows(layer, q, 0)
-        check_sampled_decode(layer, q, o, [(0, h) for h in range(layer.hkv)])
-    check_int2(layer, 0, trace, layer.e[0] - 16, layer.e[0])
+        assert np.isfinite(o).all(), step
+        if step in (0, 50, 99):
+            check_sampled_decode(layer, q, o, [(0, h) for h in range(layer.hkv)])
+    assert (layer.len[0], layer.e[0]) == (n + steps, n + steps - spec.recent)
+    # the tokens the steps evicted into INT2
+    check_int2(layer, 0, trace, n - spec.recent, layer.e[0])
+    check_window(layer, 0)
     assert layer.ctx.error_flags() == 0
 
 
@@ -185,26 +195,36 @@ def test_fullsize_qwen3_8b_bs16_ragged():
 
 
 # ---------------------------------------------------------------------------
-# Qwen3-32B layer, batch 28 x 100000 tokens (copies of one populated request)
+# Qwen3-32B layer, batch 28 x ~100000 tokens: three requests populated
+# independently (their own seeds and lengths), the others copies of request 0
 # ---------------------------------------------------------------------------
 
 def test_fullsize_qwen3_32b_bs28_100k():
     spec = WORKLOADS["qwen3_32b_bs28_100k"]
     n, B = spec.context, spec.batch
+    own = {0: n, 13: n - 37, 27: n - 1000}      # request -> its own length
     layer = spec_layer(spec, B, n + 16)
     trace = layer.new_trace(n)
     populate(layer, 0, n, 10_000, trace)
     rng = np.random.default_rng(3)
     check_sampled_int2(layer, 0, trace, rng)
     del trace
+    for b, length in own.items():
+        if b:
+            populate(layer, b, length, 30_000 + 100 * b)
     for b in range(1, B):
-        clone_request(layer, 0, b)
+        if b not in own:
+            clone_request(layer, 0, b)
     q = draw_queries(layer.seed, 3, B, layer.hq, layer.hkv, D)
     o = decode_rows(layer, q, 0)
     assert np.isfinite(o).all()
     heads = (0, 5)
+    for b in own:
+        caches = {h: oracle_head(layer, b, h) for h in heads}
+        check_sampled_decode(layer, q, o, [(b, h) for h in heads], caches=caches)
+    # a copied request reads the same cache as request 0 through other pages
     caches = {h: oracle_head(layer, 0, h) for h in heads}
-    check_sampled_decode(layer, q, o, [(b, h) for b in (0, 13, 27) for h in heads], caches=caches)
+    check_sampled_decode(layer, q, o, [(b, h) for b in (5, 20) for h in heads], caches=caches)
     assert layer.ctx.error_flags() == 0
 
 
