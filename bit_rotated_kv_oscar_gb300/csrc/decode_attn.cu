@@ -1024,6 +1024,107 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   }
 }
 
+// --------------------------------------------------------------------------
+// 3b. the same merge for calls with few (request, KV head) pairs: CTA z = 4 m + q
+//     of (request y, KV head x) produces output channels 32 q .. 32 q + 31 of
+//     query head m, from all of m's partial rows and the 32 columns of R_V^T it
+//     needs, so that 8 times more CTAs share the work and each un-rotates 32
+//     rows per thread instead of 64 (the merge of a small batch is a latency
+//     chain, not a bandwidth bound); calls with up to kMergeChunk slots
+// --------------------------------------------------------------------------
+constexpr int kMergeColsThreads = 128;
+constexpr int kMergeColsMaxCtas = 64;   // merge-kernel CTAs (2 query heads each) up to which it is used
+constexpr int kMergeCols = 32;
+constexpr int kMergeColsSmem =
+    (kHeadDim * kMergeCols + kMergeChunk * kPartFloats + kMergeChunk + 2 * kHeadDim + 4 * kMergeCols) * 4;
+
+__global__ void __launch_bounds__(kMergeColsThreads) oscar_merge_cols_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  const int g = p.gqa, nslots = p.win_slots + p.prefix_splits + p.splits, nwin = p.win_slots;
+  float* RTc = reinterpret_cast<float*>(dsm);                  // [128 rows][32 columns] of R_V^T
+  float* rows = RTc + kHeadDim * kMergeCols;                    // [nslots][kPartFloats]
+  float* wts = rows + kMergeChunk * kPartFloats;                // [nslots]
+  float* osum = wts + kMergeChunk;                              // [2][128]: INT2 sums, window sums
+  float* red = osum + 2 * kHeadDim;                             // [4][32]
+  __shared__ float lsum;
+  const int h = blockIdx.x, b = blockIdx.y, m = blockIdx.z >> 2, q = blockIdx.z & 3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int col0 = q * kMergeCols;
+  if (!p.fold_rv) {
+    // columns col0 .. col0 + 31 of every row of R_V^T[h] (constant data)
+    const float* src = p.R_VT + (size_t)h * kHeadDim * kHeadDim + col0;
+    for (int i = tid; i < kHeadDim * (kMergeCols / 4); i += kMergeColsThreads) {
+      const int r = i / (kMergeCols / 4), u = i % (kMergeCols / 4);
+      cp_async16(RTc + r * kMergeCols + 4 * u, src + (size_t)r * kHeadDim + 4 * u);
+    }
+  }
+  cp_commit();
+  // rows of query head m for every slot: slot s at ((b Hkv + h) nslots + s) g + m
+  const float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots * g + m) * kPartFloats;
+  pdl_wait();  // the partials come from the decode kernel
+  pdl_trigger();
+  constexpr int kChunks16 = kPartFloats / 4;
+  for (int i = tid; i < nslots * kChunks16; i += kMergeColsThreads) {
+    const int sl = i / kChunks16, u = i % kChunks16;
+    cp_async16(rows + sl * kPartFloats + 4 * u, part + (size_t)sl * g * kPartFloats + 4 * u);
+  }
+  cp_commit();
+  cp_wait<0>();
+  __syncthreads();
+  if (warp == 0) {
+    float mx = -INFINITY;
+    for (int sl = lane; sl < nslots; sl += 32) mx = fmaxf(mx, rows[sl * kPartFloats + kHeadDim]);
+    mx = warp_maxf(mx);
+    float ls = 0.f;
+    for (int sl = lane; sl < nslots; sl += 32) {
+      const float ms = rows[sl * kPartFloats + kHeadDim];
+      const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+      wts[sl] = w;
+      ls = fmaf(w, rows[sl * kPartFloats + kHeadDim + 1], ls);
+    }
+    ls = warp_sum(ls);
+    if (lane == 0) lsum = ls;
+  }
+  __syncthreads();
+  {
+    // thread c: the weighted sums of channel c over the INT2 and the window slots
+    const int c = tid;
+    float ow = 0.f, o0 = 0.f, o1 = 0.f;
+    int sl = 0;
+    for (; sl < nwin; ++sl) ow = fmaf(wts[sl], rows[sl * kPartFloats + c], ow);
+#pragma unroll 4
+    for (; sl + 1 < nslots; sl += 2) {
+      o0 = fmaf(wts[sl], rows[sl * kPartFloats + c], o0);
+      o1 = fmaf(wts[sl + 1], rows[(sl + 1) * kPartFloats + c], o1);
+    }
+    if (sl < nslots) o0 = fmaf(wts[sl], rows[sl * kPartFloats + c], o0);
+    osum[c] = o0 + o1;
+    osum[kHeadDim + c] = ow;
+  }
+  __syncthreads();
+  // output channel col0 + j: warp w takes rows 32 w .. 32 w + 31 of the un-rotation
+  const int j = lane;
+  float oi;
+  if (!p.fold_rv) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+    for (int r = 32 * warp; r < 32 * warp + 32; r += 2) {
+      a0 = fmaf(osum[r], RTc[r * kMergeCols + j], a0);
+      a1 = fmaf(osum[r + 1], RTc[(r + 1) * kMergeCols + j], a1);
+    }
+    red[warp * kMergeCols + j] = a0 + a1;
+    __syncthreads();
+    oi = red[j] + red[kMergeCols + j] + red[2 * kMergeCols + j] + red[3 * kMergeCols + j];
+  } else {
+    oi = osum[col0 + j];
+  }
+  if (warp == 0) {
+    const float l = lsum;
+    p.o[((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + col0 + j] =
+        l > 0.f ? (oi + osum[kHeadDim + col0 + j]) / l : 0.f;
+  }
+}
+
 int decode_smem_bytes() {
   const int window = 2 * kWinChunk * kHeadDim * 2 + (kMaxGqa * kWinChunk + 2 * kMaxGqa) * 4;
   const int merge = (kWarps * kMaxGqa * kHeadDim + kWarps * kMaxGqa * 2) * 4;
@@ -1050,6 +1151,8 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
       e = cudaFuncSetAttribute(oscar_rotate_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(oscar_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(oscar_merge_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeColsSmem);
     return e;
   });
   if (ea != cudaSuccess) return ea;
@@ -1069,9 +1172,17 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
                    dim3(p.win_slots + p.prefix_splits + p.splits, p.num_kv_heads, batch), dim3(kThreads),
                    smem, s, p);
   if (e == cudaSuccess && ev_after) e = cudaEventRecord(ev_after, s);
-  if (e == cudaSuccess)
-    e = launch_pdl(oscar_merge_kernel, dim3(p.num_kv_heads, batch, (p.gqa + 1) / 2), dim3(kMergeThreads),
-                   merge_smem_bytes(p.win_slots + p.prefix_splits + p.splits), s, p);
+  // few (request, KV head) pairs: the merge by columns (8 times the CTAs)
+  const int nslots = p.win_slots + p.prefix_splits + p.splits;
+  const bool by_cols = nslots <= kMergeChunk && (int64_t)batch * p.num_kv_heads * ((p.gqa + 1) / 2) <= kMergeColsMaxCtas;
+  if (e == cudaSuccess) {
+    if (by_cols)
+      e = launch_pdl(oscar_merge_cols_kernel, dim3(p.num_kv_heads, batch, 4 * p.gqa), dim3(kMergeColsThreads),
+                     kMergeColsSmem, s, p);
+    else
+      e = launch_pdl(oscar_merge_kernel, dim3(p.num_kv_heads, batch, (p.gqa + 1) / 2), dim3(kMergeThreads),
+                     merge_smem_bytes(nslots), s, p);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
