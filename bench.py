@@ -783,6 +783,8 @@ def main():
                              "frac": round(kach / peak, 4), "nominal_peak": NOMINAL_HBM_GBS,
                              "frac_of_nominal": round(kach / NOMINAL_HBM_GBS, 4),
                              "traffic": profiled_traffic("prefill_128k_prefix16", "prefill"),
+                             "traffic_note": "lower bound: codes written back from L2 after the kernel ends "
+                                             "are not counted in its DRAM bytes",
                              "kernel": "oscar_prefill_append_kernel",
                              "launch_us": round(pre["prefill_kernel_us"], 2),
                              "algorithmic_bytes_per_launch": pre["prefill_kernel_bytes"]},
