@@ -97,13 +97,15 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 // [code(min_c), code(max_c)], the codes of the group's clipped extremes; that
 // is the only clamp applied per element.
 //
-// Packing: the bits of kMagic + code are kMagicBits + code. Every code of a token
-// goes to a 2-bit field of one of 16 half-words: channel ch = 16 si + rr to
-// half-word 2 (rr % 8) + rr / 8 at bit 2 si (the V layout); a K word (b2, x) is the
-// pair of half-words 4 b2 + x (low) and 4 b2 + 2 + x (high). A half-word is
-// accumulated in 32 bits as sum (bits << 2 si); kMagicBits has no bits below 16,
-// so the low 16 bits are exactly the packed codes.
+// Packing: the bits of kMagic + code are kMagicBits + code, whose low 16 bits
+// are the code itself (two's complement for the negative codes of values that
+// the clamp will raise). Every code of a token goes to a 2-bit field of one of
+// 16 half-words: channel ch = 16 si + rr to half-word 2 (rr % 8) + rr / 8 at bit
+// 2 si (the V layout); a K word (b2, x) is the pair of half-words 4 b2 + x (low)
+// and 4 b2 + 2 + x (high). The eight K words are accumulated in 32-bit
+// registers; the clamped codes never carry into the next field.
 constexpr float kMagic = 12582912.f;        // 1.5 * 2^23
+constexpr uint32_t kMagicBits = 0x4B400000u; // its bit pattern
 
 __device__ __forceinline__ void chunk_minmax(const uint32_t (&r)[32], float& mn, float& mx) {
 #pragma unroll
@@ -119,9 +121,12 @@ __device__ __forceinline__ void chunk_minmax(const uint32_t (&r)[32], float& mn,
 struct GroupQ {
   __half s16, z16;
   float zf, rsf, lo, hi;
+  uint32_t lo2, hi2;   // the codes of lo and hi in both 16-bit halves
+  bool small;          // every value's code before the clamp fits a signed 16-bit half
 };
 __device__ __forceinline__ GroupQ group_params(float mn, float mx, float clip) {
   GroupQ q;
+  const float mn_raw = mn, mx_raw = mx;
   mn = fminf(fmaxf(mn, -clip), clip);
   mx = fminf(fmaxf(mx, -clip), clip);
   q.s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
@@ -131,34 +136,83 @@ __device__ __forceinline__ GroupQ group_params(float mn, float mx, float clip) {
   q.rsf = sf != 0.f ? __frcp_rn(sf) : 0.f;  // sf == 0: every code is 0
   q.lo = fminf(fmaxf(__fadd_rn(__fmul_rn(__fsub_rn(mn, q.zf), q.rsf), kMagic), kMagic), kMagic + 3.f);
   q.hi = fminf(fmaxf(__fadd_rn(__fmul_rn(__fsub_rn(mx, q.zf), q.rsf), kMagic), kMagic), kMagic + 3.f);
+  q.lo2 = (__float_as_uint(q.lo) - kMagicBits) * 0x10001u;
+  q.hi2 = (__float_as_uint(q.hi) - kMagicBits) * 0x10001u;
+  // the unclipped extremes bound every value's scaled offset (all steps are monotone)
+  const float umin = __fmul_rn(__fsub_rn(mn_raw, q.zf), q.rsf);
+  const float umax = __fmul_rn(__fsub_rn(mx_raw, q.zf), q.rsf);
+  q.small = umin > -16384.f && umax < 16384.f;
   return q;
 }
 
-// codes of the 32 channels 32 CH .. 32 CH + 31 into the packed half-words
-template <int CH>
-__device__ __forceinline__ void chunk_codes(const uint32_t (&r)[32], const GroupQ& q, uint32_t (&acc)[16]) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float m = __fadd_rn(__fmul_rn(__fsub_rn(__uint_as_float(r[i]), q.zf), q.rsf), kMagic);
-    m = fminf(fmaxf(m, q.lo), q.hi);
-    constexpr int kCh0 = 32 * CH;
-    const int ch = kCh0 + i;                            // compile-time
-    const int si = ch >> 4, rr = ch & 15;
-    acc[2 * (rr & 7) + (rr >> 3)] += __float_as_uint(m) << (2 * si);
-  }
+// fp32(fp32(x - zf) * rsf) for two values at once: the packed fp32 pair
+// instructions round every lane to nearest like the scalar ones. kMagic is
+// added by the caller with a scalar add: a packed add right after the packed
+// multiply may be contracted into one fused multiply-add (one rounding instead
+// of two), which changes the code of a product that rounds to a tie.
+__device__ __forceinline__ void scaled_pair(uint32_t x0, uint32_t x1, uint64_t zz, uint64_t rr, float& u0, float& u1) {
+  asm("{\n .reg .b64 t;\n mov.b64 t, {%2, %3};\n sub.rn.f32x2 t, t, %4;\n mul.rn.f32x2 t, t, %5;\n"
+      " mov.b64 {%0, %1}, t;\n}\n"
+      : "=f"(u0), "=f"(u1)
+      : "r"(x0), "r"(x1), "l"(zz), "l"(rr));
+}
+__device__ __forceinline__ uint64_t pair_of(float f) {
+  const uint64_t u = __float_as_uint(f);
+  return u | (u << 32);
 }
 
-__device__ __forceinline__ uint32_t low_halves(uint32_t lo, uint32_t hi) {
-  return __byte_perm(lo, hi, 0x5410);
+// codes of the 32 channels 32 CH .. 32 CH + 31 into the packed K words.
+// Channels 2 k and 2 k + 1 go to the low and high half of the same word at the
+// same shift, so a pair of codes is packed into one register (the low 16 bits
+// of kMagic + code are the code) and added at once. SMALL: the codes before the
+// clamp fit signed 16-bit halves, so both are clamped with one pair of 16-bit
+// SIMD min / max; otherwise each is clamped as a float first.
+template <int CH, bool SMALL>
+__device__ __forceinline__ void chunk_codes_t(const uint32_t (&r)[32], const GroupQ& q, uint32_t (&acc)[8]) {
+  const uint64_t zz = pair_of(q.zf), rr = pair_of(q.rsf);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float u0, u1;
+    scaled_pair(r[i], r[i + 1], zz, rr, u0, u1);
+    float m0 = __fadd_rn(u0, kMagic), m1 = __fadd_rn(u1, kMagic);
+    if (!SMALL) {
+      m0 = fminf(fmaxf(m0, q.lo), q.hi);
+      m1 = fminf(fmaxf(m1, q.lo), q.hi);
+    }
+    uint32_t pr = __byte_perm(__float_as_uint(m0), __float_as_uint(m1), 0x5410);
+    if (SMALL) {
+      asm("max.s16x2 %0, %0, %1;" : "+r"(pr) : "r"(q.lo2));
+      asm("min.s16x2 %0, %0, %1;" : "+r"(pr) : "r"(q.hi2));
+    }
+    constexpr int kCh0 = 32 * CH;
+    const int ch = kCh0 + i;                            // even, compile-time
+    const int si = ch >> 4, rr4 = ch & 15;
+    const int hw = 2 * (rr4 & 7) + (rr4 >> 3);         // half-word of the even channel
+    const int word = 2 * (hw >> 2) + (hw & 1);
+    acc[word] += pr << (2 * si);
+  }
+}
+template <int CH>
+__device__ __forceinline__ void chunk_codes(const uint32_t (&r)[32], const GroupQ& q, uint32_t (&acc)[8]) {
+  if (__all_sync(0xffffffffu, q.small))
+    chunk_codes_t<CH, true>(r, q, acc);
+  else
+    chunk_codes_t<CH, false>(r, q, acc);
 }
 
 // ---- epilogue: one token of one kind per thread ----------------------------------
-__device__ __forceinline__ uint8_t* token_block(const PrefillParams& p, int64_t pos, bool valid, int h, int b) {
-  if (!valid) return nullptr;
+// page id of a token's position: kNoPage when the position is not one this launch
+// writes, -1 when it lies past the request's page-table row; token_block reports
+// every id outside the pool and returns no block for it
+constexpr int32_t kNoPage = INT32_MIN;
+__device__ __forceinline__ int32_t token_page(const PrefillParams& p, int64_t pos, bool valid, int b) {
+  if (!valid) return kNoPage;
   const int64_t pidx = pos / kPage;
-  const int32_t id = pidx < p.pt_stride ? p.page_table[(int64_t)b * p.pt_stride + pidx] : -1;
+  return pidx < p.pt_stride ? p.page_table[(int64_t)b * p.pt_stride + pidx] : -1;
+}
+__device__ __forceinline__ uint8_t* token_block(const PrefillParams& p, int32_t id, int h) {
   if (id >= 0 && id < p.num_pages) return p.pool + ((int64_t)id * p.num_kv_heads + h) * block_bytes(p.ngroups);
-  atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
+  if (id != kNoPage) atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
   return nullptr;
 }
 
@@ -171,8 +225,9 @@ __device__ __forceinline__ void trace_group(const PrefillParams& p, const uint32
   }
 }
 
-// sz[g]: scale (low half) and zero (high half) of group g; ng groups per token
-__device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos, const uint32_t (&acc)[16],
+// words: the eight packed K words; sz[g]: scale (low half)
+// and zero (high half) of group g; ng groups per token
+__device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos, const uint32_t (&words)[8],
                                             const uint32_t (&sz)[kGroups], int ng) {
   const int t = (int)(pos % kPage);
   const int a = t & 7, bb = (t & 7) >> 1, th = t & 1, tt = t >> 3;
@@ -180,8 +235,7 @@ __device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos,
     // codes: words (b2, x) at 16 (4 a + b2) + 4 (2 tt + x)
 #pragma unroll
     for (int b2 = 0; b2 < 4; ++b2)
-      *reinterpret_cast<uint2*>(blk + 16 * (4 * a + b2) + 8 * tt) =
-          make_uint2(low_halves(acc[4 * b2], acc[4 * b2 + 2]), low_halves(acc[4 * b2 + 1], acc[4 * b2 + 3]));
+      *reinterpret_cast<uint2*>(blk + 16 * (4 * a + b2) + 8 * tt) = make_uint2(words[2 * b2], words[2 * b2 + 1]);
 #pragma unroll
     for (int g = 0; g < kGroups; ++g)
       if (g < ng) *reinterpret_cast<uint16_t*>(blk + kscale_off(ng, t, g)) = (uint16_t)sz[g];
@@ -192,10 +246,13 @@ __device__ __forceinline__ void store_token(uint8_t* blk, int kind, int64_t pos,
     else
       *reinterpret_cast<uint32_t*>(blk + kzero_off(ng, t, 0)) = __byte_perm(sz[0], sz[1], 0x7632);
   } else {
+    // half-word i of the V layout is half (i / 2) % 2 of word 2 (i / 4) + i % 2
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int a2 = i >> 1, x = i & 1;
-      *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a2 + bb) + 4 * (2 * tt + x) + 2 * th) = (uint16_t)acc[i];
+      const uint32_t w = words[2 * (i >> 2) + (i & 1)];
+      *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a2 + bb) + 4 * (2 * tt + x) + 2 * th) =
+          (uint16_t)(((i >> 1) & 1) ? (w >> 16) : w);
     }
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
@@ -352,9 +409,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
       tc_fence_after();
       const int64_t pos = tile_start(j) + row;
       const bool valid = pos >= d0 && pos < d1;
-      uint32_t acc[16];
+      // the page id of this token's position is read now and used after the
+      // arithmetic, so that its latency is hidden
+      const int32_t page = token_page(p, pos, valid, b);
+      uint32_t acc[8];   // packed K words
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc[i] = 0u;
+      for (int i = 0; i < 8; ++i) acc[i] = 0u;
       uint32_t sz[kGroups];   // scale (low half) and zero (high half) of each group
       uint32_t r[32];
       auto load_chunk = [&](int ch) {
@@ -407,7 +467,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) oscar_prefill_append_kernel(con
         }
         sz[2] = sz[3] = 0u;
       }
-      uint8_t* blk = token_block(p, pos, valid, h, b);
+      uint8_t* blk = token_block(p, page, h);
       if (blk) store_token(blk, kind, pos, acc, sz, NG);
     }
   }

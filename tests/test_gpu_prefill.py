@@ -73,11 +73,13 @@ def test_prefill_fold_rv():
     check_decode(layer, 1)
 
 
-@pytest.mark.parametrize("frac", [0.15, 0.02])
+@pytest.mark.parametrize("frac", [0.15, 0.02, 1e-5])
 def test_prefill_heavy_clipping(frac):
     """Clip values far below the calibrated ones: most groups have clipped
     extremes (and some are clipped whole), so codes of values beyond the clip
-    must come out as the codes of the clip itself."""
+    must come out as the codes of the clip itself. At 1e-5 the values beyond
+    the clip sit tens of thousands of scale steps past it, outside the 16-bit
+    range in which the epilogue clamps two codes at once."""
     layer = Layer(8, 2, 4, 64, 1, 2048, seed=11 + int(frac * 100))
     for key in ("clip_K32", "clip_V32", "clip_K", "clip_V"):
         layer.cal[key] = layer.cal[key] * frac
