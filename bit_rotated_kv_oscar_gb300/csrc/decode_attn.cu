@@ -10,7 +10,7 @@
 // Three launches on one stream:
 //   1. oscar_rotate_q_kernel   q~ = q R_K * scale * log2(e) per (request, KV head),
 //      written as ready-to-use tensor-core operand fragments (fp16 hi + lo).
-//   2. oscar_decode_kernel<NG, FEW> grid (window chunks + prefix splits + splits, Hkv,
+//   2. oscar_decode_kernel<NG, FEW, MERGED> grid (window chunks + prefix splits + splits, Hkv,
 //      B), NG = 128 / group size: the first CTAs attend over the BF16 sink +
 //      recent ring in the raw basis (64 or 160 tokens each, per call); the
 //      others stream a slice of the INT2 pages, computing scores and the P.V
@@ -232,14 +232,18 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
   // column fragments of m16n8k16 (k = channel, n = head): per slot kb and lane
   // (gid, tig) four words, hi parts of head gid at channels 16 kb + 2 tig (+1) and
   // + 8 (+9), then the lo parts at the same channels, so that each operand pair
-  // is one aligned half of the 16-byte record entry
+  // is one aligned half of the 16-byte record entry. With g = 1, 2 or 4 heads the
+  // hi words of the spare columns gid = g .. 2g - 1 carry the lo parts of heads
+  // gid - g, so that one product per slot covers both parts (the merged scores)
+  const bool merged = g == 1 || g == 2 || g == 4;
 #pragma unroll
   for (int n = 0; n < 4; ++n) {
     const int widx = tid + kRotThreads * n;
     const int r = widx & 3, lane = (widx >> 2) & 31, kb = widx >> 7;
     const int gid = lane >> 2, tig = lane & 3;
     const int col = kb * 16 + 2 * tig + ((r & 1) ? 8 : 0);
-    const __half* src = hs[r >> 1][gid];
+    const bool spare_lo = merged && r < 2 && gid >= g && gid < 2 * g;
+    const __half* src = spare_lo ? hs[1][gid - g] : hs[r >> 1][gid];
     const uint32_t lo = __half_as_ushort(src[col]);
     const uint32_t hi = __half_as_ushort(src[col + 1]);
     rec[widx] = lo | (hi << 16);
@@ -387,9 +391,13 @@ constexpr float kLazyLog2 = 8.f;
 // so hi + lo needs no extra add. zqb: the zero-point column operand (group sums
 // of q~, hi in k rows 0-3, lo in rows 4-7).
 // NG: quantisation groups per token (4 of 32 channels, or 2 of 64).
-template <int NG>
+// MERGED (query groups of 1, 2 or 4 heads): columns g .. 2g - 1 of the query
+// operand hold the lo parts of heads 0 .. g - 1 (see oscar_rotate_q_kernel), so
+// one product per slot covers hi and lo, and the two column halves are added
+// afterwards (within a lane for g = 1, across lanes tig ^ (g / 2) otherwise).
+template <int NG, bool MERGED>
 __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* sbB, const uint4* qs,
-                                            uint32_t zqb, int lane, float (&u)[8]) {
+                                            uint32_t zqb, int lane, int g, float (&u)[8]) {
   const int gid = lane >> 2, tig = lane & 3;
   const uint4 kwA = *reinterpret_cast<const uint4*>(sbA + lane * 16);
   const uint4 kwB = *reinterpret_cast<const uint4*>(sbB + lane * 16);
@@ -420,15 +428,21 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
     float a[4], c[4];
 #define OSCAR_QK(KB, MMA)                                                                          \
   {                                                                                                \
-    const uint4 q4 = qs[(KB) * 32 + lane];                                                         \
     const uint32_t xa = slot_bits<KB>(kwA.x, kwAh.x), ya = slot_bits<KB>(kwA.y, kwAh.y);           \
     const uint32_t za = slot_bits<KB>(kwA.z, kwAh.z), wa = slot_bits<KB>(kwA.w, kwAh.w);           \
     const uint32_t xb = slot_bits<KB>(kwB.x, kwBh.x), yb = slot_bits<KB>(kwB.y, kwBh.y);           \
     const uint32_t zb = slot_bits<KB>(kwB.z, kwBh.z), wb = slot_bits<KB>(kwB.w, kwBh.w);           \
-    MMA(a, xa, za, ya, wa, q4.x, q4.y);                                                            \
-    mma16816(a, xa, za, ya, wa, q4.z, q4.w);                                                       \
-    MMA(c, xb, zb, yb, wb, q4.x, q4.y);                                                            \
-    mma16816(c, xb, zb, yb, wb, q4.z, q4.w);                                                       \
+    if constexpr (MERGED) {                                                                        \
+      const uint2 q2 = reinterpret_cast<const uint2*>(qs)[2 * ((KB) * 32 + lane)];                 \
+      MMA(a, xa, za, ya, wa, q2.x, q2.y);                                                          \
+      MMA(c, xb, zb, yb, wb, q2.x, q2.y);                                                          \
+    } else {                                                                                       \
+      const uint4 q4 = qs[(KB) * 32 + lane];                                                       \
+      MMA(a, xa, za, ya, wa, q4.x, q4.y);                                                          \
+      mma16816(a, xa, za, ya, wa, q4.z, q4.w);                                                     \
+      MMA(c, xb, zb, yb, wb, q4.x, q4.y);                                                          \
+      mma16816(c, xb, zb, yb, wb, q4.z, q4.w);                                                     \
+    }                                                                                              \
   }
     if constexpr (NG == kGroups) {
       if (gq == 0) { OSCAR_QK(0, mma16816_z) OSCAR_QK(1, mma16816) }
@@ -450,6 +464,18 @@ __device__ __forceinline__ void pair_scores(const uint8_t* sbA, const uint8_t* s
     u[5] = fmaf(sB.x, c[1], u[5]);
     u[6] = fmaf(sB.y, c[2], u[6]);
     u[7] = fmaf(sB.y, c[3], u[7]);
+  }
+  if constexpr (MERGED) {
+    if (g == 1) {
+      // column 0: hi, column 1: lo of the one head (lane tig = 0)
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) u[i] = u[i + 1] = u[i] + u[i + 1];
+    } else {
+      // lanes tig and tig ^ (g / 2) hold the hi and lo columns of the same heads
+      const int x = g >> 1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] += __shfl_xor_sync(0xffffffffu, u[i], x);
+    }
   }
 }
 
@@ -544,7 +570,7 @@ __device__ __forceinline__ void zero_masked_value_meta(uint8_t* sbA, uint8_t* sb
 // FEW: every warp of the CTA streams at most 64 pages (splits of up to 512
 // pages, the automatic split sizes), so all of a warp's page ids fit two
 // registers per lane.
-template <int NG, bool PACK, bool FEW>
+template <int NG, bool PACK, bool FEW, bool MERGED = false>
 __device__ void int2_attention(const DecodeParams& p, int h, int split, int nsplits, int r0, int nreq,
                                uint32_t okmask, int lo, int hi, int slot, uint8_t* smem, uint4* qs,
                                int2* wbounds) {
@@ -704,7 +730,7 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     uint8_t* sbB = sbA + kBlockBytes;
 
     float u[8];
-    pair_scores<NG>(sbA, sbB, qs, zqb, lane, u);
+    pair_scores<NG, MERGED>(sbA, sbB, qs, zqb, lane, g, u);
     if (MASKED) {
       // tokens outside [lo, hi), on a page the warp does not have or whose id is
       // outside the pool: scores -inf, and their value scales and zeros set to 0
@@ -850,7 +876,7 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
 // INT2 CTAs keep all their page ids in registers; the host picks the instance
 // from the page-table width and the split counts (few_pages_call)
 constexpr int kFewPages = 64 * kWarps;
-template <int NG, bool FEW>
+template <int NG, bool FEW, bool MERGED>
 __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint4 qs[8 * 32];
@@ -886,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
     const oscar_seq_state st = p.state[z];
     const bool ok = state_ok(st, S, W, p.max_batch);
     const int lo = max(S, P), hi = min(st.int2_end, st.seq_len);
-    int2_attention<NG, false, FEW>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo, hi,
+    int2_attention<NG, false, FEW, MERGED>(p, h, x - p.win_slots - p.prefix_splits, p.splits, z, 1, ok ? 1u : 0u, lo, hi,
                                    x, smem, qs, wb);
   }
 }
@@ -1139,14 +1165,13 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
   static PerDeviceOnce attrs;
   const int smem = decode_smem_bytes();
   cudaError_t ea = once_for_current_device(attrs, [&] {
-    cudaError_t e =
-        cudaFuncSetAttribute(oscar_decode_kernel<kGroups, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(oscar_decode_kernel<kGroups, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(oscar_decode_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(oscar_decode_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    void (*const kernels[])(DecodeParams) = {
+        oscar_decode_kernel<kGroups, true, false>, oscar_decode_kernel<kGroups, false, false>,
+        oscar_decode_kernel<2, true, false>,       oscar_decode_kernel<2, false, false>,
+        oscar_decode_kernel<kGroups, true, true>,  oscar_decode_kernel<2, true, true>};
+    cudaError_t e = cudaSuccess;
+    for (auto k : kernels)
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(oscar_rotate_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmem);
     if (e == cudaSuccess)
@@ -1163,12 +1188,17 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
   const int64_t prefix_pages = (int64_t)(p.prefix_tokens + kPage - 1) / kPage;
   const bool few = (p.pt_stride + p.splits - 1) / p.splits <= kFewPages &&
                    (p.prefix_splits == 0 || (prefix_pages + p.prefix_splits - 1) / p.prefix_splits <= kFewPages);
+  // one query-operand product per slot covers hi and lo (see pair_scores)
+  const bool merged = p.gqa == 1 || p.gqa == 2 || p.gqa == 4;
   cudaError_t e = launch_pdl(oscar_rotate_q_kernel, dim3(p.num_kv_heads, batch), dim3(kRotThreads), kRotSmem,
                              s, p);
   if (e == cudaSuccess && ev_before) e = cudaEventRecord(ev_before, s);
   if (e == cudaSuccess)
-    e = launch_pdl(p.ngroups == kGroups ? (few ? oscar_decode_kernel<kGroups, true> : oscar_decode_kernel<kGroups, false>)
-                                        : (few ? oscar_decode_kernel<2, true> : oscar_decode_kernel<2, false>),
+    e = launch_pdl(p.ngroups == kGroups
+                       ? (few ? (merged ? oscar_decode_kernel<kGroups, true, true> : oscar_decode_kernel<kGroups, true, false>)
+                              : oscar_decode_kernel<kGroups, false, false>)
+                       : (few ? (merged ? oscar_decode_kernel<2, true, true> : oscar_decode_kernel<2, true, false>)
+                              : oscar_decode_kernel<2, false, false>),
                    dim3(p.win_slots + p.prefix_splits + p.splits, p.num_kv_heads, batch), dim3(kThreads),
                    smem, s, p);
   if (e == cudaSuccess && ev_after) e = cudaEventRecord(ev_after, s);
