@@ -274,12 +274,19 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
 //     [c x, c x + c), c = p.win_chunk (sink first, then the ring in position
 //     order)
 // --------------------------------------------------------------------------
+// Shared-memory rows are padded so that the rows read by one warp fall into
+// different banks (8 consecutive rows of a K / V chunk, the query heads).
+constexpr int kWinRow = kHeadDim + 8;   // bf16 elements per staged window row (272 bytes)
+constexpr int kQRow = kHeadDim + 4;     // floats per staged query row
+constexpr int kWindowSmem = 2 * kWinChunk * kWinRow * 2 + kMaxGqa * kQRow * 4 + (kMaxGqa * kWinChunk + 2 * kMaxGqa) * 4;
+
 __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = p.gqa, S = p.sink, W = p.recent;
-  __nv_bfloat16* krows = reinterpret_cast<__nv_bfloat16*>(smem);             // [chunk][128]
-  __nv_bfloat16* vrows = krows + kWinChunk * kHeadDim;                        // [chunk][128]
-  float* sc = reinterpret_cast<float*>(vrows + kWinChunk * kHeadDim);         // [8][chunk]
+  __nv_bfloat16* krows = reinterpret_cast<__nv_bfloat16*>(smem);             // [chunk][kWinRow]
+  __nv_bfloat16* vrows = krows + kWinChunk * kWinRow;                         // [chunk][kWinRow]
+  float* qsm = reinterpret_cast<float*>(vrows + kWinChunk * kWinRow);         // [8][kQRow]
+  float* sc = qsm + kMaxGqa * kQRow;                                          // [8][chunk]
   float* stat = sc + kMaxGqa * kWinChunk;                                     // [8][2]
   const int nslots = p.win_slots + p.prefix_splits + p.splits;
   float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots + chunk) * g * kPartFloats;
@@ -300,41 +307,42 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
   for (int idx = tid; idx < n * 16; idx += kThreads) {
     const int r = idx >> 4, u = idx & 15, t = t0 + r;
     const int slot = t < ns ? t : S + (rb + t - ns) % W;
-    cp_async16(krows + r * kHeadDim + 8 * u, wk + (size_t)slot * kHeadDim + 8 * u);
-    cp_async16(vrows + r * kHeadDim + 8 * u, wv + (size_t)slot * kHeadDim + 8 * u);
+    cp_async16(krows + r * kWinRow + 8 * u, wk + (size_t)slot * kHeadDim + 8 * u);
+    cp_async16(vrows + r * kWinRow + 8 * u, wv + (size_t)slot * kHeadDim + 8 * u);
   }
   cp_commit();
-  // query channels 4*lane .. 4*lane+3 of every head, in registers
-  float qr[kMaxGqa][4];
-#pragma unroll
-  for (int m = 0; m < kMaxGqa; ++m) {
-    if (m < g) {
-      // element loads: q needs no alignment beyond its element size
-      const __nv_bfloat16* qp = p.q + ((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + 4 * lane;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) qr[m][e] = __bfloat162float(qp[e]) * p.scale_log2;
-    } else {
-      qr[m][0] = qr[m][1] = qr[m][2] = qr[m][3] = 0.f;
-    }
+  // the query heads of this KV head, scaled to log2 units (element loads: q needs
+  // no alignment beyond its element size)
+  for (int i = tid; i < g * kHeadDim; i += kThreads) {
+    const int m = i >> 7, c = i & (kHeadDim - 1);
+    qsm[m * kQRow + c] = __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + c]) * p.scale_log2;
   }
   cp_wait<0>();
   __syncthreads();
-  // scores: one warp per token, lanes over channels
-  for (int r = warp; r < n; r += kWarps) {
-    const uint2 w = reinterpret_cast<const uint2*>(krows + r * kHeadDim)[lane];
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
-    const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
-#pragma unroll
-    for (int m = 0; m < kMaxGqa; ++m) {
-      if (m < g) {
-        float d = qr[m][0] * a.x;
-        d = fmaf(qr[m][1], a.y, d);
-        d = fmaf(qr[m][2], c.x, d);
-        d = fmaf(qr[m][3], c.y, d);
-        d = warp_sum(d);
-        if (lane == 0) sc[m * kWinChunk + r] = d;
-      }
+  // scores: one (token, head) pair per thread, the whole dot product
+  for (int i = tid; i < n * g; i += kThreads) {
+    const int r = i / g, m = i - r * g;
+    const uint4* kr = reinterpret_cast<const uint4*>(krows + r * kWinRow);
+    const float4* qr = reinterpret_cast<const float4*>(qsm + m * kQRow);
+    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll 4
+    for (int u = 0; u < kHeadDim / 8; ++u) {
+      const uint4 kw = kr[u];
+      const float4 qa = qr[2 * u], qb = qr[2 * u + 1];
+      const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.x));
+      const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.y));
+      const float2 k2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.z));
+      const float2 k3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.w));
+      d0 = fmaf(qa.x, k0.x, d0);
+      d1 = fmaf(qa.y, k0.y, d1);
+      d2 = fmaf(qa.z, k1.x, d2);
+      d3 = fmaf(qa.w, k1.y, d3);
+      d0 = fmaf(qb.x, k2.x, d0);
+      d1 = fmaf(qb.y, k2.y, d1);
+      d2 = fmaf(qb.z, k3.x, d2);
+      d3 = fmaf(qb.w, k3.y, d3);
     }
+    sc[m * kWinChunk + r] = (d0 + d1) + (d2 + d3);
   }
   __syncthreads();
   for (int m = warp; m < g; m += kWarps) {
@@ -354,16 +362,38 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
     }
   }
   __syncthreads();
-  // values: thread per (head, channel)
-  for (int i = tid; i < g * kHeadDim; i += kThreads) {
-    const int m = i >> 7, c = i & (kHeadDim - 1);
-    float acc = 0.f;
-    for (int r = 0; r < n; ++r) acc = fmaf(sc[m * kWinChunk + r], __bfloat162float(vrows[r * kHeadDim + c]), acc);
-    float* dst = part + (size_t)m * kPartFloats;
-    dst[c] = acc;
-    if (c == 0) {
-      dst[kHeadDim] = stat[2 * m];
-      dst[kHeadDim + 1] = stat[2 * m + 1];
+  // values: thread (channel pair cp, head set mh) for channels 2 cp, 2 cp + 1 of
+  // heads mh, mh + 4 (a warp shares mh, so the probabilities are broadcast)
+  {
+    const int cp = tid & 63, mh = tid >> 6;
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+    const bool two = mh + 4 < g;
+    if (mh < g) {
+      const float* p0 = sc + mh * kWinChunk;
+      const float* p1 = sc + (two ? mh + 4 : mh) * kWinChunk;
+#pragma unroll 4
+      for (int r = 0; r < n; ++r) {
+        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vrows + r * kWinRow + 2 * cp));
+        const float w0 = p0[r], w1 = p1[r];
+        a0 = fmaf(w0, v.x, a0);
+        a1 = fmaf(w0, v.y, a1);
+        b0 = fmaf(w1, v.x, b0);
+        b1 = fmaf(w1, v.y, b1);
+      }
+      float* dst = part + (size_t)mh * kPartFloats;
+      *reinterpret_cast<float2*>(dst + 2 * cp) = make_float2(a0, a1);
+      if (cp == 0) {
+        dst[kHeadDim] = stat[2 * mh];
+        dst[kHeadDim + 1] = stat[2 * mh + 1];
+      }
+      if (two) {
+        float* dst2 = part + (size_t)(mh + 4) * kPartFloats;
+        *reinterpret_cast<float2*>(dst2 + 2 * cp) = make_float2(b0, b1);
+        if (cp == 0) {
+          dst2[kHeadDim] = stat[2 * (mh + 4)];
+          dst2[kHeadDim + 1] = stat[2 * (mh + 4) + 1];
+        }
+      }
     }
   }
 }
@@ -1152,7 +1182,7 @@ __global__ void __launch_bounds__(kMergeColsThreads) oscar_merge_cols_kernel(Dec
 }
 
 int decode_smem_bytes() {
-  const int window = 2 * kWinChunk * kHeadDim * 2 + (kMaxGqa * kWinChunk + 2 * kMaxGqa) * 4;
+  const int window = kWindowSmem;
   const int merge = (kWarps * kMaxGqa * kHeadDim + kWarps * kMaxGqa * 2) * 4;
   int m = kStageBytes;
   if (window > m) m = window;
