@@ -850,8 +850,11 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   // ---- per-warp partial -> shared memory, then CTA merge --------------------
   const float inv_ps = 1.f / pscale;
   __syncthreads();  // staging buffers are reused below
-  float* wpart = reinterpret_cast<float*>(smem);              // [8 warps][8 heads][128]
-  float* wml = wpart + kWarps * kMaxGqa * kHeadDim;           // [8 warps][8 heads][2]
+  // rows padded by 4 floats: the 32 lanes of a warp store (2 tig + e, 16 cb + gid)
+  // into 32 different banks
+  constexpr int kWRow = kHeadDim + 4;
+  float* wpart = reinterpret_cast<float*>(smem);              // [8 warps][8 heads][kWRow]
+  float* wml = wpart + kWarps * kMaxGqa * kWRow;              // [8 warps][8 heads][2]
   if (gid == 4) {
     // oz row 4: the sums of the probabilities of heads 2 tig, 2 tig + 1
     wml[(warp * kMaxGqa + 2 * tig) * 2] = m0 * us0;             // log2 units
@@ -867,11 +870,11 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     const float sc = 16777216.f / slot_factor(cb) * inv_ps;
     const int ch = 16 * cb + gid;
     const int he = 2 * tig, ho = 2 * tig + 1;
-    float* base = wpart + warp * kMaxGqa * kHeadDim;
-    base[he * kHeadDim + ch] = fmaf(acc[cb][0], sc, ze);
-    base[ho * kHeadDim + ch] = fmaf(acc[cb][1], sc, zo);
-    base[he * kHeadDim + ch + 8] = fmaf(acc[cb][2], sc, ze);
-    base[ho * kHeadDim + ch + 8] = fmaf(acc[cb][3], sc, zo);
+    float* base = wpart + warp * kMaxGqa * kWRow;
+    base[he * kWRow + ch] = fmaf(acc[cb][0], sc, ze);
+    base[ho * kWRow + ch] = fmaf(acc[cb][1], sc, zo);
+    base[he * kWRow + ch + 8] = fmaf(acc[cb][2], sc, ze);
+    base[ho * kWRow + ch + 8] = fmaf(acc[cb][3], sc, zo);
   }
   __syncthreads();
   const int nslots = p.win_slots + p.prefix_splits + p.splits;
@@ -888,7 +891,7 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
       for (int w = 0; w < kWarps; ++w) {
         const float mw = wml[(w * kMaxGqa + n) * 2];
         const float sw = mw == -INFINITY ? 0.f : exp2f(mw - M);
-        o = fmaf(sw, wpart[(w * kMaxGqa + n) * kHeadDim + c], o);
+        o = fmaf(sw, wpart[(w * kMaxGqa + n) * kWRow + c], o);
         l = fmaf(sw, wml[(w * kMaxGqa + n) * 2 + 1], l);
       }
     }
@@ -1183,7 +1186,7 @@ __global__ void __launch_bounds__(kMergeColsThreads) oscar_merge_cols_kernel(Dec
 
 int decode_smem_bytes() {
   const int window = kWindowSmem;
-  const int merge = (kWarps * kMaxGqa * kHeadDim + kWarps * kMaxGqa * 2) * 4;
+  const int merge = (kWarps * kMaxGqa * (kHeadDim + 4) + kWarps * kMaxGqa * 2) * 4;
   int m = kStageBytes;
   if (window > m) m = window;
   if (merge > m) m = merge;
