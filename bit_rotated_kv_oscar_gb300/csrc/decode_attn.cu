@@ -877,30 +877,44 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     base[ho * kWRow + ch + 8] = fmaf(acc[cb][3], sc, zo);
   }
   __syncthreads();
-  const int nslots = p.win_slots + p.prefix_splits + p.splits;
-  for (int i = tid; i < (PACK ? nreq : 1) * g * kHeadDim; i += kThreads) {
-    const int n = i / kHeadDim, c = i % kHeadDim;  // column n: head n % g of request r0 + n / g
-    const int cr = PACK ? n / g : 0;
-    const bool okr = (okmask >> cr) & 1u;
-    float M = -INFINITY;
+  // per column n the weights of the 8 warps' partials, their running maximum and
+  // the merged sum, once: thread (n, w) for the first 8 ncols threads, the 8 warps
+  // of a column being 8 consecutive lanes
+  const int ncols = (PACK ? nreq : 1) * g;
+  float* wts = wml + kWarps * kMaxGqa * 2;   // [8 columns][8 warps], then [8 columns][2]: M, l
+  if (warp < (kWarps * ncols + 31) / 32) {   // whole warps (the shuffles); lanes past the columns write nothing
+    const int n = tid >> 3, w = tid & 7;   // n < 8 here
+    const float mw = wml[(w * kMaxGqa + n) * 2];
+    float M = mw;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * kMaxGqa + n) * 2]);
-    float o = 0.f, l = 0.f;
-    if (okr && M != -INFINITY) {
+    for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const bool okr = (okmask >> (PACK ? n / g : 0)) & 1u;
+    const float sw = (!okr || mw == -INFINITY) ? 0.f : exp2f(mw - M);
+    float l = sw * wml[(w * kMaxGqa + n) * 2 + 1];
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = wml[(w * kMaxGqa + n) * 2];
-        const float sw = mw == -INFINITY ? 0.f : exp2f(mw - M);
-        o = fmaf(sw, wpart[(w * kMaxGqa + n) * kWRow + c], o);
-        l = fmaf(sw, wml[(w * kMaxGqa + n) * 2 + 1], l);
+    for (int o = 1; o < 8; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    if (n < ncols) {
+      wts[n * kWarps + w] = sw;
+      if (w == 0) {
+        wts[kWarps * kMaxGqa + 2 * n] = okr ? M : -INFINITY;
+        wts[kWarps * kMaxGqa + 2 * n + 1] = l;
       }
     }
+  }
+  __syncthreads();
+  const int nslots = p.win_slots + p.prefix_splits + p.splits;
+  for (int i = tid; i < ncols * kHeadDim; i += kThreads) {
+    const int n = i / kHeadDim, c = i % kHeadDim;  // column n: head n % g of request r0 + n / g
+    const int cr = PACK ? n / g : 0;
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) o = fmaf(wts[n * kWarps + w], wpart[(w * kMaxGqa + n) * kWRow + c], o);
     float* dst = p.part + ((((size_t)(r0 + cr) * p.num_kv_heads + h) * nslots + slot) * g + (PACK ? n % g : n)) *
                               kPartFloats;
     dst[c] = o;
     if (c == 0) {
-      dst[kHeadDim] = okr ? M : -INFINITY;
-      dst[kHeadDim + 1] = l;
+      dst[kHeadDim] = wts[kWarps * kMaxGqa + 2 * n];
+      dst[kHeadDim + 1] = wts[kWarps * kMaxGqa + 2 * n + 1];
     }
   }
 }
@@ -1186,7 +1200,7 @@ __global__ void __launch_bounds__(kMergeColsThreads) oscar_merge_cols_kernel(Dec
 
 int decode_smem_bytes() {
   const int window = kWindowSmem;
-  const int merge = (kWarps * kMaxGqa * (kHeadDim + 4) + kWarps * kMaxGqa * 2) * 4;
+  const int merge = (kWarps * kMaxGqa * (kHeadDim + 4) + kWarps * kMaxGqa * 2 + kMaxGqa * kWarps + kMaxGqa * 2) * 4;
   int m = kStageBytes;
   if (window > m) m = window;
   if (merge > m) m = merge;
