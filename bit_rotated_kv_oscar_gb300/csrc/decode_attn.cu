@@ -274,19 +274,50 @@ __global__ void __launch_bounds__(kRotThreads) oscar_rotate_q_kernel(DecodeParam
 //     [c x, c x + c), c = p.win_chunk (sink first, then the ring in position
 //     order)
 // --------------------------------------------------------------------------
-// Shared-memory rows are padded so that the rows read by one warp fall into
-// different banks (8 consecutive rows of a K / V chunk, the query heads).
-constexpr int kWinRow = kHeadDim + 8;   // bf16 elements per staged window row (272 bytes)
-constexpr int kQRow = kHeadDim + 4;     // floats per staged query row
-constexpr int kWindowSmem = 2 * kWinChunk * kWinRow * 2 + kMaxGqa * kQRow * 4 + (kMaxGqa * kWinChunk + 2 * kMaxGqa) * 4;
+// Shared-memory rows are padded by 16 bytes so that the 8 rows an 8x8 matrix
+// load reads fall into different banks.
+constexpr int kWinRow = kHeadDim + 8;   // bf16 elements per staged window / query row (272 bytes)
+constexpr int kWindowSmem = 2 * kWinChunk * kWinRow * 2 + kMaxGqa * kWinRow * 2 + (kMaxGqa * kWinChunk + 2 * kMaxGqa) * 4;
+static_assert(kWinChunk % 16 == 0, "window chunks are whole 16-token tiles");
 
+// four 8x8 b16 matrices from shared memory (lane l gives the row address of
+// matrix l / 8), optionally transposed
+__device__ __forceinline__ void ldsm_x4(uint32_t saddr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(saddr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t saddr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(saddr));
+}
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// a bf16 pair as an fp16 pair (exact for the window's values: 8-bit mantissas
+// inside the fp16 range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+  return f2_to_h2_bits(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
+// The chunk's tokens as 16-token tiles (rows past the chunk zero-filled). Scores:
+// warp w takes tiles w, w + 8 with the K rows as the bf16 row operand and the
+// raw bf16 query heads as the column operand (exact products, fp32 sums), scaled
+// to log2 units afterwards. Values: warp w takes channels 16 w .. 16 w + 15 for
+// every tile, V^T as the row operand (fp16 after a conversion that is exact for
+// values of magnitude 2^-14 .. 65504) and the fp16 probabilities as the column
+// operand, as in the INT2 value product.
 __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3;
   const int g = p.gqa, S = p.sink, W = p.recent;
   __nv_bfloat16* krows = reinterpret_cast<__nv_bfloat16*>(smem);             // [chunk][kWinRow]
   __nv_bfloat16* vrows = krows + kWinChunk * kWinRow;                         // [chunk][kWinRow]
-  float* qsm = reinterpret_cast<float*>(vrows + kWinChunk * kWinRow);         // [8][kQRow]
-  float* sc = qsm + kMaxGqa * kQRow;                                          // [8][chunk]
+  __nv_bfloat16* qb = vrows + kWinChunk * kWinRow;                            // [8][kWinRow]
+  float* sc = reinterpret_cast<float*>(qb + kMaxGqa * kWinRow);               // [8][chunk]
   float* stat = sc + kMaxGqa * kWinChunk;                                     // [8][2]
   const int nslots = p.win_slots + p.prefix_splits + p.splits;
   float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots + chunk) * g * kPartFloats;
@@ -299,61 +330,66 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
   const int nr = ok && L > rb ? L - rb : 0;
   const int t0 = chunk * p.win_chunk;
   const int n = max(0, min(p.win_chunk, ns + nr - t0));
+  const int ntiles = (n + 15) / 16;
   const size_t slots = (size_t)(S + W);
   const size_t wrow = ok ? (size_t)st.window_row : 0;
   const __nv_bfloat16* wk = p.window + ((wrow * p.num_kv_heads + h) * 2 + 0) * slots * kHeadDim;
   const __nv_bfloat16* wv = p.window + ((wrow * p.num_kv_heads + h) * 2 + 1) * slots * kHeadDim;
 
-  for (int idx = tid; idx < n * 16; idx += kThreads) {
+  for (int idx = tid; idx < ntiles * 16 * 16; idx += kThreads) {
     const int r = idx >> 4, u = idx & 15, t = t0 + r;
-    const int slot = t < ns ? t : S + (rb + t - ns) % W;
-    cp_async16(krows + r * kWinRow + 8 * u, wk + (size_t)slot * kHeadDim + 8 * u);
-    cp_async16(vrows + r * kWinRow + 8 * u, wv + (size_t)slot * kHeadDim + 8 * u);
+    const bool in = r < n;
+    const int slot = !in ? 0 : (t < ns ? t : S + (rb + t - ns) % W);
+    cp_async16_s((uint32_t)__cvta_generic_to_shared(krows + r * kWinRow + 8 * u), wk + (size_t)slot * kHeadDim + 8 * u,
+                 in ? 16u : 0u);
+    cp_async16_s((uint32_t)__cvta_generic_to_shared(vrows + r * kWinRow + 8 * u), wv + (size_t)slot * kHeadDim + 8 * u,
+                 in ? 16u : 0u);
   }
   cp_commit();
-  // the query heads of this KV head, scaled to log2 units (element loads: q needs
-  // no alignment beyond its element size)
-  for (int i = tid; i < g * kHeadDim; i += kThreads) {
+  // the raw query heads of this KV head (element loads: q needs no alignment
+  // beyond its element size); heads past g are zero
+  for (int i = tid; i < kMaxGqa * kHeadDim; i += kThreads) {
     const int m = i >> 7, c = i & (kHeadDim - 1);
-    qsm[m * kQRow + c] = __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + c]) * p.scale_log2;
+    qb[m * kWinRow + c] = m < g ? p.q[((size_t)b * p.num_q_heads + h * g + m) * kHeadDim + c] : __float2bfloat16(0.f);
   }
   cp_wait<0>();
   __syncthreads();
-  // scores: one (token, head) pair per thread, the whole dot product
-  for (int i = tid; i < n * g; i += kThreads) {
-    const int r = i / g, m = i - r * g;
-    const uint4* kr = reinterpret_cast<const uint4*>(krows + r * kWinRow);
-    const float4* qr = reinterpret_cast<const float4*>(qsm + m * kQRow);
-    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-#pragma unroll 4
-    for (int u = 0; u < kHeadDim / 8; ++u) {
-      const uint4 kw = kr[u];
-      const float4 qa = qr[2 * u], qb = qr[2 * u + 1];
-      const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.x));
-      const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.y));
-      const float2 k2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.z));
-      const float2 k3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.w));
-      d0 = fmaf(qa.x, k0.x, d0);
-      d1 = fmaf(qa.y, k0.y, d1);
-      d2 = fmaf(qa.z, k1.x, d2);
-      d3 = fmaf(qa.w, k1.y, d3);
-      d0 = fmaf(qb.x, k2.x, d0);
-      d1 = fmaf(qb.y, k2.y, d1);
-      d2 = fmaf(qb.z, k3.x, d2);
-      d3 = fmaf(qb.w, k3.y, d3);
+  const uint32_t ks = (uint32_t)__cvta_generic_to_shared(krows), vs = (uint32_t)__cvta_generic_to_shared(vrows);
+  for (int t = warp; t < ntiles; t += kWarps) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    const int j = lane >> 3;
+    const uint32_t arow = ks + (uint32_t)(((16 * t + (lane & 7) + 8 * (j & 1)) * kWinRow + 8 * (j >> 1)) * 2);
+#pragma unroll
+    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(arow + 32 * kk, a0, a1, a2, a3);
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(qb + gid * kWinRow + 16 * kk + 2 * tig);
+      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(qb + gid * kWinRow + 16 * kk + 2 * tig + 8);
+      mma16816_bf16(d, a0, a1, a2, a3, b0, b1);
     }
-    sc[m * kWinChunk + r] = (d0 + d1) + (d2 + d3);
+    const int r0 = 16 * t + gid, h0 = 2 * tig;
+    if (h0 < g) {
+      sc[h0 * kWinChunk + r0] = d[0] * p.scale_log2;
+      sc[h0 * kWinChunk + r0 + 8] = d[2] * p.scale_log2;
+    }
+    if (h0 + 1 < g) {
+      sc[(h0 + 1) * kWinChunk + r0] = d[1] * p.scale_log2;
+      sc[(h0 + 1) * kWinChunk + r0 + 8] = d[3] * p.scale_log2;
+    }
   }
   __syncthreads();
+  // softmax per head; the probabilities of the tile rows past the chunk are 0.
+  // The sum adds the probabilities as the value product sees them (rounded to
+  // fp16), so that numerator and denominator agree to the last bit of p.
   for (int m = warp; m < g; m += kWarps) {
     float mx = -INFINITY;
     for (int t = lane; t < n; t += 32) mx = fmaxf(mx, sc[m * kWinChunk + t]);
     mx = warp_maxf(mx);
     float l = 0.f;
-    for (int t = lane; t < n; t += 32) {
-      const float e = exp2f(sc[m * kWinChunk + t] - mx);
+    for (int t = lane; t < 16 * ntiles; t += 32) {
+      const float e = t < n ? exp2f(sc[m * kWinChunk + t] - mx) : 0.f;
       sc[m * kWinChunk + t] = e;
-      l += e;
+      l += __half2float(__float2half_rn(e));
     }
     l = warp_sum(l);
     if (lane == 0) {
@@ -362,38 +398,33 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
     }
   }
   __syncthreads();
-  // values: thread (channel pair cp, head set mh) for channels 2 cp, 2 cp + 1 of
-  // heads mh, mh + 4 (a warp shares mh, so the probabilities are broadcast)
   {
-    const int cp = tid & 63, mh = tid >> 6;
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-    const bool two = mh + 4 < g;
-    if (mh < g) {
-      const float* p0 = sc + mh * kWinChunk;
-      const float* p1 = sc + (two ? mh + 4 : mh) * kWinChunk;
-#pragma unroll 4
-      for (int r = 0; r < n; ++r) {
-        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vrows + r * kWinRow + 2 * cp));
-        const float w0 = p0[r], w1 = p1[r];
-        a0 = fmaf(w0, v.x, a0);
-        a1 = fmaf(w0, v.y, a1);
-        b0 = fmaf(w1, v.x, b0);
-        b1 = fmaf(w1, v.y, b1);
-      }
-      float* dst = part + (size_t)mh * kPartFloats;
-      *reinterpret_cast<float2*>(dst + 2 * cp) = make_float2(a0, a1);
-      if (cp == 0) {
-        dst[kHeadDim] = stat[2 * mh];
-        dst[kHeadDim + 1] = stat[2 * mh + 1];
-      }
-      if (two) {
-        float* dst2 = part + (size_t)(mh + 4) * kPartFloats;
-        *reinterpret_cast<float2*>(dst2 + 2 * cp) = make_float2(b0, b1);
-        if (cp == 0) {
-          dst2[kHeadDim] = stat[2 * (mh + 4)];
-          dst2[kHeadDim + 1] = stat[2 * (mh + 4) + 1];
-        }
-      }
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    const int j = lane >> 3;
+    const uint32_t vrow = vs + (uint32_t)((((lane & 7) + 8 * (j >> 1)) * kWinRow + 16 * warp + 8 * (j & 1)) * 2);
+    const float* pg = sc + (gid < g ? gid : 0) * kWinChunk;
+    for (int t = 0; t < ntiles; ++t) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(vrow + (uint32_t)(16 * t * kWinRow * 2), a0, a1, a2, a3);
+      const float2 p0 = *reinterpret_cast<const float2*>(pg + 16 * t + 2 * tig);
+      const float2 p1 = *reinterpret_cast<const float2*>(pg + 16 * t + 2 * tig + 8);
+      const uint32_t b0 = gid < g ? f2_to_h2_bits(p0.x, p0.y) : 0u;
+      const uint32_t b1 = gid < g ? f2_to_h2_bits(p1.x, p1.y) : 0u;
+      mma16816(d, bf16x2_to_f16x2(a0), bf16x2_to_f16x2(a1), bf16x2_to_f16x2(a2), bf16x2_to_f16x2(a3), b0, b1);
+    }
+    // rows: channels 16 warp + gid (+ 8), columns: heads 2 tig, 2 tig + 1
+    const int c0 = 16 * warp + gid, h0 = 2 * tig;
+    if (h0 < g) {
+      part[(size_t)h0 * kPartFloats + c0] = d[0];
+      part[(size_t)h0 * kPartFloats + c0 + 8] = d[2];
+    }
+    if (h0 + 1 < g) {
+      part[(size_t)(h0 + 1) * kPartFloats + c0] = d[1];
+      part[(size_t)(h0 + 1) * kPartFloats + c0 + 8] = d[3];
+    }
+    if (tid < g) {
+      part[(size_t)tid * kPartFloats + kHeadDim] = stat[2 * tid];
+      part[(size_t)tid * kPartFloats + kHeadDim + 1] = stat[2 * tid + 1];
     }
   }
 }
