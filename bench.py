@@ -2,11 +2,13 @@
 """Benchmark of the OSCAR INT2 KV-cache serving path (write path + fused paged
 decode attention) on synthetic Qwen3-shaped attention layers.
 
-A step is one decode step of one layer for the whole batch: quant_append of
-one new token per request (rotate, clip, quantise and pack the token leaving
-the recent window, ring write) followed by decode_attn (query rotation,
-split-K INT2 + BF16 attention, merge and un-rotation). Inputs are resident in
-device memory before timing starts.
+A step is one decode step of one layer for the whole batch through
+oscar_decode_step: one new token per request appended (ring write; the token
+leaving the recent window rotated, clipped, quantised and packed) and one
+decode query over the cache that then holds it (query rotation, split-K INT2 +
+BF16 attention, merge and un-rotation), the append done by CTAs of the decode
+launch. The same step as two calls (quant_append, then decode_attn) is timed
+beside it. Inputs are resident in device memory before timing starts.
 
 Default workload: Qwen3-8B layer shape (32 query / 8 KV heads, d = 128), batch
 1 at 32768 tokens. Its cache (25.6 MB) fits in L2, so the timed loop cycles
@@ -129,7 +131,7 @@ def max_over_ranks(values, dist, device):
     return [float(x) for x in t.tolist()]
 
 
-KERNEL_SOURCES = {"decode": ("decode_attn.cu", "oscar_internal.cuh"),
+KERNEL_SOURCES = {"decode": ("decode_attn.cu", "oscar_internal.cuh", "token_quant.cuh"),
                   "prefill": ("prefill_append.cu", "oscar_internal.cuh")}
 
 
@@ -283,17 +285,18 @@ class Workload:
         ctx.decode_attn_timed(self.q[j], cache.page_table, cache.state, self.o, self.B, ev_before, ev_after,
                               stream)
 
-    def step(self, i, stream, ev=None):
+    def step(self, i, stream):
+        """One decode step: oscar_decode_step (the append inside the decode launches)."""
         ctx, cache = self.layers[i % len(self.layers)]
         j = i % self.n_inputs
-        if ev is not None:
-            ev[0].record(stream)
+        ctx.decode_step(cache.page_table, cache.state, self.q[j], self.k[j], self.v[j], self.o, self.B, stream)
+
+    def step_two_calls(self, i, stream):
+        """The same step as quant_append followed by decode_attn."""
+        ctx, cache = self.layers[i % len(self.layers)]
+        j = i % self.n_inputs
         ctx.quant_append(cache.page_table, cache.state, self.k[j], self.v[j], self.B, 1, stream)
-        if ev is not None:
-            ev[1].record(stream)
         ctx.decode_attn(self.q[j], cache.page_table, cache.state, self.o, self.B, stream)
-        if ev is not None:
-            ev[2].record(stream)
 
 
 def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True):
@@ -313,62 +316,68 @@ def run_oscar(name, args, device, rank, world, dist, clocks_index, with_e2e=True
         if i > n_total - 5 * args.steps - 2 * args.warmup - 32:
             break
     torch.cuda.synchronize()
-    # two CUDA graphs, captured once and warmed once:
-    #   g_time - K full steps (append + decode): the timed region, the headline value;
+    # three CUDA graphs, captured once and warmed once:
+    #   g_time - K decode steps (oscar_decode_step): the timed region, the headline value;
+    #   g_two  - the same K steps as quant_append + decode_attn, timed after it;
     #   g_dec  - K decode_attn calls over the same layers (decode leaves the cache
-    #            unchanged), timed right after it: the decode call's duration
+    #            unchanged), timed last: the decode call's duration
     cap = torch.cuda.Stream(device)
     cap.wait_stream(stream)
-    g_time = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(g_time, stream=cap):
-            for k in range(args.steps):
-                wl.step(i + k, cap)
-    g_dec = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(cap):
-        with torch.cuda.graph(g_dec, stream=cap):
-            for k in range(args.steps):
-                wl.decode_only(i + k, cap)
-    g_time.replay()
-    g_dec.replay()
+    graphs = []
+    for fn in (wl.step, wl.step_two_calls, wl.decode_only):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for k in range(args.steps):
+                    fn(i + k, cap)
+        graphs.append(g)
+    for g in graphs:
+        g.replay()
     torch.cuda.synchronize()
-    i += args.steps
+    i += 2 * args.steps
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    ev[0].record(stream)
-    g_time.replay()
-    ev[1].record(stream)
-    torch.cuda.synchronize()
-    ev[2].record(stream)
-    g_dec.replay()
-    ev[3].record(stream)
-    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    # NVTX ranges name the replays for profilers (ncu --nvtx --nvtx-include
+    # "timed_steps/"); they are host-side markers outside the events
+    for n, g in enumerate(graphs):
+        torch.cuda.nvtx.range_push(("timed_steps", "two_call_steps", "decode_calls")[n])
+        ev[2 * n].record(stream)
+        g.replay()
+        ev[2 * n + 1].record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clocks = sampler.stop()
     total_ms = ev[0].elapsed_time(ev[1])
-    dec_ms = ev[2].elapsed_time(ev[3]) / args.steps
-    app_ms = max(total_ms / args.steps - dec_ms, 0.0)
+    two_ms = ev[2].elapsed_time(ev[3]) / args.steps
+    dec_ms = ev[4].elapsed_time(ev[5]) / args.steps
+    # the append kernel's share of a two-call step
+    app_ms = max(two_ms - dec_ms, 0.0)
     warm_done = i
-    i += args.steps
+    i += 2 * args.steps
     # the split-K attention kernel alone: eager decode calls, each bracketing that
     # launch with its own event pair (layers cycled as in the timed graphs)
     n_k = min(args.steps, 64)
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_k)]
+    torch.cuda.nvtx.range_push("decode_timed")
     for k in range(n_k):
         wl.decode_timed(i + k, stream, *kev[k])
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     kern_ms = sum(a.elapsed_time(b) for a, b in kev) / n_k
-    total_ms, app_ms, dec_ms, kern_ms = max_over_ranks([total_ms, app_ms, dec_ms, kern_ms], dist, device)
+    total_ms, app_ms, dec_ms, kern_ms, two_ms = max_over_ranks([total_ms, app_ms, dec_ms, kern_ms, two_ms], dist,
+                                                               device)
     us_step = total_ms * 1000.0 / args.steps
     mid = warm_done + args.steps // 2
     dbytes = wl.decode_bytes(mid // len(wl.layers))
     res = {
         "workload": name, "us_per_step": us_step, "decode_us": dec_ms * 1000.0, "kernel_us": kern_ms * 1000.0,
         "kernel_bytes": dbytes - wl.B * wl.spec.num_q_heads * D * 6,
-        "append_us": app_ms * 1000.0, "decode_bytes": dbytes, "append_bytes": wl.append_bytes(),
+        "append_us": app_ms * 1000.0, "two_call_us_per_step": two_ms * 1000.0,
+        "decode_bytes": dbytes, "append_bytes": wl.append_bytes(),
         "layers_cycled": len(wl.layers), "per_layer_bytes": wl.per_layer_bytes, "clocks": clocks,
         "batch": wl.B, "lengths": [int(x) for x in wl.lengths[:4]],
     }
@@ -753,12 +762,13 @@ def main():
             "config": dict(workload_config(args.workload, world),
                            l2="inputs larger than L2: %d independent layer caches cycled" % main_res["layers_cycled"]),
             "decode_us": round(main_res["decode_us"], 3), "append_us": round(main_res["append_us"], 3),
+            "two_call_us_per_step": round(main_res["two_call_us_per_step"], 3),
             "decode_gbs": round(main_res["decode_bytes"] / (main_res["decode_us"] * 1e-6) / 1e9, 1),
-            "append_gbs": round(main_res["append_bytes"] / (main_res["append_us"] * 1e-6) / 1e9, 1),
+            "append_gbs": round(main_res["append_bytes"] / (max(main_res["append_us"], 1e-3) * 1e-6) / 1e9, 1),
             "roofline": roof(main_res),
             "cpu_baseline": cpu,
             "e2e": main_res["e2e"],
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,
             "clocks": main_res["clocks"],
             "extra": [],
         }
@@ -766,10 +776,10 @@ def main():
             es = WORKLOADS[r["workload"]]
             out["extra"].append({
                 "workload": r["workload"], "group": es.group_size, "sink": es.sink, "recent": es.recent,
-                "us_per_step": round(r["us_per_step"], 3),
+                "us_per_step": round(r["us_per_step"], 3), "two_call_us_per_step": round(r["two_call_us_per_step"], 3),
                 "decode_us": round(r["decode_us"], 3), "append_us": round(r["append_us"], 3),
                 "decode_gbs": round(r["decode_bytes"] / (r["decode_us"] * 1e-6) / 1e9, 1),
-                "append_gbs": round(r["append_bytes"] / (r["append_us"] * 1e-6) / 1e9, 1),
+                "append_gbs": round(r["append_bytes"] / (max(r["append_us"], 1e-3) * 1e-6) / 1e9, 1),
                 "roofline": roof(r), "clocks": r["clocks"], "layers_cycled": r["layers_cycled"],
             })
         if pre is not None:

@@ -79,6 +79,7 @@ _SIGS = {
     "oscar_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P]),
     "oscar_decode_attn_timed": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.c_int32, _P, _P, _P]),
     "oscar_decode_attn_shared_prefix": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P]),
+    "oscar_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int32, _P]),
     "oscar_decode_step_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int32, _P]),
     "oscar_calibration_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32, ctypes.c_int32]),
     "oscar_calibration_covariances": (ctypes.c_int, [_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -258,6 +259,13 @@ class Context:
         same pages: the shared range is read once per pack of requests."""
         _check(lib().oscar_decode_attn_shared_prefix(self.handle, _ptr(q), _ptr(page_table), _ptr(state),
                                                      prefix_tokens, _ptr(o), batch, _stream(stream)), self.handle)
+
+    def decode_step(self, page_table, state, q, k, v, o, batch, stream=None):
+        """oscar_decode_step: one new token per request (k, v [batch][Hkv][128])
+        appended and one decode query (q) over the cache that then holds it, in the
+        decode call's launches."""
+        _check(lib().oscar_decode_step(self.handle, _ptr(page_table), _ptr(state), _ptr(q), _ptr(k), _ptr(v),
+                                       _ptr(o), batch, _stream(stream)), self.handle)
 
     def decode_step_host(self, page_table, state, h_qkv, d_qkv, o, h_o, batch, stream=None):
         """oscar_decode_step_host: one new token per request and one decode query,

@@ -10,7 +10,7 @@
 // Three launches on one stream:
 //   1. oscar_rotate_q_kernel   q~ = q R_K * scale * log2(e) per (request, KV head),
 //      written as ready-to-use tensor-core operand fragments (fp16 hi + lo).
-//   2. oscar_decode_kernel<NG, FEW, MERGED> grid (window chunks + prefix splits + splits, Hkv,
+//   2. oscar_decode_kernel<NG, FEW, MERGED, STEP> grid (window chunks + prefix splits + splits, Hkv,
 //      B), NG = 128 / group size: the first CTAs attend over the BF16 sink +
 //      recent ring in the raw basis (64 or 160 tokens each, per call); the
 //      others stream a slice of the INT2 pages, computing scores and the P.V
@@ -37,6 +37,7 @@
 #include <type_traits>
 
 #include "oscar_internal.cuh"
+#include "token_quant.cuh"
 
 namespace oscar {
 
@@ -310,6 +311,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
 // every tile, V^T as the row operand (fp16 after a conversion that is exact for
 // values of magnitude 2^-14 .. 65504) and the fp16 probabilities as the column
 // operand, as in the INT2 value product.
+template <bool STEP>
 __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk, uint8_t* smem) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -319,12 +321,22 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
   __nv_bfloat16* qb = vrows + kWinChunk * kWinRow;                            // [8][kWinRow]
   float* sc = reinterpret_cast<float*>(qb + kMaxGqa * kWinRow);               // [8][chunk]
   float* stat = sc + kMaxGqa * kWinChunk;                                     // [8][2]
-  const int nslots = p.win_slots + p.prefix_splits + p.splits;
+  const int nslots = total_slots(p);
   float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots + chunk) * g * kPartFloats;
 
   const oscar_seq_state st = p.state[b];
   const bool ok = state_ok(st, S, W, p.max_batch);
-  const int L = st.seq_len, E = st.int2_end;
+  int L = st.seq_len, E = st.int2_end;
+  // a decode step attends over the window as its append leaves it: position L
+  // added (read from the caller's k / v, since the append CTA writes the window
+  // concurrently), the entry it evicts (or, without a ring, the token itself)
+  // left to the append CTA's INT2 slot
+  int newpos = -1;
+  if (STEP && ok) {
+    newpos = L;
+    E = max(E, max(L + 1 - W, S));
+    L = L + 1;
+  }
   const int ns = ok ? min(S, L) : 0;
   const int rb = max(E, S);
   const int nr = ok && L > rb ? L - rb : 0;
@@ -335,15 +347,18 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
   const size_t wrow = ok ? (size_t)st.window_row : 0;
   const __nv_bfloat16* wk = p.window + ((wrow * p.num_kv_heads + h) * 2 + 0) * slots * kHeadDim;
   const __nv_bfloat16* wv = p.window + ((wrow * p.num_kv_heads + h) * 2 + 1) * slots * kHeadDim;
+  const size_t in_off = ((size_t)b * p.num_kv_heads + h) * kHeadDim;
 
   for (int idx = tid; idx < ntiles * 16 * 16; idx += kThreads) {
     const int r = idx >> 4, u = idx & 15, t = t0 + r;
     const bool in = r < n;
-    const int slot = !in ? 0 : (t < ns ? t : S + (rb + t - ns) % W);
-    cp_async16_s((uint32_t)__cvta_generic_to_shared(krows + r * kWinRow + 8 * u), wk + (size_t)slot * kHeadDim + 8 * u,
-                 in ? 16u : 0u);
-    cp_async16_s((uint32_t)__cvta_generic_to_shared(vrows + r * kWinRow + 8 * u), wv + (size_t)slot * kHeadDim + 8 * u,
-                 in ? 16u : 0u);
+    const int pos = t < ns ? t : rb + t - ns;
+    const int slot = !in ? 0 : (t < ns ? t : S + pos % W);
+    const bool fresh = STEP && in && pos == newpos;
+    const __nv_bfloat16* ksrc = fresh ? p.step_k + in_off : wk + (size_t)slot * kHeadDim;
+    const __nv_bfloat16* vsrc = fresh ? p.step_v + in_off : wv + (size_t)slot * kHeadDim;
+    cp_async16_s((uint32_t)__cvta_generic_to_shared(krows + r * kWinRow + 8 * u), ksrc + 8 * u, in ? 16u : 0u);
+    cp_async16_s((uint32_t)__cvta_generic_to_shared(vrows + r * kWinRow + 8 * u), vsrc + 8 * u, in ? 16u : 0u);
   }
   cp_commit();
   // the raw query heads of this KV head (element loads: q needs no alignment
@@ -933,7 +948,7 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
     }
   }
   __syncthreads();
-  const int nslots = p.win_slots + p.prefix_splits + p.splits;
+  const int nslots = total_slots(p);
   for (int i = tid; i < ncols * kHeadDim; i += kThreads) {
     const int n = i / kHeadDim, c = i % kHeadDim;  // column n: head n % g of request r0 + n / g
     const int cr = PACK ? n / g : 0;
@@ -950,16 +965,215 @@ __device__ void int2_attention(const DecodeParams& p, int h, int split, int nspl
   }
 }
 
+// --------------------------------------------------------------------------
+// 2c. A decode step's append (oscar_decode_step): the last CTA of every
+//     (request, KV head) appends the request's new token. With L, E the state
+//     before the step and E' = max(E, L + 1 - recent, sink), position L goes to
+//     the sink (L < sink) or to the recent ring, whose slot first hands the
+//     entry it held, position L - recent, to INT2 when that lies in [E, E');
+//     without a ring (recent = 0) position L itself goes to INT2. That position
+//     is rotated, clipped, quantised and packed with the append kernel's
+//     arithmetic, and this CTA attends over it: its partial (the score of the
+//     dequantised key in log2 units, weight 1, the dequantised value) takes the
+//     call's last slot, in the R_V basis like the splits' partials.
+//     Sources: "Juntos, AI Open-Sources OSCAR ..." (7minutos.es), section "El
+//     sistema de servicio" (BF16 sink and recent ring, INT2 for the rest; the
+//     write path's rotate, clip and group quantisation).
+// --------------------------------------------------------------------------
+constexpr int kStepSmem =
+    (kHeadDim * kHeadDim + 2 * kMaxGqa * kHeadDim + 8 * kHeadDim + 16) * 4 + 2 * kHeadDim + 2 * kGroups * 2 * 2;
+
+__device__ __forceinline__ float warp_minf(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ void step_append(const DecodeParams& p, int h, int b, uint8_t* smem) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = p.gqa, S = p.sink, W = p.recent, Hkv = p.num_kv_heads;
+  // thread (kind, c): kind 0 = K, 1 = V (or, in the rotations, the half of the rows)
+  const int kind = tid >> 7, c = tid & (kHeadDim - 1);
+  float* Rs = reinterpret_cast<float*>(smem);                // [128][128]: R_K[h], later R_V[h]
+  float* qf = Rs + kHeadDim * kHeadDim;                       // [8][128]: the raw query heads
+  float* qt = qf + kMaxGqa * kHeadDim;                        // [8][128]: q~ in log2 units
+  float* xs = qt + kMaxGqa * kHeadDim;                        // [2][128]: K, V of the position going to INT2
+  float* red = xs + 2 * kHeadDim;                             // [2 kinds][2 halves][128]
+  float* deq = red + 4 * kHeadDim;                            // [2][128]: its dequantised K, V (R basis)
+  float* wmm = deq + 2 * kHeadDim;                            // [2 kinds][4 warps][2]: min, max
+  uint8_t(*codes)[kHeadDim] = reinterpret_cast<uint8_t(*)[kHeadDim]>(wmm + 16);
+  __half(*meta)[kGroups][2] = reinterpret_cast<__half(*)[kGroups][2]>(codes + 2);
+  const size_t rmat = (size_t)h * kHeadDim * kHeadDim;
+
+  // constant data and the caller's q before the wait: R_K staged, R_V into the
+  // level-2 cache, q~ = q R_K * scale * log2(e) (thread (half, c) sums 64 rows)
+  stage_matrix(Rs, p.R_K + rmat, tid, kThreads);
+  if (tid == 0 && !p.fold_rv)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p.R_V + rmat), "r"(kHeadDim * kHeadDim * 4)
+                 : "memory");
+  for (int i = tid; i < kMaxGqa * kHeadDim; i += kThreads)
+    qf[i] = (i >> 7) < g ? __bfloat162float(p.q[((size_t)b * p.num_q_heads + h * g) * kHeadDim + i]) : 0.f;
+  cp_wait<0>();
+  __syncthreads();
+  {
+    const int i0 = 64 * kind;
+    float acc[kMaxGqa];
+#pragma unroll
+    for (int m = 0; m < kMaxGqa; ++m) acc[m] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < 64; ++i) {
+      const float r = Rs[(i0 + i) * kHeadDim + c];
+#pragma unroll
+      for (int m = 0; m < kMaxGqa; ++m)
+        if (m < g) acc[m] = fmaf(qf[m * kHeadDim + i0 + i], r, acc[m]);
+    }
+    if (kind == 1) {
+#pragma unroll
+      for (int m = 0; m < kMaxGqa; ++m)
+        if (m < g) qt[m * kHeadDim + c] = acc[m];
+    }
+    __syncthreads();
+    if (kind == 0) {
+#pragma unroll
+      for (int m = 0; m < kMaxGqa; ++m)
+        if (m < g) qt[m * kHeadDim + c] = (acc[m] + qt[m * kHeadDim + c]) * p.scale_log2;
+    }
+  }
+
+  pdl_wait();  // the state, the window and the pages come from earlier kernels
+  pdl_trigger();
+  const oscar_seq_state st = p.state[b];
+  const bool ok = state_ok(st, S, W, p.max_batch);
+  if (!ok && tid == 0) atomicOr(p.err_flags, OSCAR_FLAG_BAD_STATE);
+  const int L = st.seq_len, E = st.int2_end;
+  const int E2 = max(E, max(L + 1 - W, S));
+  // the window slot of position L (-1: none) and the position going to INT2
+  // (-1: none), taken from the ring or from the caller's k / v
+  int wslot = -1, qpos = -1;
+  bool from_ring = false;
+  if (ok) {
+    if (L < S) {
+      wslot = L;
+    } else if (L < E2) {
+      qpos = L;
+    } else {
+      const int pe = L - W;
+      if (pe >= E && pe < E2 && pe >= S) {
+        qpos = pe;
+        from_ring = true;
+      }
+      wslot = S + L % W;
+    }
+  }
+  const size_t slots = (size_t)(S + W);
+  const size_t wrow = ok ? (size_t)st.window_row : 0;
+  __nv_bfloat16* win = p.step_window + ((wrow * Hkv + h) * 2 + kind) * slots * kHeadDim;
+  const __nv_bfloat16* in = (kind ? p.step_v : p.step_k) + ((size_t)b * Hkv + h) * kHeadDim;
+  int page = -1;
+  if (qpos >= 0) {
+    xs[kind * kHeadDim + c] = __bfloat162float(from_ring ? win[(size_t)(S + qpos % W) * kHeadDim + c] : in[c]);
+    const int pidx = qpos / kPage;
+    page = pidx < p.pt_stride ? p.page_table[(size_t)b * p.pt_stride + pidx] : -1;
+  }
+  __syncthreads();  // the entry the new token evicts is read before the window write
+  if (wslot >= 0) win[(size_t)wslot * kHeadDim + c] = in[c];
+
+  const int nslot = total_slots(p);
+  float* part = p.part + (((size_t)b * Hkv + h) * nslot + nslot - 1) * g * kPartFloats;
+  if (qpos < 0) {
+    // nothing goes to INT2 in this step: an empty partial
+    for (int i = tid; i < g * kPartFloats; i += kThreads) part[i] = i % kPartFloats == kHeadDim ? -INFINITY : 0.f;
+    return;
+  }
+  // the rotation x R as in the append kernel: thread (half, c) sums 64 terms in
+  // order and the halves are added afterwards; K with R_K, then V with R_V
+  {
+    const int i0 = 64 * kind;
+    float acc = 0.f;
+#pragma unroll 16
+    for (int i = 0; i < 64; ++i) acc = fmaf(xs[i0 + i], Rs[(i0 + i) * kHeadDim + c], acc);
+    red[kind * kHeadDim + c] = acc;
+    float accv = 0.f;
+    if (p.fold_rv) {
+      accv = kind ? 0.f : xs[kHeadDim + c];  // identity: V is already in the R_V basis
+    } else {
+      __syncthreads();  // R_K is no longer read
+      stage_matrix(Rs, p.R_V + rmat, tid, kThreads);
+      cp_wait<0>();
+      __syncthreads();
+#pragma unroll 16
+      for (int i = 0; i < 64; ++i) accv = fmaf(xs[kHeadDim + i0 + i], Rs[(i0 + i) * kHeadDim + c], accv);
+    }
+    red[(2 + kind) * kHeadDim + c] = accv;
+  }
+  __syncthreads();
+  // thread (kind, c): clip, group minimum and maximum (a group of 32 channels is
+  // one warp, one of 64 two warps), scale, zero and code
+  const float x_rot = red[(2 * kind) * kHeadDim + c] + red[(2 * kind + 1) * kHeadDim + c];
+  const float clip = (kind ? p.clip_V : p.clip_K)[h];
+  const float x = fminf(fmaxf(x_rot, -clip), clip);
+  float mn = warp_minf(x), mx = warp_maxf(x);
+  if (p.ngroups != kGroups) {
+    if (lane == 0) {
+      wmm[(kind * 4 + (c >> 5)) * 2] = mn;
+      wmm[(kind * 4 + (c >> 5)) * 2 + 1] = mx;
+    }
+    __syncthreads();
+    const int w = (c >> 5) ^ 1;  // the other warp of a 64-channel group
+    mn = fminf(mn, wmm[(kind * 4 + w) * 2]);
+    mx = fmaxf(mx, wmm[(kind * 4 + w) * 2 + 1]);
+  }
+  __half s16, z16;
+  group_scale_zero(mn, mx, s16, z16);
+  const float sf = __half2float(s16), zf = __half2float(z16);
+  const int code = group_code(x, sf, zf);
+  codes[kind][c] = (uint8_t)code;
+  const int gsz = kHeadDim / p.ngroups;
+  if ((c & (gsz - 1)) == 0) {
+    meta[kind][c / gsz][0] = s16;
+    meta[kind][c / gsz][1] = z16;
+  }
+  deq[kind * kHeadDim + c] = fmaf(sf, (float)code, zf);
+  __syncthreads();
+  if (tid < 72) {
+    if (page >= 0 && page < p.num_pages)
+      store_token_block(p.step_pool + ((size_t)page * Hkv + h) * block_bytes(p.ngroups), qpos % kPage, tid,
+                        p.ngroups, codes, meta);
+    else if (tid == 0)
+      atomicOr(p.err_flags, OSCAR_FLAG_BAD_PAGE_ID);
+  }
+  // the partial of that position (warp m: query head m)
+  for (int m = warp; m < g; m += kWarps) {
+    float sc = 0.f;
+    for (int cc = lane; cc < kHeadDim; cc += 32) sc = fmaf(qt[m * kHeadDim + cc], deq[cc], sc);
+    sc = warp_sum(sc);
+    float* row = part + (size_t)m * kPartFloats;
+    for (int cc = lane; cc < kHeadDim; cc += 32) row[cc] = deq[kHeadDim + cc];
+    if (lane == 0) {
+      row[kHeadDim] = sc;
+      row[kHeadDim + 1] = 1.f;
+    }
+  }
+}
+
 // FEW: no split holds more than 64 pages per warp (kFewPages per CTA), so the
 // INT2 CTAs keep all their page ids in registers; the host picks the instance
 // from the page-table width and the split counts (few_pages_call)
 constexpr int kFewPages = 64 * kWarps;
-template <int NG, bool FEW, bool MERGED>
+// STEP: the instance a decode step launches (the step's append CTAs; see 2c),
+// separate so that plain decodes run code without them
+template <int NG, bool FEW, bool MERGED, bool STEP>
 __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint4 qs[8 * 32];
   __shared__ int2 wb[kWarps];
   const int x = blockIdx.x, h = blockIdx.y, z = blockIdx.z;
+  if constexpr (STEP) {
+    if (x == total_slots(p) - 1) {
+      step_append(p, h, z, smem);
+      return;
+    }
+  }
   // R_V^T[h] (constant) into the level-2 cache for the merge, whose CTAs only
   // become resident as these retire: one bulk prefetch per KV head
   if (x == 0 && z == 0 && threadIdx.x == 0 && !p.fold_rv) {
@@ -970,7 +1184,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
   pdl_trigger();
   const int S = p.sink, W = p.recent, P = p.prefix_tokens;
   if (x < p.win_slots) {
-    window_attention(p, z, h, x, smem);
+    window_attention<STEP>(p, z, h, x, smem);
   } else if (x < p.win_slots + p.prefix_splits) {
     // the shared prefix [S, P) once for requests z pack .. z pack + pack - 1; every
     // one of them must hold [S, P) in INT2
@@ -1003,7 +1217,7 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
 //    waits for the level-2 cache once.
 // --------------------------------------------------------------------------
 constexpr int kMergeThreads = 256;
-constexpr int kMaxSlots = 256 + kMaxWindow / kWindowChunkSmall;   // INT2 splits + window chunks
+constexpr int kMaxSlots = 256 + kMaxWindow / kWindowChunkSmall + 1;   // INT2 splits + window chunks + a step's slot
 constexpr int kMergeChunk = 64;                            // slots staged per round
 // floats of the staged rows (also the un-rotation partials, 4 x 128 floats)
 __host__ __device__ constexpr int merge_rows_floats(int nslots) {
@@ -1016,9 +1230,24 @@ __host__ __device__ constexpr int merge_smem_bytes(int nslots) {
 }
 constexpr int kMergeSmem = merge_smem_bytes(kMergeChunk);
 
+// the state after a decode step's append, written by one merge CTA per request
+// once every CTA of the decode kernel (which all read the state from before
+// the step) has completed: {L + 1, max(E, L + 1 - recent, sink)}
+__device__ __forceinline__ void publish_step_state(const DecodeParams& p, int b) {
+  oscar_seq_state st = p.step_state[b];
+  if (!state_ok(st, p.sink, p.recent, p.max_batch)) return;
+  const int64_t nl = (int64_t)st.seq_len + 1;
+  int64_t ne = nl - p.recent;
+  if (ne < st.int2_end) ne = st.int2_end;
+  if (ne < p.sink) ne = p.sink;
+  st.seq_len = (int32_t)nl;
+  st.int2_end = (int32_t)ne;
+  p.step_state[b] = st;
+}
+
 __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
-  const int g = p.gqa, nslots = p.win_slots + p.prefix_splits + p.splits, nwin = p.win_slots;
+  const int g = p.gqa, nslots = total_slots(p), nwin = p.win_slots;
   const int chunk = nslots < kMergeChunk ? nslots : kMergeChunk;
   float* RT = reinterpret_cast<float*>(dsm);                   // R_V^T[h], [128][128]
   float* rows = RT + kHeadDim * kHeadDim;                       // [chunk slots][2 heads][kPartFloats]
@@ -1030,6 +1259,7 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
   pdl_wait();  // the partials come from the decode kernel
   pdl_trigger();
+  if (p.step_slots && h == 0 && blockIdx.z == 0 && tid == 0) publish_step_state(p, b);
   // warp hh < nh keeps the running maximum and row sum of head hh and writes the
   // round's slot weights; thread (head hh, channel c) keeps the weighted sums of
   // the window and INT2 partials, relative to the running maximum
@@ -1144,7 +1374,7 @@ constexpr int kMergeColsSmem =
 
 __global__ void __launch_bounds__(kMergeColsThreads) oscar_merge_cols_kernel(DecodeParams p) {
   extern __shared__ __align__(16) uint8_t dsm[];
-  const int g = p.gqa, nslots = p.win_slots + p.prefix_splits + p.splits, nwin = p.win_slots;
+  const int g = p.gqa, nslots = total_slots(p), nwin = p.win_slots;
   float* RTc = reinterpret_cast<float*>(dsm);                  // [128 rows][32 columns] of R_V^T
   float* rows = RTc + kHeadDim * kMergeCols;                    // [nslots][kPartFloats]
   float* wts = rows + kMergeChunk * kPartFloats;                // [nslots]
@@ -1167,6 +1397,7 @@ __global__ void __launch_bounds__(kMergeColsThreads) oscar_merge_cols_kernel(Dec
   const float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots * g + m) * kPartFloats;
   pdl_wait();  // the partials come from the decode kernel
   pdl_trigger();
+  if (p.step_slots && h == 0 && blockIdx.z == 0 && tid == 0) publish_step_state(p, b);
   constexpr int kChunks16 = kPartFloats / 4;
   for (int i = tid; i < nslots * kChunks16; i += kMergeColsThreads) {
     const int sl = i / kChunks16, u = i % kChunks16;
@@ -1235,7 +1466,22 @@ int decode_smem_bytes() {
   int m = kStageBytes;
   if (window > m) m = window;
   if (merge > m) m = merge;
+  if (kStepSmem > m) m = kStepSmem;
   return m;
+}
+
+// the decode kernel instance for ng groups per token (4 or 2), splits of at
+// most kFewPages pages (few), merged hi / lo score columns (query groups of 1,
+// 2 or 4 heads; only with few) and a decode step's append CTAs (step)
+static void (*decode_instance(int ng, bool few, bool merged, bool step))(DecodeParams) {
+  if (ng == kGroups) {
+    if (!few) return step ? oscar_decode_kernel<kGroups, false, false, true> : oscar_decode_kernel<kGroups, false, false, false>;
+    if (merged) return step ? oscar_decode_kernel<kGroups, true, true, true> : oscar_decode_kernel<kGroups, true, true, false>;
+    return step ? oscar_decode_kernel<kGroups, true, false, true> : oscar_decode_kernel<kGroups, true, false, false>;
+  }
+  if (!few) return step ? oscar_decode_kernel<2, false, false, true> : oscar_decode_kernel<2, false, false, false>;
+  if (merged) return step ? oscar_decode_kernel<2, true, true, true> : oscar_decode_kernel<2, true, true, false>;
+  return step ? oscar_decode_kernel<2, true, false, true> : oscar_decode_kernel<2, true, false, false>;
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cudaEvent_t ev_before,
@@ -1244,9 +1490,12 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
   const int smem = decode_smem_bytes();
   cudaError_t ea = once_for_current_device(attrs, [&] {
     void (*const kernels[])(DecodeParams) = {
-        oscar_decode_kernel<kGroups, true, false>, oscar_decode_kernel<kGroups, false, false>,
-        oscar_decode_kernel<2, true, false>,       oscar_decode_kernel<2, false, false>,
-        oscar_decode_kernel<kGroups, true, true>,  oscar_decode_kernel<2, true, true>};
+        decode_instance(kGroups, true, false, false), decode_instance(kGroups, false, false, false),
+        decode_instance(2, true, false, false),       decode_instance(2, false, false, false),
+        decode_instance(kGroups, true, true, false),  decode_instance(2, true, true, false),
+        decode_instance(kGroups, true, false, true),  decode_instance(kGroups, false, false, true),
+        decode_instance(2, true, false, true),        decode_instance(2, false, false, true),
+        decode_instance(kGroups, true, true, true),   decode_instance(2, true, true, true)};
     cudaError_t e = cudaSuccess;
     for (auto k : kernels)
       if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1259,7 +1508,7 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
     return e;
   });
   if (ea != cudaSuccess) return ea;
-  if (p.win_slots + p.prefix_splits + p.splits > kMaxSlots) return cudaErrorInvalidValue;
+  if (total_slots(p) > kMaxSlots) return cudaErrorInvalidValue;
   if (p.win_chunk < 1 || p.win_chunk > kWinChunk) return cudaErrorInvalidValue;
   // every split of the call streams at most kFewPages pages: a request's INT2
   // pages fit its page-table row, the shared prefix its own page count
@@ -1272,16 +1521,12 @@ cudaError_t launch_decode(const DecodeParams& p, int batch, cudaStream_t s, cuda
                              s, p);
   if (e == cudaSuccess && ev_before) e = cudaEventRecord(ev_before, s);
   if (e == cudaSuccess)
-    e = launch_pdl(p.ngroups == kGroups
-                       ? (few ? (merged ? oscar_decode_kernel<kGroups, true, true> : oscar_decode_kernel<kGroups, true, false>)
-                              : oscar_decode_kernel<kGroups, false, false>)
-                       : (few ? (merged ? oscar_decode_kernel<2, true, true> : oscar_decode_kernel<2, true, false>)
-                              : oscar_decode_kernel<2, false, false>),
-                   dim3(p.win_slots + p.prefix_splits + p.splits, p.num_kv_heads, batch), dim3(kThreads),
+    e = launch_pdl(decode_instance(p.ngroups, few, merged, p.step_slots != 0),
+                   dim3(total_slots(p), p.num_kv_heads, batch), dim3(kThreads),
                    smem, s, p);
   if (e == cudaSuccess && ev_after) e = cudaEventRecord(ev_after, s);
   // few (request, KV head) pairs: the merge by columns (8 times the CTAs)
-  const int nslots = p.win_slots + p.prefix_splits + p.splits;
+  const int nslots = total_slots(p);
   const bool by_cols = nslots <= kMergeChunk && (int64_t)batch * p.num_kv_heads * ((p.gqa + 1) / 2) <= kMergeColsMaxCtas;
   if (e == cudaSuccess) {
     if (by_cols)

@@ -106,13 +106,15 @@ int win_chunk_for(const oscar_ctx* ctx, int batch) {
   return window_chunk(ctx->cfg.sink + ctx->cfg.recent, (int64_t)batch * ctx->cfg.num_kv_heads, ctx->num_sms);
 }
 
-int auto_splits(const oscar_ctx* ctx, int batch) {
+// extra: CTAs per (request, KV head) besides the window and the splits (a
+// decode step's append CTA)
+int auto_splits(const oscar_ctx* ctx, int batch, int extra = 0) {
   if (ctx->cfg.num_splits > 0) return ctx->cfg.num_splits;
   const int64_t units = (int64_t)batch * ctx->cfg.num_kv_heads;
   const int64_t pages = ctx->cfg.max_pages_per_seq;
   // fill one wave of decode CTAs together with the BF16-window CTAs; at most
   // kSplitPages pages per CTA
-  const int64_t wins = units * window_slots(ctx->cfg.sink + ctx->cfg.recent, win_chunk_for(ctx, batch));
+  const int64_t wins = units * (window_slots(ctx->cfg.sink + ctx->cfg.recent, win_chunk_for(ctx, batch)) + extra);
   int64_t by_wave = (kDecodeCtasPerSm * (int64_t)ctx->num_sms - wins) / units;
   int64_t by_pages = (pages + kSplitPages - 1) / kSplitPages;
   int64_t s = by_wave > by_pages ? by_wave : by_pages;
@@ -441,9 +443,11 @@ static void shared_prefix_splits(const oscar_ctx* ctx, int batch, int prefix_tok
   *splits = (int)ss;
 }
 
+// step_k / step_v non-null: a decode step (oscar_decode_step), the one-token
+// append of every request done inside the call
 static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table, const oscar_seq_state* state,
                        float* o, int32_t batch, void* stream, cudaEvent_t ev_before, cudaEvent_t ev_after,
-                       int32_t prefix_tokens = 0) {
+                       int32_t prefix_tokens = 0, const void* step_k = nullptr, const void* step_v = nullptr) {
   if (!ctx) return OSCAR_ERR_INVALID_ARG;
   if (!ctx->loaded) return fail(ctx, OSCAR_ERR_NOT_LOADED, "decode_attn: rotations not loaded");
   if (!ctx->pool) return fail(ctx, OSCAR_ERR_NOT_BOUND, "decode_attn: no cache bound");
@@ -473,7 +477,8 @@ static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table,
   p.sink = ctx->cfg.sink;
   p.ngroups = kHeadDim / ctx->cfg.group_size;
   p.recent = ctx->cfg.recent;
-  p.splits = auto_splits(ctx, batch);
+  const bool step = step_k != nullptr;
+  p.splits = auto_splits(ctx, batch, step ? 1 : 0);
   p.win_chunk = win_chunk_for(ctx, batch);
   p.win_slots = window_slots(ctx->cfg.sink + ctx->cfg.recent, p.win_chunk);
   p.batch = batch;
@@ -488,6 +493,17 @@ static int decode_impl(oscar_ctx* ctx, const void* q, const int32_t* page_table,
   p.max_batch = ctx->cfg.max_batch;
   p.scale_log2 = ctx->cfg.softmax_scale * 1.4426950408889634f;
   p.err_flags = ctx->flags;
+  if (step) {
+    p.step_slots = 1;
+    p.step_k = static_cast<const __nv_bfloat16*>(step_k);
+    p.step_v = static_cast<const __nv_bfloat16*>(step_v);
+    p.step_state = const_cast<oscar_seq_state*>(state);   // the caller's writable state (oscar_decode_step)
+    p.step_pool = ctx->pool;
+    p.step_window = ctx->window;
+    p.R_V = ctx->R_V;
+    p.clip_K = ctx->clip_K;
+    p.clip_V = ctx->clip_V;
+  }
   cudaError_t e = launch_decode(p, batch, static_cast<cudaStream_t>(stream), ev_before, ev_after);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "decode_attn launch");
   return OSCAR_OK;
@@ -509,6 +525,24 @@ int oscar_decode_attn_timed(oscar_ctx* ctx, const void* q, const int32_t* page_t
                             void* ev_before, void* ev_after) {
   return decode_impl(ctx, q, page_table, state, o, batch, stream, static_cast<cudaEvent_t>(ev_before),
                      static_cast<cudaEvent_t>(ev_after));
+}
+
+// one decode step on device buffers: the append and the attention in the same
+// launches when k and v allow 16-byte copies, else the append kernel first
+static int step_impl(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state, const void* q,
+                     const void* k, const void* v, float* o, int32_t batch, void* stream) {
+  if (!ctx) return OSCAR_ERR_INVALID_ARG;
+  if (!k || !v) return fail(ctx, OSCAR_ERR_INVALID_ARG, "decode_step: null pointer");
+  if (((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15) == 0)
+    return decode_impl(ctx, q, page_table, state, o, batch, stream, nullptr, nullptr, 0, k, v);
+  const int st = append_impl(ctx, page_table, state, k, v, batch, 1, nullptr, 0, stream);
+  if (st != OSCAR_OK) return st;
+  return decode_impl(ctx, q, page_table, state, o, batch, stream, nullptr, nullptr);
+}
+
+int oscar_decode_step(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state, const void* q,
+                      const void* k, const void* v, float* o, int32_t batch, void* stream) {
+  return step_impl(ctx, page_table, state, q, k, v, o, batch, stream);
 }
 
 int oscar_decode_step_host(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state,
@@ -537,9 +571,7 @@ int oscar_decode_step_host(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_
     if (e != cudaSuccess) return cuda_fail(ctx, e, "decode_step_host: input copy");
     in = static_cast<const uint8_t*>(d_qkv);
   }
-  int st = append_impl(ctx, page_table, state, in + qbytes, in + qbytes + kbytes, batch, 1, nullptr, 0, stream);
-  if (st != OSCAR_OK) return st;
-  st = decode_impl(ctx, in, page_table, state, out ? out : o, batch, stream, nullptr, nullptr);
+  const int st = step_impl(ctx, page_table, state, in, in + qbytes, in + qbytes + kbytes, out ? out : o, batch, stream);
   if (st != OSCAR_OK) return st;
   if (!out) {
     e = cudaMemcpyAsync(h_o, o, (size_t)batch * ctx->cfg.num_q_heads * kHeadDim * sizeof(float),

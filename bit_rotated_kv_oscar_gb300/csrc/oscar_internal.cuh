@@ -140,7 +140,28 @@ struct DecodeParams {
   int32_t prefix_tokens, prefix_splits, pack;
   float scale_log2;         // softmax_scale * log2(e)
   uint32_t* err_flags;
+  // A decode step (oscar_decode_step): one new token per request is appended by
+  // the call itself. step_slots = 1 adds, after the splits, the slot of the
+  // position the step quantises (written by one more CTA per request and KV
+  // head, which also writes the new token into the window); every other CTA
+  // works from the state before the step, and the merge publishes the new one.
+  // step_slots = 0 (a plain decode): the fields below are unused.
+  int32_t step_slots;
+  const __nv_bfloat16* step_k;   // [B][Hkv][128], 16-byte aligned
+  const __nv_bfloat16* step_v;
+  oscar_seq_state* step_state;   // = state, written by the merge
+  uint8_t* step_pool;            // = pool, writable
+  __nv_bfloat16* step_window;    // = window, writable
+  const float* R_V;              // [Hkv][128][128]
+  const float* clip_K;           // [Hkv]
+  const float* clip_V;
 };
+
+// partial slots of a decode call per (request, KV head): window chunks, shared
+// prefix splits, splits, and the slot of a step's newly quantised position
+__host__ __device__ __forceinline__ int total_slots(const DecodeParams& p) {
+  return p.win_slots + p.prefix_splits + p.splits + p.step_slots;
+}
 
 // Programmatic dependent launch: kernels launched with launch_pdl may start
 // while the previous kernel on the stream is still running. Before its
@@ -154,6 +175,9 @@ struct DecodeParams {
 // completed, wherever those kernels placed their pdl_trigger. The append lets
 // its dependents start at once, so that the query rotation stages R_K and
 // computes q~ beside it.
+// A decode step's append CTA reads only R_K, R_V (level-2 prefetch) and the
+// caller's q, k and v before its wait; its writes (window, page, partial) and the
+// merge's state publication come after the waits.
 // One exception to "constant data": the no-alloc decode keeps R_V^T and the
 // probability scales in its shared scratch array and rewrites them at every
 // call with an ordinary (non-overlapping) preparation launch, while the merge

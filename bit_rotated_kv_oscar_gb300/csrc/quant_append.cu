@@ -10,6 +10,7 @@
 // "OSCAR: Offline Spectral Covariance-Aware Rotation ..." (gist.science, it),
 // Riepilogo Tecnico 2.2 B (mixed-precision paged layout).
 #include "oscar_internal.cuh"
+#include "token_quant.cuh"
 
 namespace oscar {
 
@@ -287,16 +288,9 @@ oscar_quant_append_kernel(AppendParams p) {
           }
         }
         if (qthread) {
-          const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
-          const __half z16 = __float2half_rn(mn);
-          const float sf = __half2float(s16), zf = __half2float(z16);
-          int code = 0;
-          if (sf != 0.f) {
-            float u = rintf(__fmul_rn(__fsub_rn(x, zf), __frcp_rn(sf)));
-            u = fminf(fmaxf(u, 0.f), 3.f);
-            code = (int)u;
-          }
-          codes[kind][c] = (uint8_t)code;
+          __half s16, z16;
+          group_scale_zero(mn, mx, s16, z16);
+          codes[kind][c] = (uint8_t)group_code(x, __half2float(s16), __half2float(z16));
           const int gsz = kHeadDim / p.ngroups;
           if ((c & (gsz - 1)) == 0) {
             meta[kind][c / gsz][0] = s16;
@@ -305,43 +299,7 @@ oscar_quant_append_kernel(AppendParams p) {
         }
         __syncthreads();
         uint8_t* blk = tid < 72 ? block_of(p, s_page, h) : nullptr;
-        if (blk) {
-          const int t = (int)(qpos % kPage);
-          if (tid < 8) {
-            // K: 8 words of this token
-            const int bb = tid >> 1, x = tid & 1;
-            uint32_t w = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int ch = 16 * i + 2 * bb + 8 * x;
-              w |= (uint32_t)codes[0][ch] << (2 * i);
-              w |= (uint32_t)codes[0][ch + 1] << (16 + 2 * i);
-            }
-            const int a = t & 7, th = t >> 3;
-            *reinterpret_cast<uint32_t*>(blk + 16 * (4 * a + bb) + 4 * (2 * th + x)) = w;
-          } else if (tid >= 32 && tid < 48) {
-            // V: 16 half-words of this token
-            const int u = tid - 32, a = u >> 1, x = u & 1;
-            uint32_t hw = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hw |= (uint32_t)codes[1][16 * i + a + 8 * x] << (2 * i);
-            const int tt = t >> 3, bb = (t & 7) >> 1, hi = t & 1;
-            *reinterpret_cast<uint16_t*>(blk + 512 + 16 * (4 * a + bb) + 4 * (2 * tt + x) + 2 * hi) =
-                (uint16_t)hw;
-          } else if (tid >= 64 && tid < 72) {
-            // scale / zero of each group, K and V
-            const int u = tid - 64, kind2 = u >> 2, gq = u & 3, ng = p.ngroups;
-            if (gq < ng) {
-              if (kind2 == 0) {
-                *reinterpret_cast<__half*>(blk + kscale_off(ng, t, gq)) = meta[0][gq][0];
-                *reinterpret_cast<__half*>(blk + kzero_off(ng, t, gq)) = meta[0][gq][1];
-              } else {
-                *reinterpret_cast<__half*>(blk + vscale_off(ng, t, gq)) = meta[1][gq][0];
-                *reinterpret_cast<__half*>(blk + vzero_off(ng, t, gq)) = meta[1][gq][1];
-              }
-            }
-          }
-        }
+        if (blk) store_token_block(blk, (int)(qpos % kPage), tid, p.ngroups, codes, meta);
         __syncthreads();  // codes / meta / xs reused by the next token
       }
     }

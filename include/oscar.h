@@ -226,6 +226,25 @@ int oscar_decode_attn_shared_prefix(oscar_ctx* ctx, const void* q, const int32_t
                                     const oscar_seq_state* state, int32_t prefix_tokens, float* o,
                                     int32_t batch, void* stream);
 
+/* One serving step on device buffers: every request gets one new token,
+ * written to the cache, and one decode query over the cache that then holds it
+ * ([ES] "El sistema de servicio": the new K / V enter the BF16 sink or ring,
+ * the ring entry they replace is quantised to INT2, and the step attends over
+ * sink, ring and INT2 history). The same cache contents, state and output as
+ * oscar_quant_append(k, v, n_new = 1) followed by oscar_decode_attn(q), in the
+ * decode call's launches: one more CTA per request and KV head writes the new
+ * token, quantises the position that leaves the ring (the append kernel's
+ * arithmetic, so the same bytes) and attends over it, while the other CTAs
+ * attend over the rest; the state is published by the call's last launch.
+ * q: DEVICE bf16 [batch][num_q_heads][128]; k, v: DEVICE bf16
+ * [batch][num_kv_heads][128]; o: DEVICE float32 [batch][num_q_heads][128];
+ * state: DEVICE [batch], read and updated as by oscar_quant_append. With k or v
+ * not 16-byte aligned the call runs oscar_quant_append, then oscar_decode_attn.
+ * A decode step may use one INT2 split fewer than oscar_decode_attn (its
+ * append CTAs take their place in the wave). Statuses as for those calls. */
+int oscar_decode_step(oscar_ctx* ctx, const int32_t* page_table, oscar_seq_state* state, const void* q,
+                      const void* k, const void* v, float* o, int32_t batch, void* stream);
+
 /* One serving step with host-side inputs and output: every request gets one
  * new token, written to the cache, then one decode query over the cache that
  * now holds it ([ES] "El sistema de servicio": the new K / V enter the BF16
@@ -233,9 +252,9 @@ int oscar_decode_attn_shared_prefix(oscar_ctx* ctx, const void* q, const int32_t
  * ring and INT2 history).
  * h_qkv: HOST bf16, q [batch][num_q_heads][128], then k and v
  * [batch][num_kv_heads][128] each, back to back. h_o: HOST float32
- * [batch][num_q_heads][128], written. On `stream`: oscar_quant_append(k, v,
- * n_new = 1), then oscar_decode_attn(q) into the output; asynchronous, h_o
- * holds the result once the stream has passed the call.
+ * [batch][num_q_heads][128], written. On `stream`: oscar_decode_step(q, k, v)
+ * into the output; asynchronous, h_o holds the result once the stream has
+ * passed the call.
  * Page-locked host memory (cudaHostAlloc / cudaHostRegister) is read and
  * written by the kernels in place over the host-device link: then d_qkv and o
  * are not used and may be NULL. Other host memory goes through copies: h_qkv

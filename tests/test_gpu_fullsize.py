@@ -144,31 +144,52 @@ def clone_request(layer, src, dst):
 # ---------------------------------------------------------------------------
 
 def test_fullsize_qwen3_8b_bs1_32k():
-    # the workload's 100 decode steps, each appending one token (which evicts the
-    # oldest recent token into INT2) before decoding; outputs of every KV head
-    # checked at steps 0, 50 and 99
+    # the workload's 100 decode steps as the benchmark runs them (oscar_decode_step:
+    # one token appended, which evicts the oldest recent token into INT2, and the
+    # decode query, in the same launches), next to a twin layer that takes the
+    # same steps as quant_append (traced) + decode_attn: the step's cache must
+    # equal the twin's byte for byte, the twin's evicted codes are checked against
+    # the oracle through its trace, and the step's outputs of every KV head against
+    # the oracle at steps 0, 50 and 99
     spec = WORKLOADS["qwen3_8b_bs1_32k"]
     n, steps = spec.context, spec.decode_steps
     assert steps == 100
     layer = spec_layer(spec, 1, n + steps + 16)
+    twin = spec_layer(spec, 1, n + steps + 16)
     trace = layer.new_trace(n + steps)
     populate(layer, 0, n, 10_000, trace)
+    populate(twin, 0, n, 10_000)
     rng = np.random.default_rng(1)
     check_sampled_int2(layer, 0, trace, rng)
     check_window(layer, 0)
     for step in range(steps):
         k, v = draw_kv(layer.seed, 100 + step, 1, layer.hkv, D, layer.spikes)
-        layer.append(0, k.view(1, layer.hkv, D), v.view(1, layer.hkv, D), trace)
         q = draw_queries(layer.seed, 100 + step, 1, layer.hq, layer.hkv, D)
-        o = decode_rows(layer, q, 0)
+        layer.append(0, k.view(1, layer.hkv, D), v.view(1, layer.hkv, D), trace)
+        o_two = decode_rows(layer, q, 0)
+        twin.cache.reserve(0, twin.len[0] + 1)
+        o = torch.full((1, twin.hq, D), float("nan"), device=twin.device)
+        twin.ctx.decode_step(twin.cache.page_table, twin.cache.state, q.to(torch.bfloat16).to(twin.device),
+                             k.view(1, twin.hkv, D).to(torch.bfloat16).to(twin.device),
+                             v.view(1, twin.hkv, D).to(torch.bfloat16).to(twin.device), o, 1)
+        torch.cuda.synchronize()
+        twin._record(0, k.view(1, twin.hkv, D), v.view(1, twin.hkv, D))
+        o = o.cpu().numpy()
         assert np.isfinite(o).all(), step
+        assert rel_l2(o, o_two) <= REL_L2, step
         if step in (0, 50, 99):
-            check_sampled_decode(layer, q, o, [(0, h) for h in range(layer.hkv)])
+            check_sampled_decode(twin, q, o, [(0, h) for h in range(twin.hkv)])
     assert (layer.len[0], layer.e[0]) == (n + steps, n + steps - spec.recent)
-    # the tokens the steps evicted into INT2
-    check_int2(layer, 0, trace, n - spec.recent, layer.e[0])
+    assert tuple(twin.device_state()[0][:2]) == (n + steps, n + steps - spec.recent)
+    # the tokens the steps evicted into INT2: the twin's against the oracle, the
+    # step's against the twin's
+    lo, hi = n - spec.recent, layer.e[0]
+    check_int2(layer, 0, trace, lo, hi)
+    for x, y in zip(layer.int2_codes(0, lo, hi), twin.int2_codes(0, lo, hi)):
+        assert np.array_equal(np.ascontiguousarray(x).view(np.uint8), np.ascontiguousarray(y).view(np.uint8))
     check_window(layer, 0)
-    assert layer.ctx.error_flags() == 0
+    check_window(twin, 0)
+    assert layer.ctx.error_flags() == 0 and twin.ctx.error_flags() == 0
 
 
 # ---------------------------------------------------------------------------

@@ -1,6 +1,7 @@
 """oscar_decode_step_host (one serving step with host-side inputs and output)
-against the same step made of oscar_quant_append + oscar_decode_attn on device
-tensors: bit-identical outputs and states over steps that evict through the
+against the same step on device tensors (oscar_decode_step, or, for inputs that
+are not 16-byte aligned, oscar_quant_append + oscar_decode_attn, which the step
+then runs): bit-identical outputs and states over steps that evict through the
 ring and cross page boundaries, with page-locked host buffers (read and written
 by the kernels in place) and with pageable ones (copied through the staging
 buffer), the resulting cache against the float64 oracle, and the argument
@@ -34,9 +35,10 @@ def _vp(t, offset=0):
 @pytest.mark.parametrize("group,pinned,fold_rv,offset",
                          [(32, True, 0, 0), (64, True, 0, 0), (32, False, 0, 0), (32, True, 1, 0),
                           (64, True, 0, 2)])
-def test_step_host_matches_separate_calls(group, pinned, fold_rv, offset):
+def test_step_host_matches_device_step(group, pinned, fold_rv, offset):
     """offset: bytes the inputs start after a 16-byte boundary of the page-locked
-    buffer (2: the append reads them with plain loads instead of 16-byte copies)."""
+    buffer (2: the step runs the append kernel, which reads them with plain
+    loads, then the decode)."""
     bsz, hq, hkv = 3, 16, 4
     a = Layer(hq, hkv, 4, 64, bsz, 1400, seed=21, group=group, fold_rv=fold_rv)
     b = Layer(hq, hkv, 4, 64, bsz, 1400, seed=21, group=group, fold_rv=fold_rv)
@@ -62,8 +64,11 @@ def test_step_host_matches_separate_calls(group, pinned, fold_rv, offset):
         qd = q.to(torch.bfloat16).to(dev).contiguous()
         kd = k.to(torch.bfloat16).reshape(bsz, 1, hkv, D).to(dev).contiguous()
         vd = v.to(torch.bfloat16).reshape(bsz, 1, hkv, D).to(dev).contiguous()
-        a.ctx.quant_append(a.cache.page_table, a.cache.state, kd, vd, bsz, 1)
-        a.ctx.decode_attn(qd, a.cache.page_table, a.cache.state, o_a, bsz)
+        if offset % 16 == 0:
+            a.ctx.decode_step(a.cache.page_table, a.cache.state, qd, kd, vd, o_a, bsz)
+        else:
+            a.ctx.quant_append(a.cache.page_table, a.cache.state, kd, vd, bsz, 1)
+            a.ctx.decode_attn(qd, a.cache.page_table, a.cache.state, o_a, bsz)
         h_qkv = torch.cat([qd.reshape(-1), kd.reshape(-1), vd.reshape(-1)]).cpu()
         if pinned:
             pad = offset // 2
