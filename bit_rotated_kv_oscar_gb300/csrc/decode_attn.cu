@@ -311,8 +311,10 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
 // every tile, V^T as the row operand (fp16 after a conversion that is exact for
 // values of magnitude 2^-14 .. 65504) and the fp16 probabilities as the column
 // operand, as in the INT2 value product.
+// newrow: with STEP, threads 0-15 / 16-31 hold 16-byte pieces of the step's new
+// K / V row, loaded before the kernel's wait
 template <bool STEP>
-__device__ void window_attention(const DecodeParams& p, int b, int h, int chunk, uint8_t* smem) {
+__device__ void window_attention(const DecodeParams& p, int b, int h, int chunk, uint8_t* smem, uint4 newrow) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int g = p.gqa, S = p.sink, W = p.recent;
@@ -347,20 +349,24 @@ __device__ void window_attention(const DecodeParams& p, int b, int h, int chunk,
   const size_t wrow = ok ? (size_t)st.window_row : 0;
   const __nv_bfloat16* wk = p.window + ((wrow * p.num_kv_heads + h) * 2 + 0) * slots * kHeadDim;
   const __nv_bfloat16* wv = p.window + ((wrow * p.num_kv_heads + h) * 2 + 1) * slots * kHeadDim;
-  const size_t in_off = ((size_t)b * p.num_kv_heads + h) * kHeadDim;
 
   for (int idx = tid; idx < ntiles * 16 * 16; idx += kThreads) {
     const int r = idx >> 4, u = idx & 15, t = t0 + r;
     const bool in = r < n;
     const int pos = t < ns ? t : rb + t - ns;
+    if (STEP && in && pos == newpos) continue;  // the new token's row comes from registers (below)
     const int slot = !in ? 0 : (t < ns ? t : S + pos % W);
-    const bool fresh = STEP && in && pos == newpos;
-    const __nv_bfloat16* ksrc = fresh ? p.step_k + in_off : wk + (size_t)slot * kHeadDim;
-    const __nv_bfloat16* vsrc = fresh ? p.step_v + in_off : wv + (size_t)slot * kHeadDim;
-    cp_async16_s((uint32_t)__cvta_generic_to_shared(krows + r * kWinRow + 8 * u), ksrc + 8 * u, in ? 16u : 0u);
-    cp_async16_s((uint32_t)__cvta_generic_to_shared(vrows + r * kWinRow + 8 * u), vsrc + 8 * u, in ? 16u : 0u);
+    cp_async16_s((uint32_t)__cvta_generic_to_shared(krows + r * kWinRow + 8 * u), wk + (size_t)slot * kHeadDim + 8 * u,
+                 in ? 16u : 0u);
+    cp_async16_s((uint32_t)__cvta_generic_to_shared(vrows + r * kWinRow + 8 * u), wv + (size_t)slot * kHeadDim + 8 * u,
+                 in ? 16u : 0u);
   }
   cp_commit();
+  if (STEP && newpos >= 0 && tid < 32) {
+    // window token index of position L: in the sink, or after the sink in the ring
+    const int r = (newpos < S ? newpos : ns + (newpos - rb)) - t0;
+    if (r >= 0 && r < n) *reinterpret_cast<uint4*>(((tid >> 4) ? vrows : krows) + r * kWinRow + 8 * (tid & 15)) = newrow;
+  }
   // the raw query heads of this KV head (element loads: q needs no alignment
   // beyond its element size); heads past g are zero
   for (int i = tid; i < kMaxGqa * kHeadDim; i += kThreads) {
@@ -1005,9 +1011,11 @@ __device__ void step_append(const DecodeParams& p, int h, int b, uint8_t* smem) 
   __half(*meta)[kGroups][2] = reinterpret_cast<__half(*)[kGroups][2]>(codes + 2);
   const size_t rmat = (size_t)h * kHeadDim * kHeadDim;
 
-  // constant data and the caller's q before the wait: R_K staged, R_V into the
-  // level-2 cache, q~ = q R_K * scale * log2(e) (thread (half, c) sums 64 rows)
+  // constant data and the caller's q, k, v before the wait: R_K staged, R_V into
+  // the level-2 cache, this thread's element of the new K / V row, q~ = q R_K *
+  // scale * log2(e) (thread (half, c) sums 64 rows)
   stage_matrix(Rs, p.R_K + rmat, tid, kThreads);
+  const __nv_bfloat16 xin = ((kind ? p.step_v : p.step_k) + ((size_t)b * Hkv + h) * kHeadDim)[c];
   if (tid == 0 && !p.fold_rv)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p.R_V + rmat), "r"(kHeadDim * kHeadDim * 4)
                  : "memory");
@@ -1068,15 +1076,14 @@ __device__ void step_append(const DecodeParams& p, int h, int b, uint8_t* smem) 
   const size_t slots = (size_t)(S + W);
   const size_t wrow = ok ? (size_t)st.window_row : 0;
   __nv_bfloat16* win = p.step_window + ((wrow * Hkv + h) * 2 + kind) * slots * kHeadDim;
-  const __nv_bfloat16* in = (kind ? p.step_v : p.step_k) + ((size_t)b * Hkv + h) * kHeadDim;
   int page = -1;
   if (qpos >= 0) {
-    xs[kind * kHeadDim + c] = __bfloat162float(from_ring ? win[(size_t)(S + qpos % W) * kHeadDim + c] : in[c]);
+    xs[kind * kHeadDim + c] = __bfloat162float(from_ring ? win[(size_t)(S + qpos % W) * kHeadDim + c] : xin);
     const int pidx = qpos / kPage;
     page = pidx < p.pt_stride ? p.page_table[(size_t)b * p.pt_stride + pidx] : -1;
   }
   __syncthreads();  // the entry the new token evicts is read before the window write
-  if (wslot >= 0) win[(size_t)wslot * kHeadDim + c] = in[c];
+  if (wslot >= 0) win[(size_t)wslot * kHeadDim + c] = xin;
 
   const int nslot = total_slots(p);
   float* part = p.part + (((size_t)b * Hkv + h) * nslot + nslot - 1) * g * kPartFloats;
@@ -1180,11 +1187,20 @@ __global__ void __launch_bounds__(kThreads, kDecodeCtasPerSm) oscar_decode_kerne
     const float* rvt = p.R_VT + (size_t)h * kHeadDim * kHeadDim;
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(rvt), "r"(kHeadDim * kHeadDim * 4) : "memory");
   }
+  // a decode step's new K / V row (the caller's input) is loaded before the
+  // wait, so that the window CTA holding it does not read it after the wait
+  uint4 newrow = make_uint4(0u, 0u, 0u, 0u);
+  if constexpr (STEP) {
+    if (x < p.win_slots && threadIdx.x < 32) {
+      const size_t off = ((size_t)z * p.num_kv_heads + h) * kHeadDim + 8 * (threadIdx.x & 15);
+      newrow = *reinterpret_cast<const uint4*>(((threadIdx.x >> 4) ? p.step_v : p.step_k) + off);
+    }
+  }
   pdl_wait();  // cache, state and q~ come from earlier kernels
   pdl_trigger();
   const int S = p.sink, W = p.recent, P = p.prefix_tokens;
   if (x < p.win_slots) {
-    window_attention<STEP>(p, z, h, x, smem);
+    window_attention<STEP>(p, z, h, x, smem, newrow);
   } else if (x < p.win_slots + p.prefix_splits) {
     // the shared prefix [S, P) once for requests z pack .. z pack + pack - 1; every
     // one of them must hold [S, P) in INT2

@@ -153,3 +153,68 @@ def test_step_split_counts(splits):
 def test_step_unaligned_inputs_take_the_two_kernel_path():
     ref, stp = _twins(8, 2, 4, 32, 2, 512, seed=49)
     _run(ref, stp, [100, 37], 4, aligned=False)
+
+
+def test_step_statuses():
+    cfg = abi.make_config(8, 2, 4, 64, 2, 64)
+    ctx = abi.Context(cfg)
+    q = torch.zeros(2, 8, D, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(2, 2, D, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros(2, 8, D, device="cuda")
+    pt = torch.zeros(2, 64, dtype=torch.int32, device="cuda")
+    st = torch.zeros(2, 4, dtype=torch.int32, device="cuda")
+    with pytest.raises(abi.OscarError) as e:
+        ctx.decode_step(pt, st, q, kv, kv, o, 2)
+    assert e.value.status == -2          # rotations not loaded
+    eye = np.broadcast_to(np.eye(D, dtype=np.float32), (2, D, D))
+    ctx.load_rotations(eye, eye, np.ones(2, np.float32), np.ones(2, np.float32))
+    with pytest.raises(abi.OscarError) as e:
+        ctx.decode_step(pt, st, q, kv, kv, o, 2)
+    assert e.value.status == -6          # no cache bound
+    from bit_rotated_kv_oscar_gb300.cache import PagedCache
+    PagedCache(ctx, 64, device="cuda")
+    with pytest.raises(abi.OscarError) as e:
+        ctx.decode_step(pt, st, q, kv, kv, o, 3)
+    assert e.value.status == -3          # batch above max_batch
+    with pytest.raises(abi.OscarError) as e:
+        ctx.decode_step(pt, st, q, None, kv, o, 2)
+    assert e.value.status == -1
+    with pytest.raises(abi.OscarError) as e:
+        ctx.decode_step(pt, st, None, kv, kv, o, 2)
+    assert e.value.status == -1
+    torch.cuda.synchronize()
+    assert ctx.error_flags() == 0
+
+
+def test_step_bad_page_id_raises_a_flag_not_a_fault():
+    # a full ring: the step quantises position L - recent = 536 into page 33
+    layer = Layer(8, 2, 4, 64, 1, 1024, seed=53)
+    k, v = layer.draw(600)
+    layer.append(0, k, v)
+    assert layer.ctx.error_flags() == 0
+    layer.cache.reserve(0, 601)
+    layer.cache.page_table[0, 33] = 10 ** 6
+    k1, v1 = layer.draw(1)
+    q = layer.queries(1, 4).to(torch.bfloat16).cuda()
+    o = torch.full((1, 8, D), float("nan"), device="cuda")
+    layer.ctx.decode_step(layer.cache.page_table, layer.cache.state, q, k1.to(torch.bfloat16).cuda(),
+                          v1.to(torch.bfloat16).cuda(), o, 1)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all()
+    assert layer.ctx.error_flags() & abi.FLAG_BAD_PAGE_ID
+    assert tuple(layer.device_state()[0][:2]) == (601, 537)
+
+
+def test_step_bad_state_raises_a_flag():
+    layer = Layer(8, 2, 4, 64, 1, 1024, seed=54)
+    k, v = layer.draw(300)
+    layer.append(0, k, v)
+    layer.cache.state[0] = torch.tensor([300, 2, 0, 0], dtype=torch.int32)  # int2_end below the sink
+    q = layer.queries(1, 5).to(torch.bfloat16).cuda()
+    o = torch.full((1, 8, D), float("nan"), device="cuda")
+    kd = k[:1].to(torch.bfloat16).cuda()
+    layer.ctx.decode_step(layer.cache.page_table, layer.cache.state, q, kd, kd, o, 1)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0)
+    assert layer.ctx.error_flags() & abi.FLAG_BAD_STATE
+    assert tuple(layer.device_state()[0][:2]) == (300, 2)
