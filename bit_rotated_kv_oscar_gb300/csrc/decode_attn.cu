@@ -1275,7 +1275,6 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
   const float* part = p.part + ((size_t)b * p.num_kv_heads + h) * nslots * g * kPartFloats;
   pdl_wait();  // the partials come from the decode kernel
   pdl_trigger();
-  if (p.step_slots && h == 0 && blockIdx.z == 0 && tid == 0) publish_step_state(p, b);
   // warp hh < nh keeps the running maximum and row sum of head hh and writes the
   // round's slot weights; thread (head hh, channel c) keeps the weighted sums of
   // the window and INT2 partials, relative to the running maximum
@@ -1296,6 +1295,8 @@ __global__ void __launch_bounds__(kMergeThreads) oscar_merge_kernel(DecodeParams
       for (int u = lane; u < nh * kChunks16; u += 32) cp_async16(dst + 4 * u, src + 4 * u);
     }
     cp_commit();
+    // while the first round's rows are in flight
+    if (s0 == 0 && p.step_slots && h == 0 && blockIdx.z == 0 && tid == 0) publish_step_state(p, b);
     cp_wait<0>();
     __syncthreads();
     if (warp < nh) {
@@ -1413,13 +1414,14 @@ __global__ void __launch_bounds__(kMergeColsThreads) oscar_merge_cols_kernel(Dec
   const float* part = p.part + (((size_t)b * p.num_kv_heads + h) * nslots * g + m) * kPartFloats;
   pdl_wait();  // the partials come from the decode kernel
   pdl_trigger();
-  if (p.step_slots && h == 0 && blockIdx.z == 0 && tid == 0) publish_step_state(p, b);
   constexpr int kChunks16 = kPartFloats / 4;
   for (int i = tid; i < nslots * kChunks16; i += kMergeColsThreads) {
     const int sl = i / kChunks16, u = i % kChunks16;
     cp_async16(rows + sl * kPartFloats + 4 * u, part + (size_t)sl * g * kPartFloats + 4 * u);
   }
   cp_commit();
+  // while the rows are in flight
+  if (p.step_slots && h == 0 && blockIdx.z == 0 && tid == 0) publish_step_state(p, b);
   cp_wait<0>();
   __syncthreads();
   if (warp == 0) {
