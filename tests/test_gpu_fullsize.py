@@ -246,6 +246,29 @@ def test_fullsize_qwen3_32b_bs28_100k():
     # a copied request reads the same cache as request 0 through other pages
     caches = {h: oracle_head(layer, 0, h) for h in heads}
     check_sampled_decode(layer, q, o, [(b, h) for b in (5, 20) for h in heads], caches=caches)
+    del caches
+    # one decode step of all 28 requests through oscar_decode_step, the launch
+    # configuration the benchmark times at this size (the step's append CTAs
+    # beside the splits): every request's ring entry goes to INT2
+    k1, v1 = draw_kv(layer.seed, 50_000, B, layer.hkv, D, layer.spikes)
+    q1 = draw_queries(layer.seed, 4, B, layer.hq, layer.hkv, D)
+    for b in range(B):
+        layer.cache.reserve(b, layer.len[b] + 1, upload=False)
+    layer.cache.upload()
+    dev = layer.device
+    o1 = torch.full((B, layer.hq, D), float("nan"), device=dev)
+    layer.ctx.decode_step(layer.cache.page_table, layer.cache.state, q1.to(torch.bfloat16).to(dev),
+                          k1.to(torch.bfloat16).to(dev).contiguous(), v1.to(torch.bfloat16).to(dev).contiguous(),
+                          o1, B)
+    torch.cuda.synchronize()
+    for b in range(B):
+        layer._record(b, k1[b:b + 1], v1[b:b + 1])
+    o1 = o1.cpu().numpy()
+    assert np.isfinite(o1).all()
+    state = layer.device_state()
+    for b in (0, 20, 27):
+        assert tuple(state[b][:2]) == (layer.len[b], layer.e[b])
+    check_sampled_decode(layer, q1, o1, [(b, h) for b in (0, 20, 27) for h in heads])
     assert layer.ctx.error_flags() == 0
 
 
